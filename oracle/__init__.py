@@ -1,0 +1,140 @@
+"""Oracle for the paged KV-cache hot path -- TEST INFRASTRUCTURE ONLY.
+
+Plain, single-threaded float64 CPU code (``pkv_oracle.c``) that restates what
+the pages define: the slot split and byte-address formula of the cache write
+("vLLM KV Cache Layout 可视化", 核心 / 查一个 token / kernel 那一侧) and textbook
+softmax attention over a sequence's gathered blocks ("deep-dive-into-vllm-05"
+§1.2, §2, §3.2; "vLLM 技术内幕" §2.1).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library and the library never calls it.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` to values the
+pages print, closed forms, invariants and an independent brute force.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile pkv_oracle.c with the host C compiler (portable flags only)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load(path: str | None = None):
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _bind(lib):
+    lib.oracle_half_to_double.restype = ctypes.c_double
+    lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_slot_address.restype = _i64
+    lib.oracle_slot_address.argtypes = [_i64] * 7
+    lib.oracle_split_slot.restype = None
+    lib.oracle_split_slot.argtypes = [_i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+    lib.oracle_cache_write.restype = _i64
+    lib.oracle_cache_write.argtypes = [_p, _i64, _p, _p, _i64] + [_i64] * 7
+    lib.oracle_decode_attention.restype = ctypes.c_int
+    lib.oracle_decode_attention.argtypes = [_p] * 6 + [ctypes.c_double] + [_i64] * 7 + [_p, _i64]
+    return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+# --------------------------------------------------------------------------
+# Python-facing functions.  ``lib`` lets a test run the same calls against a
+# deliberately mutated build of the C source.
+
+
+def half_to_double(bits: int, lib=None) -> float:
+    return (lib or _load()).oracle_half_to_double(int(bits) & 0xFFFF)
+
+
+def split_slot(slot: int, block_size: int, lib=None) -> tuple[int, int]:
+    b, o = _i64(), _i64()
+    (lib or _load()).oracle_split_slot(slot, block_size, ctypes.byref(b), ctypes.byref(o))
+    return b.value, o.value
+
+
+def slot_address(slot: int, block_size: int, offset: int, layer: int, layer_stride: int,
+                 block_stride: int, row_width: int, lib=None) -> int:
+    return (lib or _load()).oracle_slot_address(slot, block_size, offset, layer, layer_stride,
+                                                block_stride, row_width)
+
+
+def cache_write(cache: np.ndarray, src: np.ndarray, slot_mapping: np.ndarray, *, offset: int,
+                layer: int, layer_stride: int, block_stride: int, row_width: int,
+                block_size: int, num_blocks: int, lib=None) -> int:
+    """Scatter rows of ``src`` (uint8 [T, row_width]) into ``cache`` (uint8, in place)."""
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    src = np.ascontiguousarray(src, dtype=np.uint8)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    assert src.size == slots.size * row_width
+    n = (lib or _load()).oracle_cache_write(
+        _ptr(cache), cache.nbytes, _ptr(src), _ptr(slots), slots.size, offset, layer,
+        layer_stride, block_stride, row_width, block_size, num_blocks)
+    if n < 0:
+        raise ValueError(f"oracle_cache_write failed with status {n}")
+    return n
+
+
+def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                     block_tables: np.ndarray, seq_lens: np.ndarray, scale: float, *,
+                     pairs=None, lib=None) -> np.ndarray:
+    """Textbook paged decode attention in float64.
+
+    q: fp16 [S, H, D]; caches: fp16 [NB, bs, Hk, D]; block_tables int32 [S, MB];
+    seq_lens int32 [S].  Returns float64 [S, H, D]; with ``pairs`` (a list of
+    (seq, head)) only those rows are computed (the others are NaN).
+    """
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    assert k_cache.dtype == np.float16 and v_cache.dtype == np.float16
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    S, H, D = q.shape
+    NB, bs, Hk, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    assert bt.shape[0] == S and sl.shape == (S,)
+    out = np.full((S, H, D), np.nan, dtype=np.float64)
+    if pairs is None:
+        pp, npairs = None, 0
+    else:
+        pa = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        pp, npairs = _ptr(pa), pa.shape[0]
+    st = (lib or _load()).oracle_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(sl), float(scale),
+        S, H, Hk, D, bs, bt.shape[1], NB, pp, npairs)
+    if st != 0:
+        raise ValueError(f"oracle_decode_attention failed with status {st}")
+    return out
