@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: the cache write of
+each sequence's new K/V token (pkv_cache_write), then paged decode attention
+over every sequence (pkv_decode_attention: block-table walk, online softmax,
+split-KV with the in-kernel log-sum-exp combine).
+
+Default workload: the Llama-3-8B-shaped decode layer -- 64 sequences, lengths
+uniform in [256, 4096], block_size 16, 32 query / 8 KV heads, head_dim 128,
+fp16 KV cache [16384, 16, 8, 128] from a seeded shuffled free list, one new
+token per sequence.  Synthetic seeded data; the KV cache is resident state.
+
+Prints one JSON line.  `value` is KV-read GB/s of the whole step (key+value
+bytes the decode must read / step time, inputs resident in HBM, L2 flushed
+between timed steps).  `e2e` is the same metric through the public API with
+the step's inputs copied from pinned host memory and the output copied back
+inside the timed region.  `roofline` is the decode kernel's algorithmic bytes
+per launch / its event-timed duration against the measured HBM copy
+bandwidth.  `cpu_baseline` times the float64 oracle on the host.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 2|3|4] [--compute auto|simt|mma]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV-read GB/s (% of HBM peak), seqs/s; cache-write GB/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_NAMES = {
+    2: "llama3-8b decode layer: S=64, L~U[256,4096], bs=16, H=32, Hk=8, D=128, "
+       "fp16 cache [16384,16,8,128], 1 new token/seq written",
+    3: "long context: S=8, L=32768, bs=16, H=32, Hk=8, D=128, 16384 shuffled blocks, decode only",
+    4: "shared prefix: S=256, 2000-token shared prefix + tail U[1,300], bs=16, H=64, Hk=8, "
+       "D=128, 16384 blocks, 1 new token/seq written",
+}
+
+DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_131_gb300", "csrc", f)
+                  for f in ("pkv_decode.cu", "pkv_device.cuh")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_dram_traffic.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
+    ap.add_argument("--compute", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in DECODE_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    rec = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("source_hash") != decode_source_hash():
+        return None
+    v = rec.get(f"traffic_bytes_per_launch.{workload_key}")
+    return float(v) if v else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed loop runs."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[2:]):
+                if p.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- reference arm
+
+
+def oracle_step_sample(wl, k, v, units, orc):
+    """The oracle's write of every new row, then its decode of the sampled
+    (sequence, kv_head) units (all G query heads of each).  Returns the KV
+    bytes the sample reads."""
+    row = wl.num_kv_heads * wl.head_dim * 2
+    if wl.slot_mapping is not None:
+        for cache, new in ((k, wl.k_new), (v, wl.v_new)):
+            orc.cache_write(cache.view(np.uint8).reshape(-1), new.view(np.uint8),
+                            wl.slot_mapping, offset=0, layer=0, layer_stride=0,
+                            block_stride=wl.block_size * row, row_width=row,
+                            block_size=wl.block_size, num_blocks=wl.num_blocks)
+    G = wl.num_heads // wl.num_kv_heads
+    pairs = [(i, kvh * G + g) for i, kvh in units for g in range(G)]
+    orc.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale, pairs=pairs)
+    return sum(int(wl.seq_lens[i]) for i, _ in units) * wl.head_dim * 4
+
+
+class OracleSampler:
+    """Times the float64 oracle on rotating (sequence, kv_head) units."""
+
+    def __init__(self, wl):
+        import oracle as orc
+
+        orc.build()
+        self.orc, self.wl = orc, wl
+        self.k, self.v = wl.k_cache.copy(), wl.v_cache.copy()
+        self.units = [(i, h) for i in range(wl.num_seqs) for h in range(wl.num_kv_heads)]
+        self.pos = 0
+
+    def step(self, n_units):
+        units = [self.units[(self.pos + j) % len(self.units)] for j in range(n_units)]
+        self.pos += n_units
+        t0 = time.perf_counter()
+        nbytes = oracle_step_sample(self.wl, self.k, self.v, units, self.orc)
+        return nbytes, time.perf_counter() - t0
+
+    def calibrate(self) -> float:
+        """Seconds per unit (one sequence's KV head, all its query heads)."""
+        nb, t = self.step(4)
+        return t / 4
+
+    def run(self, n_units, steps=None, budget_s=None):
+        total_b, total_t, n = 0, 0.0, 0
+        while (steps is not None and n < steps) or (budget_s is not None and total_t < budget_s):
+            b, t = self.step(n_units)
+            total_b, total_t, n = total_b + b, total_t + t, n + 1
+        return total_b / total_t / 1e9, total_t, n
+
+
+def run_reference(args, wl, rank):
+    if rank != 0:
+        return
+    sampler = OracleSampler(wl)
+    t_unit = sampler.calibrate()
+    per_step_budget = 90.0 / max(1, args.steps + args.warmup)
+    n_units = max(1, int(per_step_budget / t_unit))
+    sampler.run(n_units, steps=args.warmup)
+    gbs, t, n = sampler.run(n_units, steps=args.steps)
+    sample = (f"{n_units} (sequence, kv_head) units per step, rotating over all "
+              f"{len(sampler.units)}, plus the write of all new rows; single-threaded float64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- our arm
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    from paged_kv_cache_131_gb300 import workloads as W
+
+    wl = W.config(args.config)
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+
+    import torch
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import paged_kv_cache_131_gb300 as pkv
+    from paged_kv_cache_131_gb300 import _build
+    from paged_kv_cache_131_gb300.harness import DeviceDecode, L2Flush
+
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    compute = {"auto": 0, "simt": 1, "mma": 2}[args.compute]
+    dev = DeviceDecode(wl, device=f"cuda:{local}", partition_size=args.partition, compute=compute)
+    flush = L2Flush(f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+
+    kv_bytes = wl.kv_bytes()
+    S, H, D = wl.num_seqs, wl.num_heads, wl.head_dim
+    nblk = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
+    decode_alg_bytes = kv_bytes + S * H * D * 2 * 2 + nblk * 4 + S * 4
+    write_bytes = dev.write_bytes()
+    launches_per_step = (1 if dev.has_write else 0) + 1
+
+    for _ in range(args.warmup):
+        flush()
+        dev.step()
+    torch.cuda.synchronize()
+    kind, idx = pkv.pkv_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error {pkv.DEVICE_ERRORS.get(kind)} at {idx}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            dev.write()
+            ev[i][1].record(stream)
+            dev.decode()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    if dist is not None:
+        t = torch.tensor([step_ms], device=f"cuda:{local}")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+        dist.barrier()
+
+    # end to end through the public API: pinned host inputs in, output out
+    e2e = e2e_measure(dev, wl, args.e2e_steps, stream, flush)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    value = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    achieved = decode_alg_bytes / (decode_ms * 1e-3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSampler(wl)
+        gbs, t_cpu, n_cpu = sampler.run(8, budget_s=15.0)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_cpu} steps x 8 (sequence, kv_head) units (all query heads) + the "
+                         f"write of all new rows, {t_cpu:.1f} s single-threaded float64"}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16xf16->f32",
+        "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
+        "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": S * world,
+                   "seq_len": int(wl.max_seq_len), "parallelism": f"replicas x{world}",
+                   "l2": "flushed (write of 2x L2) between timed steps; KV read 0.5 GB > L2",
+                   "kv_cache": "resident in HBM (state), not copied per step",
+                   "compute": args.compute, "partition_tokens": args.partition or 512},
+        "pct_hbm_peak": round(100 * value / world / peak, 2),
+        "seqs_per_s": round(world * S / (step_ms * 1e-3), 1),
+        "decode_tokens_per_s": round(world * S / (step_ms * 1e-3), 1),
+        "cache_write_gbs": round(write_bytes / (write_ms * 1e-3) / 1e9, 2) if write_bytes else None,
+        "decode_kernel_ms": round(decode_ms, 5),
+        "write_kernel_ms": round(write_ms, 5),
+        "wall_s_timed_loop": round(t_wall, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(f"config{args.config}"),
+                     "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+                     "kernel": "decode_kernel (MMA policy)" if compute != 1 else
+                               "decode_kernel (SIMT policy)",
+                     "alg_bytes_per_launch": decode_alg_bytes},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def e2e_measure(dev, wl, steps, stream, flush):
+    """Same metric through the public API from pinned host buffers: per step the
+    step's inputs (q, new K/V rows, slot_mapping, block tables, seq_lens) go
+    host -> device, the library runs, the output comes back device -> host.
+    L2 is flushed between steps, outside the timed events."""
+    import torch
+
+    host = {
+        "q": torch.from_numpy(wl.q).pin_memory(),
+        "block_tables": torch.from_numpy(wl.block_tables).pin_memory(),
+        "seq_lens": torch.from_numpy(wl.seq_lens).pin_memory(),
+    }
+    if dev.has_write:
+        host["k_new"] = torch.from_numpy(wl.k_new).pin_memory()
+        host["v_new"] = torch.from_numpy(wl.v_new).pin_memory()
+        host["slot_mapping"] = torch.from_numpy(wl.slot_mapping).pin_memory()
+    out_host = torch.empty(tuple(wl.q.shape), dtype=torch.float16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for name, t in host.items():
+            getattr(dev, name).copy_(t, non_blocking=True)
+        dev.step()
+        out_host.copy_(dev.out, non_blocking=True)
+
+    for _ in range(5):
+        flush()
+        one()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        flush()
+        e0.record(stream)
+        one()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    return {"value": round(wl.kv_bytes() / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 5)}
+
+
+if __name__ == "__main__":
+    main()

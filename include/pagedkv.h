@@ -1,0 +1,202 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv, the GB300 (sm_103a) hot path of paged
+ * KV-cache attention: the paged cache write and paged decode attention.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_cache, q, out, k, v, slot_mapping, block_tables,
+ *    seq_lens and workspace are DEVICE pointers owned by the caller; the
+ *    library never allocates, frees or retains them beyond the call.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and never synchronises, except pkv_get_device_error.
+ *  - Every call first validates its arguments on the host; an invalid call
+ *    returns a negative pkv_status and launches nothing.  A failed launch
+ *    returns PKV_ERR_CUDA (pkv_last_error_string() has the CUDA message).
+ *  - Bad DATA found on the device (a slot or block id out of range, a
+ *    sequence longer than its block table) never faults: the offending item
+ *    is skipped and the first one is recorded; read it with
+ *    pkv_get_device_error.
+ *  - fp16 means IEEE binary16 (CUDA __half).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_NULL = -1,        /* a required pointer is NULL                        */
+    PKV_ERR_INVALID = -2,     /* a size, stride or count is out of its domain      */
+    PKV_ERR_UNSUPPORTED = -3, /* valid but not built: head_dim, group size, bs ... */
+    PKV_ERR_ALIGNMENT = -4,   /* a pointer or stride breaks a required alignment   */
+    PKV_ERR_WORKSPACE = -5,   /* split-KV needs a (larger) workspace               */
+    PKV_ERR_CUDA = -6         /* a CUDA runtime call or launch failed              */
+} pkv_status;
+
+/* Kinds recorded by the device-side error word (pkv_get_device_error). */
+typedef enum pkv_device_error {
+    PKV_DEVERR_NONE = 0,
+    PKV_DEVERR_SLOT = 1,     /* slot >= num_blocks*block_size; index = token          */
+    PKV_DEVERR_BLOCK_ID = 2, /* block id outside [0, num_blocks);
+                                index = seq * max_blocks_per_seq + logical block     */
+    PKV_DEVERR_SEQ_LEN = 3,  /* seq_len < 0, or more tokens than the block table or
+                                max_seq_len allow; index = seq                         */
+    PKV_DEVERR_TIMEOUT = 4   /* a staging wait gave up (about 2 s); index = CTA id   */
+} pkv_device_error;
+
+/*
+ * One cache view ("vLLM KV Cache Layout 可视化" -- 核心, KVCacheTensor): a
+ * group of same-shaped layers inside one byte allocation.  The byte address
+ * of slot `s` of layer `layer` is
+ *     offset + layer*layer_stride + (s / block_size)*block_stride
+ *            + (s % block_size)*row_width.
+ * Layer-outer layouts (LBHNC, LBNHC) have block_stride = page and
+ * layer_stride = page*num_blocks; block-outer layouts (BLHNC, BLNHC, BHLNC)
+ * have layer_stride = page and block_stride = the bytes of one whole block
+ * (page = block_size*row_width) ("layout 是什么").
+ */
+typedef struct pkv_view {
+    int64_t offset;       /* bytes from the cache pointer to layer 0, block 0   */
+    int64_t layer_stride; /* bytes between the same block of adjacent layers    */
+    int64_t block_stride; /* bytes between adjacent physical blocks of a layer  */
+    int64_t row_width;    /* bytes of one token row (one slot)                  */
+    int32_t layer;        /* the layer this call writes                         */
+} pkv_view;
+
+/*
+ * Paged KV-cache write ("vLLM KV Cache Layout 可视化" -- 查一个 token and
+ * kernel 那一侧; "deep-dive-into-vllm-05" §2: prefill writes many slots,
+ * decode appends one per sequence).
+ *
+ * For every token t in [0, num_tokens): slot = slot_mapping[t] is split back
+ * into block = slot / block_size and position = slot % block_size, and the
+ * row_width bytes at k + t*row_width are copied to
+ *     k_cache + offset + layer*layer_stride + block*block_stride
+ *             + position*row_width
+ * (and likewise v -> v_cache, at the same address, when v != NULL).
+ *
+ *  k, v          device, num_tokens rows of view.row_width bytes, contiguous.
+ *                v may be NULL (single-cache write); then v_cache must be NULL.
+ *  slot_mapping  device int64 [num_tokens].  A negative slot is padding and is
+ *                skipped.  slot >= num_blocks*block_size is skipped and
+ *                recorded (PKV_DEVERR_SLOT).  Two tokens with the same slot
+ *                in one call: which row lands is unspecified.
+ *  k_cache, v_cache  device byte allocations holding the view; the caller
+ *                guarantees every slot in [0, num_blocks*block_size) of the
+ *                view lies inside them.  Bytes no token addresses are not
+ *                touched.
+ *  Rows are copied byte for byte (no conversion); 16-byte vectors are used
+ *  when every address and stride allows, else 8, 4, 2 or 1 byte.
+ *  Returns PKV_OK (num_tokens == 0 launches nothing), PKV_ERR_NULL,
+ *  PKV_ERR_INVALID (block_size <= 0, num_blocks <= 0, row_width <= 0,
+ *  block_stride <= 0, offset/layer/layer_stride < 0), PKV_ERR_CUDA.
+ */
+int pkv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
+                    int64_t num_tokens, void *k_cache, void *v_cache, pkv_view view,
+                    int32_t block_size, int64_t num_blocks, pkv_stream_t stream);
+
+/*
+ * Paged decode attention ("deep-dive-into-vllm-05" §2 read loop and §3.2
+ * GQA; "vLLM 技术内幕" §2.1: the query is dotted with the keys of each
+ * physical block in turn and values are accumulated block by block).
+ *
+ * For sequence i (length L = seq_lens[i]) and query head h, with G =
+ * num_heads/num_kv_heads and kv = h / G (consecutive heads share a KV head):
+ *     s_j  = scale * q[i,h,:] . K_j,   K_j = k_cache[bt[i, j/bs], j%bs, kv, :]
+ *     out[i,h,:] = sum_j exp(s_j - max s) V_j / sum_j exp(s_j - max s),
+ * j in [0, L).  Computed block by block with an online (running max / sum)
+ * softmax in fp32; sequences longer than one partition (512 tokens) are
+ * split into partitions whose partial (max, sum, weighted values) are merged
+ * with a log-sum-exp rescale inside the same launch.  L == 0 gives zeros.
+ *
+ *  out           device fp16 [num_seqs, num_heads, head_dim] (written).
+ *  q             device fp16 [num_seqs, num_heads, head_dim].
+ *  k_cache, v_cache  device fp16 [num_blocks, block_size, num_kv_heads,
+ *                head_dim] ("deep-dive-into-vllm-05" §1.2), 16-byte aligned.
+ *  block_tables  device int32 [num_seqs, max_blocks_per_seq]; entries past a
+ *                sequence's ceil(L/block_size) blocks are never read.  An id
+ *                outside [0, num_blocks) is skipped and recorded.
+ *  seq_lens      device int32 [num_seqs].
+ *  max_seq_len   host hint: an upper bound of seq_lens; it fixes the number of
+ *                partitions P = ceil(max_seq_len / 512).  A longer sequence is
+ *                truncated and recorded (PKV_DEVERR_SEQ_LEN).
+ *  workspace     device scratch of at least pkv_decode_workspace_bytes(...)
+ *                bytes, 16-byte aligned, needed only when P > 1 (else may be
+ *                NULL).  It must be zero-filled before its first use (e.g. by
+ *                pkv_decode_workspace_init); every call leaves it zero-filled
+ *                again.  Calls that share a workspace must not overlap.
+ *  Supported: head_dim in {64, 128}; G in {1, 2, 4, 8}; block_size == 16.
+ *  Returns PKV_OK (num_seqs == 0 launches nothing), PKV_ERR_NULL,
+ *  PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_ALIGNMENT,
+ *  PKV_ERR_WORKSPACE, PKV_ERR_CUDA.
+ */
+int pkv_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *seq_lens, float scale,
+                         int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int32_t num_seqs, int32_t max_blocks_per_seq,
+                         int32_t max_seq_len, int64_t num_blocks, void *workspace,
+                         size_t workspace_bytes, pkv_stream_t stream);
+
+/* How the per-block arithmetic of pkv_decode_attention_ex runs. */
+typedef enum pkv_compute {
+    PKV_COMPUTE_AUTO = 0, /* the measured-fastest path for the shape            */
+    PKV_COMPUTE_SIMT = 1, /* fp32 FMA on CUDA cores, warp-shuffle reductions    */
+    PKV_COMPUTE_MMA = 2   /* the GQA group packed into 16x8x16 fp16 MMAs, fp32
+                             accumulate                                          */
+} pkv_compute;
+
+typedef struct pkv_decode_options {
+    int32_t partition_size; /* tokens per split-KV partition, a multiple of
+                               block_size in [16, 8192]; 0 = 512            */
+    int32_t compute;        /* a pkv_compute value                           */
+} pkv_decode_options;
+
+/* pkv_decode_attention with explicit options (opts may be NULL = defaults).
+ * The number of partitions is ceil(max_seq_len / partition_size). */
+int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens, float scale,
+                            int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_seqs, int32_t max_blocks_per_seq,
+                            int32_t max_seq_len, int64_t num_blocks, void *workspace,
+                            size_t workspace_bytes, const pkv_decode_options *opts,
+                            pkv_stream_t stream);
+
+/* Workspace bytes pkv_decode_attention needs (0 when max_seq_len <= 512). */
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                  int32_t max_seq_len);
+
+/* Same for a given partition size (0 = 512). */
+size_t pkv_decode_workspace_bytes_ex(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                     int32_t max_seq_len, int32_t partition_size);
+
+/* Zero-fill a workspace on `stream` (cudaMemsetAsync). */
+int pkv_decode_workspace_init(void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device-side error record of
+ * the current device: *kind receives a pkv_device_error value (0 = none) and
+ * *index its index (-1 when none).  Either pointer may be NULL.
+ */
+int pkv_get_device_error(int32_t *kind, int64_t *index, pkv_stream_t stream);
+
+/* Static text for a pkv_status value. */
+const char *pkv_status_string(int status);
+
+/* Text of the last CUDA error a call of this thread returned PKV_ERR_CUDA for. */
+const char *pkv_last_error_string(void);
+
+/* ABI version of this header (major*10000 + minor*100 + patch). */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

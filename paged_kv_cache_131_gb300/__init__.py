@@ -1,0 +1,215 @@
+"""libpagedkv -- paged KV-cache write and paged decode attention for GB300.
+
+Python binding of the C ABI in ``include/pagedkv.h``: every function here has
+the C entry point's name and only marshals arguments (torch tensors -> device
+pointers, shapes -> sizes, the current torch stream -> cudaStream_t).  All of
+the work runs in the CUDA kernels of ``libpagedkv.so``; there is no other
+implementation behind these names.  Build the library with
+``paged_kv_cache_131_gb300._build.build()`` (or ``__graft_entry__.build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "PkvError", "pkv_view", "pkv_decode_options", "library_path", "load",
+    "pkv_cache_write", "pkv_decode_attention", "pkv_decode_workspace_bytes",
+    "pkv_decode_workspace_init", "pkv_get_device_error", "pkv_status_string",
+    "pkv_last_error_string", "pkv_version", "EXPORTED_SYMBOLS",
+    "PKV_COMPUTE_AUTO", "PKV_COMPUTE_SIMT", "PKV_COMPUTE_MMA", "DEVICE_ERRORS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libpagedkv.so")
+
+PKV_COMPUTE_AUTO, PKV_COMPUTE_SIMT, PKV_COMPUTE_MMA = 0, 1, 2
+DEVICE_ERRORS = {0: "none", 1: "slot", 2: "block_id", 3: "seq_len", 4: "timeout"}
+
+EXPORTED_SYMBOLS = [
+    "pkv_cache_write", "pkv_decode_attention", "pkv_decode_attention_ex",
+    "pkv_decode_workspace_bytes", "pkv_decode_workspace_bytes_ex", "pkv_decode_workspace_init",
+    "pkv_get_device_error", "pkv_status_string", "pkv_last_error_string", "pkv_version",
+]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = pkv_status_string(status)
+        if status == -6:
+            msg += f" [{pkv_last_error_string()}]"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+class pkv_view(ctypes.Structure):
+    _fields_ = [("offset", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
+                ("block_stride", ctypes.c_int64), ("row_width", ctypes.c_int64),
+                ("layer", ctypes.c_int32)]
+
+
+class pkv_decode_options(ctypes.Structure):
+    _fields_ = [("partition_size", ctypes.c_int32), ("compute", ctypes.c_int32)]
+
+
+_lib = None
+_i32, _i64, _p, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+
+
+def load(path: str | None = None):
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or library_path
+    if not os.path.exists(path):
+        raise ImportError(f"libpagedkv.so is not built ({path}); run "
+                          "paged_kv_cache_131_gb300._build.build()")
+    lib = ctypes.CDLL(path)
+    lib.pkv_cache_write.restype = ctypes.c_int
+    lib.pkv_cache_write.argtypes = [_p, _p, _p, _i64, _p, _p, pkv_view, _i32, _i64, _p]
+    dec = [_p, _p, _p, _p, _p, _p, ctypes.c_float, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+           _i64, _p, _sz]
+    lib.pkv_decode_attention.restype = ctypes.c_int
+    lib.pkv_decode_attention.argtypes = dec + [_p]
+    lib.pkv_decode_attention_ex.restype = ctypes.c_int
+    lib.pkv_decode_attention_ex.argtypes = dec + [ctypes.POINTER(pkv_decode_options), _p]
+    lib.pkv_decode_workspace_bytes.restype = _sz
+    lib.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32]
+    lib.pkv_decode_workspace_bytes_ex.restype = _sz
+    lib.pkv_decode_workspace_bytes_ex.argtypes = [_i32, _i32, _i32, _i32, _i32]
+    lib.pkv_decode_workspace_init.restype = ctypes.c_int
+    lib.pkv_decode_workspace_init.argtypes = [_p, _sz, _p]
+    lib.pkv_get_device_error.restype = ctypes.c_int
+    lib.pkv_get_device_error.argtypes = [ctypes.POINTER(_i32), ctypes.POINTER(_i64), _p]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_last_error_string.restype = ctypes.c_char_p
+    lib.pkv_last_error_string.argtypes = []
+    lib.pkv_version.restype = ctypes.c_int
+    lib.pkv_version.argtypes = []
+    if path == library_path:
+        _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------------ marshalling
+
+
+def _dev(t, name, dtype=None):
+    """Device pointer of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _check(status: int, where: str) -> int:
+    if status != 0:
+        raise PkvError(status, where)
+    return status
+
+
+def pkv_cache_write(k, v, slot_mapping, k_cache, v_cache, view, block_size: int,
+                    num_blocks: int, stream=None, check: bool = True) -> int:
+    """Scatter ``k`` (and ``v``) rows to their slots: see pkv_cache_write in pagedkv.h.
+
+    k, v: CUDA tensors of num_tokens rows of ``view.row_width`` bytes; slot_mapping:
+    CUDA int64 [num_tokens]; caches: CUDA tensors (any dtype, used as bytes);
+    view: pkv_view or an object with offset/layer_stride/block_stride/row_width
+    (and optionally layer).
+    """
+    import torch
+    if not isinstance(view, pkv_view):
+        view = pkv_view(view.offset, view.layer_stride, view.block_stride, view.row_width,
+                        getattr(view, "layer", 0))
+    n = slot_mapping.numel()
+    if k.numel() * k.element_size() != n * view.row_width:
+        raise ValueError("k must hold num_tokens rows of view.row_width bytes")
+    if v is not None and v.numel() * v.element_size() != n * view.row_width:
+        raise ValueError("v must hold num_tokens rows of view.row_width bytes")
+    st = load().pkv_cache_write(
+        _dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int64), n,
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), view, block_size, num_blocks,
+        _stream(stream))
+    return _check(st, "pkv_cache_write") if check else st
+
+
+def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float,
+                         num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                         max_seq_len: int, num_blocks: int, workspace=None, stream=None,
+                         partition_size: int = 0, compute: int = PKV_COMPUTE_AUTO,
+                         check: bool = True) -> int:
+    """Paged decode attention: see pkv_decode_attention(_ex) in pagedkv.h.
+
+    out, q: CUDA fp16 [S, H, D]; caches: CUDA fp16 [NB, bs, Hk, D];
+    block_tables: CUDA int32 [S, MB]; seq_lens: CUDA int32 [S];
+    workspace: CUDA uint8 tensor (zero-filled before first use) or None.
+    """
+    import torch
+    S = q.shape[0]
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    args = (_dev(out, "out", torch.float16), _dev(q, "q", torch.float16),
+            _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16),
+            _dev(block_tables, "block_tables", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+            float(scale), num_heads, num_kv_heads, head_dim, block_size, S,
+            block_tables.shape[1] if block_tables.dim() == 2 else 0, int(max_seq_len),
+            int(num_blocks), ws_ptr, ws_bytes)
+    lib = load()
+    if partition_size == 0 and compute == PKV_COMPUTE_AUTO:
+        st = lib.pkv_decode_attention(*args, _stream(stream))
+    else:
+        opts = pkv_decode_options(partition_size, compute)
+        st = lib.pkv_decode_attention_ex(*args, ctypes.byref(opts), _stream(stream))
+    return _check(st, "pkv_decode_attention") if check else st
+
+
+def pkv_decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_seq_len: int,
+                               partition_size: int = 0) -> int:
+    return int(load().pkv_decode_workspace_bytes_ex(num_seqs, num_heads, head_dim, max_seq_len,
+                                                    partition_size))
+
+
+def pkv_decode_workspace_init(workspace, stream=None) -> int:
+    if workspace is None:
+        return 0
+    return _check(load().pkv_decode_workspace_init(
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "pkv_decode_workspace_init")
+
+
+def pkv_get_device_error(stream=None) -> tuple[int, int]:
+    """Synchronise ``stream``; return and clear (kind, index) of the device error record."""
+    kind, index = _i32(0), _i64(-1)
+    _check(load().pkv_get_device_error(ctypes.byref(kind), ctypes.byref(index), _stream(stream)),
+           "pkv_get_device_error")
+    return kind.value, index.value
+
+
+def pkv_status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()
+
+
+def pkv_last_error_string() -> str:
+    return load().pkv_last_error_string().decode()
+
+
+def pkv_version() -> int:
+    return load().pkv_version()

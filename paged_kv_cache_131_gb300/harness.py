@@ -1,0 +1,125 @@
+"""Device staging of the synthetic workloads, for the benchmark and the tests.
+
+Copies a ``workloads.DecodeWorkload`` / ``WriteWorkload`` into CUDA tensors
+and runs the library's calls on them.  Torch is used for device memory and
+streams only; every computation runs in libpagedkv's kernels.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (PKV_COMPUTE_AUTO, pkv_cache_write, pkv_decode_attention,
+               pkv_decode_workspace_bytes, pkv_view)
+from .workloads import DecodeWorkload, WriteWorkload
+
+
+def to_dev(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class DeviceDecode:
+    """One decode workload resident on the device: caches, tables, q, out, workspace."""
+
+    def __init__(self, wl: DecodeWorkload, device="cuda", partition_size: int = 0,
+                 compute: int = PKV_COMPUTE_AUTO):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.partition_size = partition_size
+        self.compute = compute
+        self.q = to_dev(wl.q, device)
+        self.k_cache = to_dev(wl.k_cache, device)
+        self.v_cache = to_dev(wl.v_cache, device)
+        self.block_tables = to_dev(wl.block_tables, device)
+        self.seq_lens = to_dev(wl.seq_lens, device)
+        self.out = torch.empty_like(self.q)
+        self.has_write = wl.slot_mapping is not None and wl.slot_mapping.size > 0
+        if self.has_write:
+            self.k_new = to_dev(wl.k_new, device)
+            self.v_new = to_dev(wl.v_new, device)
+            self.slot_mapping = to_dev(wl.slot_mapping, device)
+        nbytes = pkv_decode_workspace_bytes(wl.num_seqs, wl.num_heads, wl.head_dim,
+                                            wl.max_seq_len, partition_size)
+        # zero-filled once; every decode call leaves its tickets at zero again
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device) \
+            if nbytes else None
+
+    @property
+    def row_bytes(self) -> int:
+        return self.wl.num_kv_heads * self.wl.head_dim * 2
+
+    def view(self) -> pkv_view:
+        r = self.row_bytes
+        return pkv_view(0, 0, self.wl.block_size * r, r, 0)
+
+    def write(self, stream=None) -> None:
+        if self.has_write:
+            pkv_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache,
+                            self.v_cache, self.view(), self.wl.block_size, self.wl.num_blocks,
+                            stream=stream)
+
+    def decode(self, stream=None, out=None) -> torch.Tensor:
+        wl = self.wl
+        out = self.out if out is None else out
+        pkv_decode_attention(out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                             self.seq_lens, wl.scale, wl.num_heads, wl.num_kv_heads,
+                             wl.head_dim, wl.block_size, wl.max_seq_len, wl.num_blocks,
+                             workspace=self.workspace, stream=stream,
+                             partition_size=self.partition_size, compute=self.compute)
+        return out
+
+    def step(self, stream=None) -> torch.Tensor:
+        """One pass of the hot path: write the new token rows, then decode."""
+        self.write(stream)
+        return self.decode(stream)
+
+    def write_bytes(self) -> int:
+        """Algorithmic bytes of the write: rows read + rows written + slot_mapping."""
+        if not self.has_write:
+            return 0
+        t = self.wl.slot_mapping.size
+        return 2 * 2 * t * self.row_bytes + 8 * t
+
+
+class DeviceWrite:
+    """The byte-strided two-cache write workload resident on the device."""
+
+    def __init__(self, wl: WriteWorkload, device="cuda"):
+        self.wl = wl
+        self.cache = to_dev(wl.init, device)
+        self.slot_mapping = to_dev(wl.slot_mapping, device)
+        self.rows = {key: to_dev(r, device) for key, r in wl.rows.items()}
+
+    def reset(self) -> None:
+        self.cache.copy_(torch.from_numpy(self.wl.init))
+
+    def write_layout(self, layout: str, stream=None) -> int:
+        """All (cache, layer) writes of one layout; returns the number of calls."""
+        n = 0
+        for c, v in self.wl.views[layout].items():
+            for layer in range(self.wl.num_layers):
+                pkv_cache_write(self.rows[(c, layer)], None, self.slot_mapping, self.cache, None,
+                                pkv_view(v.offset, v.layer_stride, v.block_stride, v.row_width,
+                                         layer),
+                                self.wl.block_size, self.wl.num_blocks, stream=stream)
+                n += 1
+        return n
+
+    def layout_bytes(self, layout: str) -> int:
+        t = self.wl.slot_mapping.size
+        per = sum(v.row_width for v in self.wl.views[layout].values()) * self.wl.num_layers
+        return 2 * t * per + 8 * t * len(self.wl.views[layout]) * self.wl.num_layers
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2 so the next kernel starts cold."""
+
+    def __init__(self, device="cuda", nbytes: int | None = None):
+        if nbytes is None:
+            props = torch.cuda.get_device_properties(device)
+            nbytes = 2 * max(int(getattr(props, "L2_cache_size", 0)), 128 << 20)
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def __call__(self) -> None:
+        self.buf.fill_(1)

@@ -23,14 +23,20 @@ Sources for the shapes (page title -- section):
   - "vLLM 技术内幕" §2.2: shared blocks carry a reference count; writing to a
     block whose count is above one first copies it (copy on write).
 
-Random numbers: numpy PCG64 seeded with 1000 + the workload's index; fp16
-values are float32 N(0, 1) draws rounded to nearest-even by numpy.
+Random numbers: numpy PCG64 seeded with 1000 + the workload's index.  fp16
+N(0, 1) values are drawn by inverse transform at fp16 resolution: a uniform
+16-bit integer u indexes a table holding the standard normal quantile at
+(u + 0.5) / 65536, rounded to fp16 (nearest-even).  This is N(0, 1) sampled
+on a 2^-16 probability grid (|x| <= 4.3); it is an order of magnitude faster
+than float32 normal draws followed by a float16 cast, which matters for the
+gigabyte-sized caches.
 """
 
 from __future__ import annotations
 
 import math
 from dataclasses import dataclass, field
+from statistics import NormalDist
 
 import numpy as np
 
@@ -138,8 +144,24 @@ def pad_tables(tables, width: int | None = None, fill: int = -1) -> np.ndarray:
     return out
 
 
+_NORMAL_FP16 = None
+
+
+def normal_fp16_table() -> np.ndarray:
+    """fp16 standard-normal quantiles at (u + 0.5) / 65536, u = 0..65535."""
+    global _NORMAL_FP16
+    if _NORMAL_FP16 is None:
+        inv = NormalDist().inv_cdf
+        _NORMAL_FP16 = np.array([inv((u + 0.5) / 65536.0) for u in range(65536)],
+                                dtype=np.float64).astype(np.float16)
+    return _NORMAL_FP16
+
+
 def fp16_normal(rng: np.random.Generator, shape) -> np.ndarray:
-    return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+    """N(0, 1) fp16 values of the given shape (inverse transform, see the module doc)."""
+    n = int(np.prod(shape))
+    u = np.frombuffer(rng.bytes(2 * n), dtype="<u2")
+    return normal_fp16_table()[u].reshape(shape)
 
 
 # --------------------------------------------------------------------------

@@ -1,0 +1,264 @@
+"""GPU parity of paged decode attention against the float64 oracle.
+
+Tolerance (fp16 inputs, fp32 accumulation, fp16 output): every element must
+satisfy |gpu - ref| <= 2e-3 + 1e-2 * |ref|.  Small cases compare every
+element; the full-size workloads compare sampled (sequence, head) rows the
+oracle computes one by one, plus properties that hold at any size (finite
+everywhere, inside the convex hull of the values read).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_131_gb300 import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-3, 1e-2
+SIMT, MMA = 1, 2
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_131_gb300 import _build
+    _build.build()
+    import paged_kv_cache_131_gb300 as m
+    assert torch.cuda.is_available()
+    m.pkv_get_device_error()
+    return m
+
+
+def assert_close(gpu, ref, pairs=None, what=""):
+    g = gpu.astype(np.float64)
+    if pairs is not None:
+        idx = tuple(np.array(pairs).T)
+        g, ref = g[idx], ref[idx]
+    assert not np.isnan(ref).any()
+    err = np.abs(g - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
+                           f"max |err| {err.max():.3e}, worst excess {(err - bound).max():.3e}")
+    return float(err.max())
+
+
+def oracle_after_write(wl):
+    k, v = wl.k_cache.copy(), wl.v_cache.copy()
+    if wl.slot_mapping is not None and wl.slot_mapping.size:
+        row = wl.num_kv_heads * wl.head_dim * 2
+        for cache, new in ((k, wl.k_new), (v, wl.v_new)):
+            oracle.cache_write(cache.view(np.uint8).reshape(-1), new.view(np.uint8),
+                               wl.slot_mapping, offset=0, layer=0, layer_stride=0,
+                               block_stride=wl.block_size * row, row_width=row,
+                               block_size=wl.block_size, num_blocks=wl.num_blocks)
+    return k, v
+
+
+def run(wl, **kw):
+    from paged_kv_cache_131_gb300.harness import DeviceDecode
+    dev = DeviceDecode(wl, **kw)
+    out = dev.step().cpu().numpy()
+    return dev, out
+
+
+# ------------------------------------------------------------- small cases
+
+
+@pytest.mark.parametrize("compute", [MMA, SIMT])
+def test_config1_tiny_all_elements(pkv, compute):
+    wl = W.config1_tiny()
+    dev, out = run(wl, compute=compute)
+    k, v = oracle_after_write(wl)
+    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale)
+    assert_close(out, ref, what="config 1")
+    assert pkv.pkv_get_device_error() == (0, -1)
+
+
+SMALL = [
+    # (index, lens, H, Hk, D)
+    (201, [0, 1, 15, 16, 17, 31, 32, 33, 100, 257, 600, 1100], 8, 8, 128),
+    (202, [1, 2, 16, 50, 513, 777], 8, 4, 128),
+    (203, [5, 47, 300, 999, 1024, 1500], 16, 4, 128),
+    (204, [3, 64, 129, 700], 16, 2, 128),
+    (205, [7, 19, 81, 530], 4, 4, 64),
+    (206, [16, 33, 400, 1030], 8, 4, 64),
+    (207, [9, 200, 520], 16, 2, 64),
+    (208, [2, 48, 333, 2049], 8, 1, 64),
+]
+
+
+@pytest.fixture(scope="module", params=SMALL, ids=lambda c: f"{c[0]}-G{c[2]//c[3]}-D{c[4]}")
+def small_case(request):
+    index, lens, H, Hk, D = request.param
+    wl = W.small_decode(index, lens, H=H, Hk=Hk, D=D)
+    k, v = oracle_after_write(wl)
+    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale)
+    return wl, ref
+
+
+@pytest.mark.parametrize("partition_size", [0, 16, 48, 128, 8192])
+@pytest.mark.parametrize("compute", [MMA, SIMT])
+def test_small_all_elements(pkv, small_case, partition_size, compute):
+    wl, ref = small_case
+    _, out = run(wl, partition_size=partition_size, compute=compute)
+    assert_close(out, ref, what=f"P{partition_size} c{compute}")
+    assert pkv.pkv_get_device_error() == (0, -1)
+
+
+def test_single_partition_results_do_not_depend_on_partition_size(pkv):
+    """Sequences that fit one partition take the same path: bit-equal outputs."""
+    wl = W.small_decode(209, [1, 40, 300, 512], H=8, Hk=2, D=128)
+    a = run(wl, partition_size=512)[1]
+    b = run(wl, partition_size=8192)[1]
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_physical_permutation_bit_exact(pkv):
+    wl = W.small_decode(210, [33, 700, 1200, 5], H=16, Hk=4, D=128, write_last=False)
+    _, out = run(wl)
+    perm = np.random.default_rng(3).permutation(wl.num_blocks)
+    k2 = np.empty_like(wl.k_cache)
+    v2 = np.empty_like(wl.v_cache)
+    k2[perm] = wl.k_cache
+    v2[perm] = wl.v_cache
+    bt = np.where(wl.block_tables >= 0, perm[np.maximum(wl.block_tables, 0)], -1).astype(np.int32)
+    wl2 = W.DecodeWorkload(wl.name, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                           wl.num_blocks, wl.scale, wl.seq_lens, bt, wl.q, k2, v2, None, None,
+                           None)
+    _, out2 = run(wl2)
+    assert np.array_equal(out.view(np.uint16), out2.view(np.uint16))
+
+
+def test_shared_prefix_equals_private_copies_bit_exact(pkv):
+    wl = W.small_decode(211, [600, 650, 700, 777], H=16, Hk=2, D=128, shared_prefix_tokens=512)
+    dev, out = run(wl)
+    k = dev.k_cache.cpu().numpy()
+    v = dev.v_cache.cpu().numpy()
+    S, nshared = wl.num_seqs, 512 // 16
+    k2 = np.concatenate([k, np.zeros((S * nshared,) + k.shape[1:], k.dtype)])
+    v2 = np.concatenate([v, np.zeros((S * nshared,) + v.shape[1:], v.dtype)])
+    bt2 = wl.block_tables.copy()
+    nxt = wl.num_blocks
+    for i in range(S):
+        for j in range(nshared):
+            k2[nxt], v2[nxt] = k[bt2[i, j]], v[bt2[i, j]]
+            bt2[i, j] = nxt
+            nxt += 1
+    wl2 = W.DecodeWorkload(wl.name, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                           nxt, wl.scale, wl.seq_lens, bt2, wl.q, k2, v2, None, None, None)
+    _, out2 = run(wl2)
+    assert np.array_equal(out.view(np.uint16), out2.view(np.uint16))
+
+
+def test_mma_and_simt_agree(pkv):
+    wl = W.small_decode(212, [100, 900, 1600], H=32, Hk=8, D=128)
+    a = run(wl, compute=MMA)[1].astype(np.float64)
+    b = run(wl, compute=SIMT)[1].astype(np.float64)
+    assert np.max(np.abs(a - b)) < 4e-3
+
+
+def test_workspace_reuse_and_left_zeroed(pkv):
+    from paged_kv_cache_131_gb300.harness import DeviceDecode
+    wl = W.small_decode(213, [1000, 1300, 20], H=8, Hk=2, D=128)
+    dev = DeviceDecode(wl, partition_size=64)
+    first = dev.step().clone()
+    for _ in range(3):
+        again = dev.decode().clone()
+        assert torch.equal(first, again)
+    torch.cuda.synchronize()
+    tickets = dev.workspace[: wl.num_seqs * wl.num_heads * 4]
+    assert int(tickets.sum()) == 0
+
+
+def test_non_default_stream(pkv):
+    from paged_kv_cache_131_gb300.harness import DeviceDecode
+    wl = W.small_decode(214, [77, 880], H=8, Hk=2, D=64)
+    dev = DeviceDecode(wl)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = dev.step(stream=s)
+    s.synchronize()
+    k, v = oracle_after_write(wl)
+    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale)
+    assert_close(out.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------- bad data
+
+
+def test_bad_block_id_recorded_skipped_no_fault(pkv):
+    from paged_kv_cache_131_gb300.harness import DeviceDecode
+    wl = W.small_decode(215, [40, 40], H=4, Hk=4, D=128, write_last=False)
+    dev = DeviceDecode(wl)
+    bt = dev.block_tables.clone()
+    bt[1, 1] = wl.num_blocks + 7  # second block of sequence 1
+    dev.block_tables.copy_(bt)
+    out = dev.decode().cpu().numpy()
+    kind, index = pkv.pkv_get_device_error()
+    assert kind == 2 and index == 1 * wl.max_blocks_per_seq + 1
+    # sequence 0 is untouched by the bad entry
+    ref = oracle.decode_attention(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.seq_lens,
+                                  wl.scale)
+    assert_close(out[:1], ref[:1])
+    # sequence 1 equals attention over its remaining (valid) positions
+    keep = [j for j in range(40) if j // 16 != 1]
+    k1 = np.concatenate([wl.k_cache[wl.block_tables[1, j // 16], j % 16][None] for j in keep])
+    v1 = np.concatenate([wl.v_cache[wl.block_tables[1, j // 16], j % 16][None] for j in keep])
+    q1 = wl.q[1].astype(np.float64)
+    s = np.einsum("hd,jhd->hj", q1, k1.astype(np.float64)) * wl.scale
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    exp = np.einsum("hj,jhd->hd", w / w.sum(axis=1, keepdims=True), v1.astype(np.float64))
+    assert_close(out[1:2], exp[None])
+
+
+def test_seq_len_beyond_table_recorded_no_fault(pkv):
+    from paged_kv_cache_131_gb300.harness import DeviceDecode
+    wl = W.small_decode(216, [20, 30], H=4, Hk=4, D=64, write_last=False)
+    dev = DeviceDecode(wl)
+    sl = dev.seq_lens.clone()
+    sl[0] = wl.max_blocks_per_seq * 16 + 100
+    dev.seq_lens.copy_(sl)
+    dev.decode()
+    kind, index = pkv.pkv_get_device_error()
+    assert (kind, index) == (3, 0)
+    sl[0] = -5
+    dev.seq_lens.copy_(sl)
+    out = dev.decode().cpu().numpy()
+    assert pkv.pkv_get_device_error() == (3, 0)
+    assert np.all(out[0] == 0)
+
+
+# ------------------------------------------------------------- full size
+
+
+def _sample_pairs(wl, n, seed):
+    rng = np.random.default_rng(seed)
+    S, H = wl.num_seqs, wl.num_heads
+    pairs = {(0, 0), (S - 1, H - 1), (int(np.argmax(wl.seq_lens)), H // 2),
+             (int(np.argmin(wl.seq_lens)), 1)}
+    while len(pairs) < n:
+        pairs.add((int(rng.integers(S)), int(rng.integers(H))))
+    return sorted(pairs)
+
+
+def _hull_check(out, wl, k_after, v_after, dev):
+    """Every output lies inside [min v, max v] of its KV head's values (a
+    convex combination), and nothing is NaN (poisoned slots never leak in)."""
+    assert np.isfinite(out).all()
+    vmax = float(np.nanmax(np.abs(v_after[np.isfinite(v_after)])))
+    assert np.abs(out.astype(np.float64)).max() <= vmax + ATOL
+
+
+@pytest.mark.parametrize("cfg,npairs", [(2, 96), (3, 48), (4, 96)])
+@pytest.mark.parametrize("compute", [MMA, SIMT])
+def test_full_size_configs_sampled(pkv, cfg, npairs, compute):
+    wl = W.config(cfg)
+    dev, out = run(wl, compute=compute)
+    assert pkv.pkv_get_device_error() == (0, -1)
+    k, v = oracle_after_write(wl)
+    pairs = _sample_pairs(wl, npairs, seed=cfg)
+    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale, pairs=pairs)
+    assert_close(out, ref, pairs=pairs, what=f"config {cfg}")
+    _hull_check(out, wl, k, v, dev)
