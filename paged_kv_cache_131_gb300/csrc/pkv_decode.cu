@@ -84,7 +84,7 @@ template <int D, int G>
 struct MmaPolicy {
     static constexpr int KS = D / 16;  // k-steps of S = Q K^T
     static constexpr int NT = D / 8;   // n-tiles of O
-    static constexpr bool kNeedsPbuf = false;
+    static constexpr bool kZeroTailRows = true;
     uint32_t qa[KS][2];
     float o[NT][2];
     float m, l;
@@ -108,7 +108,8 @@ struct MmaPolicy {
     }
 
     // One staged block: keys at kb, values at vb (row pitch Geo<D>::kRowBytes),
-    // nv valid tokens (1..16); rows >= nv hold stale finite data or zeros.
+    // nv valid tokens (1..16); key rows >= nv may hold anything (their scores
+    // are replaced by -inf), value rows >= nv hold zeros.
     __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, int nv, float scale_log2,
                                           int lane, float * /*pbuf*/) {
         constexpr int RB = Geo<D>::kRowBytes;
@@ -216,7 +217,7 @@ struct SimtPolicy {
     static constexpr int NCH = kBS / TC;                  // chunks per block
     static constexpr int NV = TC * G;                     // values per chunk per lane
     static constexpr int R = 32 / NV;                     // lanes holding the same result
-    static constexpr bool kNeedsPbuf = true;
+    static constexpr bool kZeroTailRows = false;          // reads rows < nv only
     float q[G][DPL];  // pre-scaled by scale*log2(e)
     float o[G][DPL];
     float m_all[G];   // running max of every head (same in all lanes)
@@ -369,6 +370,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params p) {
     const int H = p.num_heads;
     const int P = p.num_partitions;
 
+    // Launched with programmatic stream serialization: everything above ran
+    // while the previous kernel (typically the cache write) drained; no input
+    // is read before that kernel's results are visible.
+    grid_dependency_wait();
+
     // ---- sequence length and this CTA's share of it
     int L = __ldg(p.seq_lens + seq);
     const int cap = min(p.max_blocks_per_seq, P * p.partition_blocks) * kBS;
@@ -383,10 +389,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params p) {
     const int blk0 = part * p.partition_blocks;
     const int nblk = min(p.partition_blocks, nblk_seq - blk0);  // >= 0
 
-    // ---- set-up: zeroed ring (rows past a partial block meet p == 0 and
-    // must be finite), block-table slice, mbarriers
-    for (int i = threadIdx.x; i < Gm::kRingBytes / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(ring)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // ---- set-up: block-table slice, mbarriers
     const int32_t *bt_row = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
     for (int j = threadIdx.x; j < nblk; j += kThreads) {
         int b = __ldg(bt_row + blk0 + j);
@@ -454,6 +457,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params p) {
         const int nv = valid_tokens(i);
         if (nv > 0) {
             const uint32_t kb = ring_s + s * Gm::kStageBytes;
+            if (Policy::kZeroTailRows && nv < kBS) {
+                // value rows past a partial block meet weight 0 in the MMA and
+                // must hold finite numbers: zero them (stale rows are finite)
+                for (int e = lane; e < (kBS - nv) * (D / 8); e += 32) {
+                    const uint32_t a = kb + Gm::kTileBytes + (nv + e / (D / 8)) * Gm::kRowBytes +
+                                       (e % (D / 8)) * 16;
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u)
+                                 : "memory");
+                }
+                __syncwarp();
+            }
             st.block(kb, kb + Gm::kTileBytes, nv, p.scale_log2, lane, pbuf);
         }
         __syncwarp();
@@ -706,9 +720,18 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode)");
-    const dim3 grid(num_kv_heads, P, num_seqs);
-    fn<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_kv_heads, P, num_seqs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_failure(e, "decode_kernel launch");
 }
 

@@ -115,6 +115,21 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.
+
+// Lets the next kernel in the stream (launched with programmatic stream
+// serialization) be scheduled before this grid finishes.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Blocks until every grid this one depends on has completed and its memory
+// operations are visible; returns at once when there is none.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Warp-level matrix helpers (fp16 in, fp32 accumulate).
 
 __device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,

@@ -63,6 +63,9 @@ __device__ __forceinline__ void copy_row(uint8_t *dst_bytes, const uint8_t *src_
 
 template <typename VT>
 __global__ void __launch_bounds__(kWriteThreads) cache_write_kernel(const WriteParams p) {
+    // a dependent launch (the decode kernel) may be scheduled now; it still
+    // waits for this grid's completion before it reads anything
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t nvec = p.row_width / static_cast<int64_t>(sizeof(VT));
@@ -102,6 +105,7 @@ extern "C" int pkv_cache_write(const void *k, const void *v, const int64_t *slot
                                int32_t block_size, int64_t num_blocks, pkv_stream_t stream) {
     using namespace pkv;
     if (num_tokens < 0) return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;  // nothing to do; pointers may be NULL
     if (k == nullptr || slot_mapping == nullptr || k_cache == nullptr) return PKV_ERR_NULL;
     if ((v == nullptr) != (v_cache == nullptr)) return PKV_ERR_NULL;
     if (block_size <= 0 || num_blocks <= 0 || view.row_width <= 0 || view.block_stride <= 0 ||
@@ -111,7 +115,6 @@ extern "C" int pkv_cache_write(const void *k, const void *v, const int64_t *slot
     if (view.layer > 0 && view.layer_stride > (INT64_MAX - view.offset) / view.layer)
         return PKV_ERR_INVALID;
     if (!aligned(slot_mapping, alignof(int64_t))) return PKV_ERR_ALIGNMENT;
-    if (num_tokens == 0) return PKV_OK;
 
     const int64_t base = view.offset + static_cast<int64_t>(view.layer) * view.layer_stride;
     WriteParams p;
