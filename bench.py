@@ -52,7 +52,7 @@ WORKLOAD_NAMES = {
 }
 
 DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_131_gb300", "csrc", f)
-                  for f in ("pkv_decode.cu", "pkv_device.cuh")]
+                  for f in ("pkv_decode_balanced.cu", "pkv_decode_common.cuh", "pkv_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_dram_traffic.txt")
 
 
@@ -64,6 +64,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
     ap.add_argument("--compute", choices=["auto", "simt", "mma"], default="auto")
+    ap.add_argument("--schedule", choices=["auto", "grid", "balanced"], default="auto")
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -275,7 +276,9 @@ def main():
     if dist is not None:
         dist.barrier()
     compute = {"auto": 0, "simt": 1, "mma": 2}[args.compute]
-    dev = DeviceDecode(wl, device=f"cuda:{local}", partition_size=args.partition, compute=compute)
+    schedule = {"auto": 0, "grid": 1, "balanced": 2}[args.schedule]
+    dev = DeviceDecode(wl, device=f"cuda:{local}", partition_size=args.partition, compute=compute,
+                       schedule=schedule)
     flush = L2Flush(f"cuda:{local}")
     stream = torch.cuda.current_stream()
 
@@ -353,7 +356,7 @@ def main():
                    "seq_len": int(wl.max_seq_len), "parallelism": f"replicas x{world}",
                    "l2": "flushed (write of 2x L2) between timed steps; KV read 0.5 GB > L2",
                    "kv_cache": "resident in HBM (state), not copied per step",
-                   "compute": args.compute, "partition_tokens": args.partition or 512},
+                   "compute": args.compute, "schedule": args.schedule},
         "pct_hbm_peak": round(100 * value / world / peak, 2),
         "seqs_per_s": round(world * S / (step_ms * 1e-3), 1),
         "decode_tokens_per_s": round(world * S / (step_ms * 1e-3), 1),
@@ -365,8 +368,9 @@ def main():
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(f"config{args.config}"),
                      "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
-                     "kernel": "decode_kernel (MMA policy)" if compute != 1 else
-                               "decode_kernel (SIMT policy)",
+                     "kernel": ("decode_grid_kernel" if schedule == 1 else
+                                "decode_balanced_kernel") +
+                               (" (SIMT policy)" if compute == 1 else " (MMA policy)"),
                      "alg_bytes_per_launch": decode_alg_bytes},
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -112,27 +112,39 @@ int pkv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
  *     s_j  = scale * q[i,h,:] . K_j,   K_j = k_cache[bt[i, j/bs], j%bs, kv, :]
  *     out[i,h,:] = sum_j exp(s_j - max s) V_j / sum_j exp(s_j - max s),
  * j in [0, L).  Computed block by block with an online (running max / sum)
- * softmax in fp32; sequences longer than one partition (512 tokens) are
- * split into partitions whose partial (max, sum, weighted values) are merged
- * with a log-sum-exp rescale inside the same launch.  L == 0 gives zeros.
+ * softmax in fp32; a sequence whose blocks are spread over several CTAs
+ * leaves partial (max, sum, weighted values) that are merged with a
+ * log-sum-exp rescale inside the same launch.  L == 0 gives zeros.
+ *
+ * Two schedules (pkv_decode_options.schedule):
+ *  - balanced (default): one wave of persistent CTAs, each owning an equal
+ *    share of all sequences' blocks; needs num_kv_heads <= 8 and a workspace
+ *    of pkv_decode_workspace_bytes(...) bytes;
+ *  - grid: one CTA per (kv head, sequence, partition of 512 tokens); needs a
+ *    workspace only when max_seq_len > 512.
+ * With AUTO the balanced schedule runs when the shape and the workspace
+ * allow it, else the grid schedule.
  *
  *  out           device fp16 [num_seqs, num_heads, head_dim] (written).
  *  q             device fp16 [num_seqs, num_heads, head_dim].
  *  k_cache, v_cache  device fp16 [num_blocks, block_size, num_kv_heads,
  *                head_dim] ("deep-dive-into-vllm-05" §1.2), 16-byte aligned.
  *  block_tables  device int32 [num_seqs, max_blocks_per_seq]; entries past a
- *                sequence's ceil(L/block_size) blocks are never read.  An id
+ *                sequence's ceil(L/block_size) blocks are ignored.  An id
  *                outside [0, num_blocks) is skipped and recorded.
- *  seq_lens      device int32 [num_seqs].
- *  max_seq_len   host hint: an upper bound of seq_lens; it fixes the number of
- *                partitions P = ceil(max_seq_len / 512).  A longer sequence is
- *                truncated and recorded (PKV_DEVERR_SEQ_LEN).
- *  workspace     device scratch of at least pkv_decode_workspace_bytes(...)
- *                bytes, 16-byte aligned, needed only when P > 1 (else may be
- *                NULL).  It must be zero-filled before its first use (e.g. by
- *                pkv_decode_workspace_init); every call leaves it zero-filled
- *                again.  Calls that share a workspace must not overlap.
- *  Supported: head_dim in {64, 128}; G in {1, 2, 4, 8}; block_size == 16.
+ *  seq_lens      device int32 [num_seqs].  A length beyond the block table
+ *                (or, on the grid schedule, beyond max_seq_len) is truncated
+ *                and recorded (PKV_DEVERR_SEQ_LEN).
+ *  max_seq_len   host hint: an upper bound of seq_lens (sizes the grid
+ *                schedule's partitions).
+ *  workspace     device scratch, 16-byte aligned, of at least
+ *                pkv_decode_workspace_bytes(...) bytes (or NULL, see above).
+ *                It must be zero-filled before its first use (e.g. by
+ *                pkv_decode_workspace_init); every call that records no
+ *                PKV_DEVERR_TIMEOUT leaves it zero-filled again.  Calls that
+ *                share a workspace must not overlap on the GPU.
+ *  Supported: head_dim in {64, 128}; G in {1, 2, 4, 8}; block_size == 16;
+ *  num_seqs <= 65535.
  *  Returns PKV_OK (num_seqs == 0 launches nothing), PKV_ERR_NULL,
  *  PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_ALIGNMENT,
  *  PKV_ERR_WORKSPACE, PKV_ERR_CUDA.
@@ -146,20 +158,29 @@ int pkv_decode_attention(void *out, const void *q, const void *k_cache, const vo
 
 /* How the per-block arithmetic of pkv_decode_attention_ex runs. */
 typedef enum pkv_compute {
-    PKV_COMPUTE_AUTO = 0, /* the measured-fastest path for the shape            */
-    PKV_COMPUTE_SIMT = 1, /* fp32 FMA on CUDA cores, warp-shuffle reductions    */
+    PKV_COMPUTE_AUTO = 0, /* the measured-fastest path (MMA)                     */
+    PKV_COMPUTE_SIMT = 1, /* fp32 FMA on CUDA cores, warp-shuffle reductions     */
     PKV_COMPUTE_MMA = 2   /* the GQA group packed into 16x8x16 fp16 MMAs, fp32
-                             accumulate                                          */
+                             accumulate                                           */
 } pkv_compute;
 
+/* Which CTA schedule pkv_decode_attention_ex uses. */
+typedef enum pkv_schedule {
+    PKV_SCHEDULE_AUTO = 0,     /* balanced when possible, else grid           */
+    PKV_SCHEDULE_GRID = 1,     /* one CTA per (kv head, sequence, partition)  */
+    PKV_SCHEDULE_BALANCED = 2  /* persistent CTAs over equal block ranges     */
+} pkv_schedule;
+
 typedef struct pkv_decode_options {
-    int32_t partition_size; /* tokens per split-KV partition, a multiple of
-                               block_size in [16, 8192]; 0 = 512            */
+    int32_t partition_size; /* grid schedule: tokens per partition, a multiple
+                               of block_size in [16, 8192]; 0 = 512          */
     int32_t compute;        /* a pkv_compute value                           */
+    int32_t schedule;       /* a pkv_schedule value                          */
 } pkv_decode_options;
 
 /* pkv_decode_attention with explicit options (opts may be NULL = defaults).
- * The number of partitions is ceil(max_seq_len / partition_size). */
+ * Asking for the balanced schedule when it cannot run returns
+ * PKV_ERR_WORKSPACE (workspace too small) or PKV_ERR_UNSUPPORTED. */
 int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, const int32_t *seq_lens, float scale,
                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -168,13 +189,16 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
                             size_t workspace_bytes, const pkv_decode_options *opts,
                             pkv_stream_t stream);
 
-/* Workspace bytes pkv_decode_attention needs (0 when max_seq_len <= 512). */
-size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                  int32_t max_seq_len);
+/* Workspace bytes for any schedule of pkv_decode_attention on the current
+ * device (its SM count sizes the balanced schedule's partials; without a
+ * device, a 256-SM bound is used).  0 for invalid arguments. */
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_seq_len);
 
-/* Same for a given partition size (0 = 512). */
-size_t pkv_decode_workspace_bytes_ex(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                     int32_t max_seq_len, int32_t partition_size);
+/* Same, for a grid-schedule partition size (0 = 512). */
+size_t pkv_decode_workspace_bytes_ex(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t max_seq_len,
+                                     int32_t partition_size);
 
 /* Zero-fill a workspace on `stream` (cudaMemsetAsync). */
 int pkv_decode_workspace_init(void *workspace, size_t workspace_bytes, pkv_stream_t stream);

@@ -18,13 +18,15 @@ __all__ = [
     "pkv_cache_write", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_get_device_error", "pkv_status_string",
     "pkv_last_error_string", "pkv_version", "EXPORTED_SYMBOLS",
-    "PKV_COMPUTE_AUTO", "PKV_COMPUTE_SIMT", "PKV_COMPUTE_MMA", "DEVICE_ERRORS",
+    "PKV_COMPUTE_AUTO", "PKV_COMPUTE_SIMT", "PKV_COMPUTE_MMA", "PKV_SCHEDULE_AUTO",
+    "PKV_SCHEDULE_GRID", "PKV_SCHEDULE_BALANCED", "DEVICE_ERRORS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpagedkv.so")
 
 PKV_COMPUTE_AUTO, PKV_COMPUTE_SIMT, PKV_COMPUTE_MMA = 0, 1, 2
+PKV_SCHEDULE_AUTO, PKV_SCHEDULE_GRID, PKV_SCHEDULE_BALANCED = 0, 1, 2
 DEVICE_ERRORS = {0: "none", 1: "slot", 2: "block_id", 3: "seq_len", 4: "timeout"}
 
 EXPORTED_SYMBOLS = [
@@ -50,7 +52,8 @@ class pkv_view(ctypes.Structure):
 
 
 class pkv_decode_options(ctypes.Structure):
-    _fields_ = [("partition_size", ctypes.c_int32), ("compute", ctypes.c_int32)]
+    _fields_ = [("partition_size", ctypes.c_int32), ("compute", ctypes.c_int32),
+                ("schedule", ctypes.c_int32)]
 
 
 _lib = None
@@ -76,9 +79,9 @@ def load(path: str | None = None):
     lib.pkv_decode_attention_ex.restype = ctypes.c_int
     lib.pkv_decode_attention_ex.argtypes = dec + [ctypes.POINTER(pkv_decode_options), _p]
     lib.pkv_decode_workspace_bytes.restype = _sz
-    lib.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32]
+    lib.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
     lib.pkv_decode_workspace_bytes_ex.restype = _sz
-    lib.pkv_decode_workspace_bytes_ex.argtypes = [_i32, _i32, _i32, _i32, _i32]
+    lib.pkv_decode_workspace_bytes_ex.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32]
     lib.pkv_decode_workspace_init.restype = ctypes.c_int
     lib.pkv_decode_workspace_init.argtypes = [_p, _sz, _p]
     lib.pkv_get_device_error.restype = ctypes.c_int
@@ -152,7 +155,7 @@ def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, seq_lens, scale
                          num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
                          max_seq_len: int, num_blocks: int, workspace=None, stream=None,
                          partition_size: int = 0, compute: int = PKV_COMPUTE_AUTO,
-                         check: bool = True) -> int:
+                         schedule: int = PKV_SCHEDULE_AUTO, check: bool = True) -> int:
     """Paged decode attention: see pkv_decode_attention(_ex) in pagedkv.h.
 
     out, q: CUDA fp16 [S, H, D]; caches: CUDA fp16 [NB, bs, Hk, D];
@@ -173,18 +176,18 @@ def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, seq_lens, scale
             block_tables.shape[1] if block_tables.dim() == 2 else 0, int(max_seq_len),
             int(num_blocks), ws_ptr, ws_bytes)
     lib = load()
-    if partition_size == 0 and compute == PKV_COMPUTE_AUTO:
+    if partition_size == 0 and compute == PKV_COMPUTE_AUTO and schedule == PKV_SCHEDULE_AUTO:
         st = lib.pkv_decode_attention(*args, _stream(stream))
     else:
-        opts = pkv_decode_options(partition_size, compute)
+        opts = pkv_decode_options(partition_size, compute, schedule)
         st = lib.pkv_decode_attention_ex(*args, ctypes.byref(opts), _stream(stream))
     return _check(st, "pkv_decode_attention") if check else st
 
 
-def pkv_decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_seq_len: int,
-                               partition_size: int = 0) -> int:
-    return int(load().pkv_decode_workspace_bytes_ex(num_seqs, num_heads, head_dim, max_seq_len,
-                                                    partition_size))
+def pkv_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                               max_seq_len: int, partition_size: int = 0) -> int:
+    return int(load().pkv_decode_workspace_bytes_ex(num_seqs, num_heads, num_kv_heads, head_dim,
+                                                    max_seq_len, partition_size))
 
 
 def pkv_decode_workspace_init(workspace, stream=None) -> int:

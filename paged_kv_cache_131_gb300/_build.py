@@ -18,7 +18,8 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 HEADER = os.path.join(ROOT, "include", "pagedkv.h")
 
-SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_decode.cu"]
+SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_decode_api.cu", "pkv_decode_grid.cu",
+           "pkv_decode_balanced.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

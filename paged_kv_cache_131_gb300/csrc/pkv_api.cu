@@ -50,11 +50,16 @@ ErrorRecord *device_error_record() {
 
 int sm_count() {
     const int dev = current_device();
-    if (dev < 0) return 1;
+    if (dev < 0) {  // no device: a generous stand-in (used only for sizing)
+        cudaGetLastError();
+        return 256;
+    }
     if (g_sm_count[dev] == 0) {
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 1;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 256;
+        }
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];

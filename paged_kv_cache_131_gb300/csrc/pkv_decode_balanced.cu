@@ -1,0 +1,436 @@
+// pkv_decode_balanced.cu -- paged decode attention, balanced schedule.
+//
+// The work is the flattened list of (sequence, logical block) pairs: T =
+// sum_i ceil(L_i / 16) blocks, each carrying all KV heads of 16 tokens.  The
+// launch is one wave of persistent CTAs; CTA c owns the contiguous range
+// [c*T/N, (c+1)*T/N) of that list, so every CTA reads the same number of
+// bytes whatever the length mix, and no CTA is empty.
+//
+// A CTA has one producer warp and one consumer warp per KV head.
+//  - The producer walks its range.  For each block it takes the next stage
+//    of a `num_stages`-deep ring (waiting on the stage's "empty" mbarrier),
+//    publishes the block's (sequence, valid tokens, block id), and issues
+//    16 + 16 bulk (TMA) copies: key row r and value row r of the block, each
+//    row = all KV heads of one token (num_kv_heads*head_dim*2 contiguous
+//    bytes), completing on the stage's "full" mbarrier.  Block-table entries
+//    are loaded a 32-block window ahead.
+//  - Consumer warp h waits on "full", folds head h's 16 keys/values into its
+//    online-softmax state (compute policy of pkv_decode_common.cuh) and
+//    arrives on "empty".  When the sequence changes it finishes the previous
+//    one: a sequence wholly inside the range is normalised and written as
+//    fp16; a sequence cut by a range boundary leaves a partial (m, l, o) in
+//    the workspace, and the last of its contributors to take a ticket merges
+//    the partials with a log-sum-exp rescale.  No warp ever waits for
+//    another CTA.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "../../include/pagedkv.h"
+#include "pkv_decode_common.cuh"
+#include "pkv_decode_host.h"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace dec {
+namespace {
+
+constexpr int kMaxStages = 4;
+constexpr int kMaxThreads = (kMaxBalancedKvHeads + 1) * 32;
+
+// Dynamic shared memory:
+//   ring   stages * 2 * 16 rows * pitch   (key tile, then value tile)
+//   full   stages mbarriers (1 arrival + transaction bytes)
+//   empty  stages mbarriers (one arrival per consumer warp)
+//   meta   stages int4 {sequence, valid tokens, block id (-1 = skip), 0}
+//   cum    S + 1 int32: exclusive prefix sum of the sequences' block counts
+//   lens   S int32: sequence lengths (clamped to the block table)
+//   misc   4 int32
+//   pbuf   Hk * 16 * G fp32 (SIMT policy: one block's softmax weights)
+int smem_bytes(int stages, int stage_bytes, int S, int Hk, int G) {
+    return stages * stage_bytes + stages * 16 + stages * 16 + (2 * S + 1) * 4 + 16 +
+           Hk * kBS * G * 4;
+}
+
+// Largest s in [0, S) with cum[s] <= f (cum non-decreasing, cum[0] = 0).
+__device__ __forceinline__ int find_seq(const int *cum, int S, int64_t f) {
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= f) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// CTA whose range holds flattened block f (ranges [c*T/N, (c+1)*T/N)).
+__device__ __forceinline__ int cta_of(int64_t f, int64_t T, int64_t N) {
+    return static_cast<int>(((f + 1) * N + T - 1) / T - 1);
+}
+
+// Merge the partials of (seq, kvh) left by CTAs c_a..c_b and write fp16 out.
+template <int D, int G>
+__device__ void combine_partials(const BalancedParams &p, int seq, int kvh, int c_a, int c_b,
+                                 int64_t f_s, int64_t T, int64_t N, int lane) {
+    constexpr int DPL = D / 32;
+    const int Hk = p.num_kv_heads;
+    float M[G], den[G], acc[G][DPL];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        M[g] = kNegInf;
+        den[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[g][i] = 0.f;
+    }
+    for (int c = c_a; c <= c_b; ++c) {
+        const int64_t fc = static_cast<int64_t>(c) * T / N;
+        const int64_t slot = 2 * static_cast<int64_t>(c) + ((c == c_a && fc < f_s) ? 1 : 0);
+        const int64_t base = (slot * Hk + kvh) * G;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float2 ml = __ldcg(p.part_ml + base + g);
+            if (ml.x == kNegInf) continue;  // a contributor whose blocks were all skipped
+            const float mn = fmaxf(M[g], ml.x);
+            const float a = M[g] == kNegInf ? 0.f : exp2f(M[g] - mn);
+            const float b = exp2f(ml.x - mn);
+            den[g] = fmaf(den[g], a, ml.y * b);
+            const float *po = p.part_o + (base + g) * D + lane * DPL;
+            float o[DPL];
+            if constexpr (DPL == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
+                o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(po));
+                o[0] = v.x; o[1] = v.y;
+            }
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[g][i] = fmaf(acc[g][i], a, o[i] * b);
+            M[g] = mn;
+        }
+    }
+    __half *out = p.out + (static_cast<int64_t>(seq) * p.num_heads + kvh * G) * D + lane * DPL;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float inv = den[g] > 0.f ? 1.f / den[g] : 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; i += 2)
+            *reinterpret_cast<__half2 *>(out + g * D + i) =
+                __floats2half2_rn(acc[g][i] * inv, acc[g][i + 1] * inv);
+    }
+}
+
+template <int D, int G, class Policy>
+__global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const BalancedParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int Hk = p.num_kv_heads, S = p.num_seqs, NS = p.num_stages, H = p.num_heads;
+    const int pitch = p.pitch;
+    const int tile_bytes = kBS * pitch;
+    const int stage_bytes = 2 * tile_bytes;
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
+    uint64_t *empty = full + NS;
+    int4 *meta = reinterpret_cast<int4 *>(empty + NS);
+    int *cum = reinterpret_cast<int *>(meta + NS);
+    int *lens = cum + S + 1;
+    int *misc = lens + S;
+    float *pbuf_all = reinterpret_cast<float *>(misc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), Hk);
+        }
+        fence_mbarrier_init();
+    }
+
+    // Launched with programmatic stream serialization: nothing below reads an
+    // input before the previous kernel's results are visible.
+    grid_dependency_wait();
+
+    // ---- lengths (clamped to the block table) and their block-count prefix sum
+    const int cap = p.max_blocks_per_seq * kBS;
+    const int chunk = (S + nthreads - 1) / nthreads;
+    const int s_begin = min(S, threadIdx.x * chunk), s_end = min(S, s_begin + chunk);
+    int local = 0;
+    for (int s = s_begin; s < s_end; ++s) {
+        int L = __ldg(p.seq_lens + s);
+        if (L < 0 || L > cap) {
+            if (blockIdx.x == 0) record_error(p.err, PKV_DEVERR_SEQ_LEN, s);
+            L = L < 0 ? 0 : cap;
+        }
+        lens[s] = L;
+        local += (L + kBS - 1) / kBS;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int *wsum = reinterpret_cast<int *>(ring);  // scratch, before the ring is used
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int v = lane < nwarps ? wsum[lane] : 0;
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane < nwarps) wsum[lane] = inc - v;
+        if (lane == nwarps - 1) wsum[32] = inc;
+    }
+    __syncthreads();
+    {
+        int run = wsum[warp] + incl - local;
+        for (int s = s_begin; s < s_end; ++s) {
+            cum[s] = run;
+            run += (lens[s] + kBS - 1) / kBS;
+        }
+        if (threadIdx.x == 0) cum[S] = wsum[32];
+    }
+    fence_proxy_async_smem();  // scratch writes before the first bulk copy into the ring
+    __syncthreads();
+
+    // ---- empty sequences get zeros (no block of theirs is in any range)
+    const int64_t T = cum[S];
+    for (int s = blockIdx.x; s < S; s += gridDim.x) {
+        if (lens[s] == 0) {
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(s) * H * D);
+            for (int e = threadIdx.x; e < H * D / 8; e += nthreads) o[e] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (T == 0) return;
+    const int64_t N = min(static_cast<int64_t>(gridDim.x), T);
+    if (blockIdx.x >= N) return;
+    const int64_t f0 = static_cast<int64_t>(blockIdx.x) * T / N;
+    const int64_t f1 = (static_cast<int64_t>(blockIdx.x) + 1) * T / N;
+    const int n = static_cast<int>(f1 - f0);  // >= 1
+
+    const uint32_t ring_s = smem_u32(ring);
+    const uint32_t full_s = smem_u32(full), empty_s = smem_u32(empty);
+
+    if (warp == Hk) {
+        // ================================ producer ================================
+        const int64_t row_elems = static_cast<int64_t>(Hk) * D;
+        const uint32_t row_bytes = static_cast<uint32_t>(Hk) * D * 2;
+        // window of 32 blocks: lane j describes block base + j
+        auto fetch = [&](int base, int &raw, int &seq, int &nv) {
+            const int i = base + lane;
+            raw = -1;
+            seq = -1;
+            nv = 0;
+            if (i < n) {
+                const int64_t f = f0 + i;
+                seq = find_seq(cum, S, f);
+                const int blk = static_cast<int>(f - cum[seq]);
+                nv = min(kBS, lens[seq] - blk * kBS);
+                // checked when its window becomes current, so the load's latency
+                // hides behind the 32 blocks before it
+                raw = __ldg(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk);
+            }
+        };
+        auto check = [&](int base, int raw, int seq) -> int {
+            const int i = base + lane;
+            if (i >= n) return -1;
+            if (raw < 0 || static_cast<int64_t>(raw) >= p.num_blocks) {
+                const int blk = static_cast<int>(f0 + i - cum[seq]);
+                record_error(p.err, PKV_DEVERR_BLOCK_ID,
+                             static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk);
+                return -1;
+            }
+            return raw;
+        };
+        int c_raw, c_seq, c_nv, n_raw, n_seq, n_nv;
+        fetch(0, c_raw, c_seq, c_nv);
+        int c_bid = check(0, c_raw, c_seq);
+        fetch(32, n_raw, n_seq, n_nv);
+        int issued = 0;
+        bool ok = true;
+        for (int i = 0; i < n; ++i) {
+            const int st = i % NS;
+            if (i >= NS) {
+                const bool free_ = mbar_wait_bounded(empty_s + st * 8, ((i / NS) - 1) & 1);
+                if (!__all_sync(0xffffffffu, free_)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (i > 0 && (i & 31) == 0) {
+                c_bid = check(i, n_raw, n_seq);
+                c_seq = n_seq;
+                c_nv = n_nv;
+                fetch(i + 32, n_raw, n_seq, n_nv);
+            }
+            const int bid = __shfl_sync(0xffffffffu, c_bid, i & 31);
+            const int seq = __shfl_sync(0xffffffffu, c_seq, i & 31);
+            const int nv = __shfl_sync(0xffffffffu, c_nv, i & 31);
+            const int ncopy = bid < 0 ? 0 : nv;
+            if (lane == 0) {
+                meta[st] = make_int4(seq, nv, bid, 0);
+                mbar_arrive_expect_tx(full_s + st * 8, static_cast<uint32_t>(ncopy) * row_bytes * 2);
+            }
+            __syncwarp();
+            const int r = lane & (kBS - 1);
+            if (r < ncopy) {
+                const __half *src = (lane < kBS ? p.k_cache : p.v_cache) +
+                                    (static_cast<int64_t>(bid) * kBS + r) * row_elems;
+                const uint32_t dst =
+                    ring_s + st * stage_bytes + (lane < kBS ? 0 : tile_bytes) + r * pitch;
+                bulk_g2s(dst, src, row_bytes, full_s + st * 8);
+            }
+            issued = i + 1;
+        }
+        if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+        // every copy issued must land before the CTA may exit
+        for (int st = 0; st < NS && st < issued; ++st) {
+            const int uses = (issued - 1 - st) / NS + 1;
+            mbar_wait_bounded(full_s + st * 8, (uses - 1) & 1);
+        }
+        return;
+    }
+    if (warp > Hk) return;
+
+    // ================================ consumers ================================
+    const int kvh = warp;
+    Policy st;
+    float *pbuf = pbuf_all + kvh * kBS * G;
+    int cur = -1;
+
+    auto finish = [&](int seq) {
+        const int64_t f_s = cum[seq], f_e = cum[seq + 1];
+        const int64_t qrow = static_cast<int64_t>(seq) * H + kvh * G;
+        if (f_s >= f0 && f_e <= f1) {
+            st.write_output(p.out + qrow * D, lane);
+            return;
+        }
+        const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (f_s <= f0 ? 0 : 1);
+        const int64_t base = (slot * Hk + kvh) * G;
+        st.write_partial(p.part_ml + base, p.part_o + base * D, lane);
+        __threadfence();
+        __syncwarp();
+        const int c_a = cta_of(f_s, T, N), c_b = cta_of(f_e - 1, T, N);
+        int last = 0;
+        if (lane == 0) {
+            int *ticket = p.counters + static_cast<int64_t>(seq) * Hk + kvh;
+            const int prev = atomicAdd(ticket, 1);
+            last = prev == c_b - c_a;
+            if (last) {
+                atomicExch(ticket, 0);  // leave the workspace zeroed
+                __threadfence();
+            }
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) combine_partials<D, G>(p, seq, kvh, c_a, c_b, f_s, T, N, lane);
+    };
+
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+        const int s = i % NS;
+        const bool landed = mbar_wait_bounded(full_s + s * 8, (i / NS) & 1);
+        if (!__all_sync(0xffffffffu, landed)) {
+            ok = false;
+            break;
+        }
+        const int4 mt = meta[s];
+        if (mt.x != cur) {
+            if (cur >= 0) finish(cur);
+            cur = mt.x;
+            st.init(p.q + (static_cast<int64_t>(cur) * H + kvh * G) * D, p.scale_log2, lane);
+        }
+        if (mt.z >= 0 && mt.y > 0) {
+            const uint32_t kb = ring_s + s * stage_bytes + kvh * D * 2;
+            const uint32_t vb = kb + tile_bytes;
+            if (Policy::kZeroTailRows && mt.y < kBS) zero_tail_rows<D>(vb, pitch, mt.y, lane);
+            st.block(kb, vb, pitch, mt.y, p.scale_log2, lane, pbuf);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_s + s * 8);
+    }
+    if (!ok) {
+        if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+        return;
+    }
+    if (cur >= 0) finish(cur);
+}
+
+using BalancedFn = void (*)(const BalancedParams);
+
+template <int D, int G>
+BalancedFn pick(bool simt) {
+    if (simt) return decode_balanced_kernel<D, G, SimtPolicy<D, G>>;
+    return decode_balanced_kernel<D, G, MmaPolicy<D, G>>;
+}
+
+BalancedFn select(int D, int G, bool simt) {
+#define PKV_CASE(d, g) \
+    if (D == d && G == g) return pick<d, g>(simt);
+    PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
+    PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
+#undef PKV_CASE
+    return nullptr;
+}
+
+}  // namespace
+
+BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms) {
+    BalancedShape r{};
+    r.ok = num_kv_heads >= 1 && num_kv_heads <= kMaxBalancedKvHeads && num_seqs >= 1 &&
+           (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
+    if (!r.ok) return r;
+    const int pitch = num_kv_heads * D * 2 + kRowPad;
+    const int stage_bytes = 2 * kBS * pitch;
+    int stages = kMaxStages;
+    while (stages >= 2 && smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G) > kSmemPerSM)
+        --stages;
+    if (stages < 2) {
+        r.ok = false;
+        return r;
+    }
+    r.stages = stages;
+    r.smem = smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G);
+    const int threads = (num_kv_heads + 1) * 32;
+    r.ctas_per_sm = std::max(1, std::min({(228 * 1024) / (r.smem + 1024), 2048 / threads, 32}));
+    r.grid = std::max(1, num_sms) * r.ctas_per_sm;
+    const int64_t slots = 2 * static_cast<int64_t>(r.grid) * num_kv_heads * G;
+    r.workspace = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4) +
+                  align256(slots * 8) + slots * D * 4;
+    return r;
+}
+
+int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
+                    cudaStream_t stream) {
+    BalancedFn fn = select(D, G, simt);
+    if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, shape.smem);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode balanced)");
+    const int threads = (p.num_kv_heads + 1) * 32;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, shape.smem);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    per_sm = std::max(1, std::min(per_sm, shape.ctas_per_sm));
+    const int grid = std::min(shape.grid, per_sm * std::max(1, shape.grid / shape.ctas_per_sm));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = shape.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_failure(e, "decode balanced launch");
+}
+
+}  // namespace dec
+}  // namespace pkv

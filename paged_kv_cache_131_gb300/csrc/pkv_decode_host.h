@@ -1,0 +1,87 @@
+// pkv_decode_host.h -- launch parameters shared by the two decode schedules
+// (grid: one CTA per kv_head x partition x sequence; balanced: persistent
+// CTAs over equal ranges of the (sequence, block) space).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct ErrorRecord;
+
+namespace dec {
+
+constexpr int kGridWarps = 4;
+constexpr int kGridStages = 2;
+constexpr int kMaxPartitionTokens = 8192;
+constexpr int kDefaultPartitionTokens = 512;
+constexpr int kMaxBalancedKvHeads = 8;   // consumer warps per CTA (+1 producer)
+constexpr int kSmemPerSM = 227 * 1024;   // opt-in dynamic shared memory per CTA
+
+// Grid schedule.
+struct GridParams {
+    __half *out;
+    const __half *q;
+    const __half *k_cache;
+    const __half *v_cache;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    float scale_log2;  // scale * log2(e): scores live in the log2 domain
+    int num_heads;
+    int num_kv_heads;
+    int max_blocks_per_seq;
+    int num_partitions;    // P, grid.z
+    int partition_blocks;  // partition_size / 16
+    int64_t num_blocks;
+    int *counters;    // [S * Hk] tickets, zero between calls
+    float2 *part_ml;  // [S, H, P] (m, l)
+    float *part_o;    // [S, H, P, D]
+    ErrorRecord *err;
+};
+
+int grid_smem_bytes(int D, int G, int partition_blocks);
+int64_t grid_workspace_bytes(int64_t S, int64_t H, int64_t D, int64_t P);
+int launch_grid(const GridParams &p, int D, int G, bool simt, int num_seqs,
+                cudaStream_t stream);
+
+// Balanced schedule.
+struct BalancedParams {
+    __half *out;
+    const __half *q;
+    const __half *k_cache;
+    const __half *v_cache;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    float scale_log2;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int max_blocks_per_seq;
+    int num_stages;  // staging ring depth (blocks in flight per CTA)
+    int pitch;       // staged row pitch in bytes: Hk*D*2 + 16
+    int64_t num_blocks;
+    int *counters;    // [S * Hk] tickets, zero between calls
+    float2 *part_ml;  // [2 * grid][Hk][G]
+    float *part_o;    // [2 * grid][Hk][G][D]
+    ErrorRecord *err;
+};
+
+struct BalancedShape {
+    bool ok;          // the schedule supports this shape
+    int stages;       // ring depth
+    int smem;         // dynamic shared memory per CTA
+    int ctas_per_sm;  // resident CTAs per SM
+    int grid;         // CTAs launched
+    int64_t workspace;  // bytes of scratch it needs
+};
+
+BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms);
+int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
+                    cudaStream_t stream);
+
+inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+}  // namespace dec
+}  // namespace pkv

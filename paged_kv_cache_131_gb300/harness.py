@@ -10,7 +10,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (PKV_COMPUTE_AUTO, pkv_cache_write, pkv_decode_attention,
+from . import (PKV_COMPUTE_AUTO, PKV_SCHEDULE_AUTO, pkv_cache_write, pkv_decode_attention,
                pkv_decode_workspace_bytes, pkv_view)
 from .workloads import DecodeWorkload, WriteWorkload
 
@@ -23,11 +23,12 @@ class DeviceDecode:
     """One decode workload resident on the device: caches, tables, q, out, workspace."""
 
     def __init__(self, wl: DecodeWorkload, device="cuda", partition_size: int = 0,
-                 compute: int = PKV_COMPUTE_AUTO):
+                 compute: int = PKV_COMPUTE_AUTO, schedule: int = PKV_SCHEDULE_AUTO):
         self.wl = wl
         self.device = torch.device(device)
         self.partition_size = partition_size
         self.compute = compute
+        self.schedule = schedule
         self.q = to_dev(wl.q, device)
         self.k_cache = to_dev(wl.k_cache, device)
         self.v_cache = to_dev(wl.v_cache, device)
@@ -39,8 +40,9 @@ class DeviceDecode:
             self.k_new = to_dev(wl.k_new, device)
             self.v_new = to_dev(wl.v_new, device)
             self.slot_mapping = to_dev(wl.slot_mapping, device)
-        nbytes = pkv_decode_workspace_bytes(wl.num_seqs, wl.num_heads, wl.head_dim,
-                                            wl.max_seq_len, partition_size)
+        with torch.cuda.device(self.device):
+            nbytes = pkv_decode_workspace_bytes(wl.num_seqs, wl.num_heads, wl.num_kv_heads,
+                                                wl.head_dim, wl.max_seq_len, partition_size)
         # zero-filled once; every decode call leaves its tickets at zero again
         self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device) \
             if nbytes else None
@@ -66,7 +68,8 @@ class DeviceDecode:
                              self.seq_lens, wl.scale, wl.num_heads, wl.num_kv_heads,
                              wl.head_dim, wl.block_size, wl.max_seq_len, wl.num_blocks,
                              workspace=self.workspace, stream=stream,
-                             partition_size=self.partition_size, compute=self.compute)
+                             partition_size=self.partition_size, compute=self.compute,
+                             schedule=self.schedule)
         return out
 
     def step(self, stream=None) -> torch.Tensor:

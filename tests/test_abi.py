@@ -75,7 +75,7 @@ def test_write_validation(lib):
 
 def _decode(lib, **kw):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, scale=0.125, H=32, Hk=8, D=128,
-             bs=16, S=4, MB=8, maxL=128, NB=64, ws=None, wsb=0, opts=None)
+             bs=16, S=4, MB=64, maxL=128, NB=64, ws=None, wsb=0, opts=None)
     a.update(kw)
     opts = None if a["opts"] is None else ctypes.byref(pkv.pkv_decode_options(*a["opts"]))
     return lib.pkv_decode_attention_ex(a["out"], a["q"], a["k"], a["v"], a["bt"], a["sl"],
@@ -98,28 +98,44 @@ def test_decode_validation(lib):
     assert _decode(lib, NB=0) == -2
     assert _decode(lib, maxL=-1) == -2
     assert _decode(lib, scale=float("nan")) == -2
-    assert _decode(lib, opts=(24, 0)) == -2   # partition not a multiple of 16
-    assert _decode(lib, opts=(16384, 0)) == -2
-    assert _decode(lib, opts=(512, 7)) == -2  # unknown compute path
+    assert _decode(lib, opts=(24, 0, 0)) == -2   # partition not a multiple of 16
+    assert _decode(lib, opts=(16384, 0, 0)) == -2
+    assert _decode(lib, opts=(512, 7, 0)) == -2  # unknown compute path
+    assert _decode(lib, opts=(512, 0, 3)) == -2  # unknown schedule
     assert _decode(lib, q=FAKE + 8) == -4
     assert _decode(lib, k=FAKE + 2) == -4
-    assert _decode(lib, maxL=513) == -5       # two partitions need a workspace
-    need = pkv.pkv_decode_workspace_bytes(4, 32, 128, 513)
-    assert _decode(lib, maxL=513, ws=FAKE, wsb=need - 1) == -5
-    assert _decode(lib, maxL=513, ws=FAKE + 8, wsb=need) == -4
+    assert _decode(lib, maxL=513, ws=FAKE + 8, wsb=1 << 30) == -4
+    # grid schedule: two partitions need a workspace
+    grid = (0, 0, 1)
+    assert _decode(lib, maxL=513, opts=grid) == -5
+    need_grid = pkv.load().pkv_decode_workspace_bytes_ex(4, 32, 8, 128, 513, 0)
+    a256 = lambda x: (x + 255) // 256 * 256
+    grid_bytes = a256(4 * 32 * 4) + a256(4 * 32 * 2 * 8) + 4 * 32 * 2 * 128 * 4
+    assert need_grid >= grid_bytes
+    assert _decode(lib, maxL=513, ws=FAKE, wsb=grid_bytes - 1, opts=grid) == -5
+    # balanced schedule: always needs its workspace; more than 8 KV heads unsupported
+    bal = (0, 0, 2)
+    assert _decode(lib, opts=bal) == -5
+    assert _decode(lib, ws=FAKE, wsb=need_grid - 1, opts=bal) == -5 or need_grid == grid_bytes
+    assert _decode(lib, H=64, Hk=16, ws=FAKE, wsb=1 << 30, opts=bal) == -3
 
 
 def test_workspace_bytes(lib):
     def a256(x):
         return (x + 255) // 256 * 256
 
-    assert pkv.pkv_decode_workspace_bytes(64, 32, 128, 512) == 0
-    assert pkv.pkv_decode_workspace_bytes(64, 32, 128, 0) == 0
-    S, H, D, L = 64, 32, 128, 4096
-    P = 8
-    assert pkv.pkv_decode_workspace_bytes(S, H, D, L) == \
-        a256(S * H * 4) + a256(S * H * P * 8) + S * H * P * D * 4
-    assert pkv.pkv_decode_workspace_bytes(8, 32, 128, 32768, 1024) == \
+    assert pkv.pkv_decode_workspace_bytes(64, 32, 8, 128, 0) == 0
+    assert pkv.pkv_decode_workspace_bytes(64, 30, 8, 128, 100) == 0  # H not a multiple of Hk
+    # the larger of the grid schedule's partials (one per 512-token partition)
+    # and the balanced schedule's (two per CTA; one CTA per SM for this shape)
+    S, H, Hk, D, L = 64, 32, 8, 128, 4096
+    grid = a256(S * H * 4) + a256(S * H * 8 * 8) + S * H * 8 * D * 4
+    got = pkv.pkv_decode_workspace_bytes(S, H, Hk, D, L)
+    assert got >= grid
+    G = H // Hk
+    per_cta = 2 * Hk * G * (8 + D * 4)
+    assert (got - a256(S * Hk * 4)) >= per_cta  # room for at least one CTA's partials
+    assert pkv.pkv_decode_workspace_bytes(8, 32, 8, 128, 32768, 1024) >= \
         a256(8 * 32 * 4) + a256(8 * 32 * 32 * 8) + 8 * 32 * 32 * 128 * 4
 
 

@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 ATOL, RTOL = 2e-3, 1e-2
 SIMT, MMA = 1, 2
+GRID, BALANCED = 1, 2
 
 
 @pytest.fixture(scope="module")
@@ -66,10 +67,11 @@ def run(wl, **kw):
 # ------------------------------------------------------------- small cases
 
 
+@pytest.mark.parametrize("schedule", [BALANCED, GRID])
 @pytest.mark.parametrize("compute", [MMA, SIMT])
-def test_config1_tiny_all_elements(pkv, compute):
+def test_config1_tiny_all_elements(pkv, compute, schedule):
     wl = W.config1_tiny()
-    dev, out = run(wl, compute=compute)
+    dev, out = run(wl, compute=compute, schedule=schedule)
     k, v = oracle_after_write(wl)
     ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale)
     assert_close(out, ref, what="config 1")
@@ -98,26 +100,51 @@ def small_case(request):
     return wl, ref
 
 
-@pytest.mark.parametrize("partition_size", [0, 16, 48, 128, 8192])
-@pytest.mark.parametrize("compute", [MMA, SIMT])
-def test_small_all_elements(pkv, small_case, partition_size, compute):
+SCHEDULES = [(BALANCED, 0, MMA), (BALANCED, 0, SIMT)] + [
+    (GRID, p, c) for p in (0, 16, 48, 128, 8192) for c in (MMA, SIMT)]
+
+
+@pytest.mark.parametrize("schedule,partition_size,compute", SCHEDULES,
+                         ids=lambda v: str(v))
+def test_small_all_elements(pkv, small_case, schedule, partition_size, compute):
     wl, ref = small_case
-    _, out = run(wl, partition_size=partition_size, compute=compute)
-    assert_close(out, ref, what=f"P{partition_size} c{compute}")
+    _, out = run(wl, partition_size=partition_size, compute=compute, schedule=schedule)
+    assert_close(out, ref, what=f"s{schedule} P{partition_size} c{compute}")
     assert pkv.pkv_get_device_error() == (0, -1)
+
+
+def test_balanced_many_short_sequences(pkv):
+    """More sequences than CTAs, many empty or one-token ones: every range
+    boundary case of the balanced split (whole sequences, cut ones, empty)."""
+    lens = [0, 1, 2, 15, 16, 17, 0, 3, 31, 33, 1, 0] * 30 + [700, 5, 1200]
+    wl = W.small_decode(217, lens, H=8, Hk=2, D=64)
+    k, v = oracle_after_write(wl)
+    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale)
+    for compute in (MMA, SIMT):
+        _, out = run(wl, compute=compute, schedule=BALANCED)
+        assert_close(out, ref, what=f"c{compute}")
+    assert pkv.pkv_get_device_error() == (0, -1)
+
+
+def test_schedules_agree(pkv):
+    wl = W.small_decode(218, [100, 900, 1600, 3], H=32, Hk=8, D=128)
+    a = run(wl, schedule=BALANCED)[1].astype(np.float64)
+    b = run(wl, schedule=GRID)[1].astype(np.float64)
+    assert np.max(np.abs(a - b)) < 4e-3
 
 
 def test_single_partition_results_do_not_depend_on_partition_size(pkv):
     """Sequences that fit one partition take the same path: bit-equal outputs."""
     wl = W.small_decode(209, [1, 40, 300, 512], H=8, Hk=2, D=128)
-    a = run(wl, partition_size=512)[1]
-    b = run(wl, partition_size=8192)[1]
+    a = run(wl, partition_size=512, schedule=GRID)[1]
+    b = run(wl, partition_size=8192, schedule=GRID)[1]
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
-def test_physical_permutation_bit_exact(pkv):
+@pytest.mark.parametrize("schedule", [BALANCED, GRID])
+def test_physical_permutation_bit_exact(pkv, schedule):
     wl = W.small_decode(210, [33, 700, 1200, 5], H=16, Hk=4, D=128, write_last=False)
-    _, out = run(wl)
+    _, out = run(wl, schedule=schedule)
     perm = np.random.default_rng(3).permutation(wl.num_blocks)
     k2 = np.empty_like(wl.k_cache)
     v2 = np.empty_like(wl.v_cache)
@@ -127,13 +154,14 @@ def test_physical_permutation_bit_exact(pkv):
     wl2 = W.DecodeWorkload(wl.name, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
                            wl.num_blocks, wl.scale, wl.seq_lens, bt, wl.q, k2, v2, None, None,
                            None)
-    _, out2 = run(wl2)
+    _, out2 = run(wl2, schedule=schedule)
     assert np.array_equal(out.view(np.uint16), out2.view(np.uint16))
 
 
-def test_shared_prefix_equals_private_copies_bit_exact(pkv):
+@pytest.mark.parametrize("schedule", [BALANCED, GRID])
+def test_shared_prefix_equals_private_copies_bit_exact(pkv, schedule):
     wl = W.small_decode(211, [600, 650, 700, 777], H=16, Hk=2, D=128, shared_prefix_tokens=512)
-    dev, out = run(wl)
+    dev, out = run(wl, schedule=schedule)
     k = dev.k_cache.cpu().numpy()
     v = dev.v_cache.cpu().numpy()
     S, nshared = wl.num_seqs, 512 // 16
@@ -148,7 +176,7 @@ def test_shared_prefix_equals_private_copies_bit_exact(pkv):
             nxt += 1
     wl2 = W.DecodeWorkload(wl.name, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
                            nxt, wl.scale, wl.seq_lens, bt2, wl.q, k2, v2, None, None, None)
-    _, out2 = run(wl2)
+    _, out2 = run(wl2, schedule=schedule)
     assert np.array_equal(out.view(np.uint16), out2.view(np.uint16))
 
 
@@ -159,10 +187,11 @@ def test_mma_and_simt_agree(pkv):
     assert np.max(np.abs(a - b)) < 4e-3
 
 
-def test_workspace_reuse_and_left_zeroed(pkv):
+@pytest.mark.parametrize("schedule", [BALANCED, GRID])
+def test_workspace_reuse_and_left_zeroed(pkv, schedule):
     from paged_kv_cache_131_gb300.harness import DeviceDecode
     wl = W.small_decode(213, [1000, 1300, 20], H=8, Hk=2, D=128)
-    dev = DeviceDecode(wl, partition_size=64)
+    dev = DeviceDecode(wl, partition_size=64, schedule=schedule)
     first = dev.step().clone()
     for _ in range(3):
         again = dev.decode().clone()
@@ -188,10 +217,11 @@ def test_non_default_stream(pkv):
 # ------------------------------------------------------------- bad data
 
 
-def test_bad_block_id_recorded_skipped_no_fault(pkv):
+@pytest.mark.parametrize("schedule", [BALANCED, GRID])
+def test_bad_block_id_recorded_skipped_no_fault(pkv, schedule):
     from paged_kv_cache_131_gb300.harness import DeviceDecode
     wl = W.small_decode(215, [40, 40], H=4, Hk=4, D=128, write_last=False)
-    dev = DeviceDecode(wl)
+    dev = DeviceDecode(wl, schedule=schedule)
     bt = dev.block_tables.clone()
     bt[1, 1] = wl.num_blocks + 7  # second block of sequence 1
     dev.block_tables.copy_(bt)
@@ -213,10 +243,11 @@ def test_bad_block_id_recorded_skipped_no_fault(pkv):
     assert_close(out[1:2], exp[None])
 
 
-def test_seq_len_beyond_table_recorded_no_fault(pkv):
+@pytest.mark.parametrize("schedule", [BALANCED, GRID])
+def test_seq_len_beyond_table_recorded_no_fault(pkv, schedule):
     from paged_kv_cache_131_gb300.harness import DeviceDecode
     wl = W.small_decode(216, [20, 30], H=4, Hk=4, D=64, write_last=False)
-    dev = DeviceDecode(wl)
+    dev = DeviceDecode(wl, schedule=schedule)
     sl = dev.seq_lens.clone()
     sl[0] = wl.max_blocks_per_seq * 16 + 100
     dev.seq_lens.copy_(sl)
@@ -251,14 +282,29 @@ def _hull_check(out, wl, k_after, v_after, dev):
     assert np.abs(out.astype(np.float64)).max() <= vmax + ATOL
 
 
+_FULL = {}
+
+
+def _full(cfg, npairs):
+    """Workload, post-write caches and sampled oracle rows of a full-size config
+    (built once per config and kept for the module)."""
+    if cfg not in _FULL:
+        _FULL.clear()
+        wl = W.config(cfg)
+        k, v = oracle_after_write(wl)
+        pairs = _sample_pairs(wl, npairs, seed=cfg)
+        ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale,
+                                      pairs=pairs)
+        _FULL[cfg] = (wl, k, v, pairs, ref)
+    return _FULL[cfg]
+
+
 @pytest.mark.parametrize("cfg,npairs", [(2, 96), (3, 48), (4, 96)])
-@pytest.mark.parametrize("compute", [MMA, SIMT])
-def test_full_size_configs_sampled(pkv, cfg, npairs, compute):
-    wl = W.config(cfg)
-    dev, out = run(wl, compute=compute)
+@pytest.mark.parametrize("schedule,compute", [(BALANCED, MMA), (BALANCED, SIMT), (GRID, MMA),
+                                              (GRID, SIMT)])
+def test_full_size_configs_sampled(pkv, cfg, npairs, schedule, compute):
+    wl, k, v, pairs, ref = _full(cfg, npairs)
+    dev, out = run(wl, compute=compute, schedule=schedule)
     assert pkv.pkv_get_device_error() == (0, -1)
-    k, v = oracle_after_write(wl)
-    pairs = _sample_pairs(wl, npairs, seed=cfg)
-    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale, pairs=pairs)
     assert_close(out, ref, pairs=pairs, what=f"config {cfg}")
     _hull_check(out, wl, k, v, dev)
