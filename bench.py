@@ -112,6 +112,24 @@ def recorded_traffic(workload_key: str):
     return float(v) if v else None
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """Max of a per-rank float over the process group (the rank's own value
+    when there is none).  NCCL reduces a CUDA tensor, gloo a CPU one."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, step_ms_max: float) -> float:
+    """Weak scaling: every rank reads its own replica's bytes each step; the
+    job's step takes as long as its slowest rank."""
+    return world * bytes_per_rank / (step_ms_max * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled while the timed loop runs."""
 
@@ -298,28 +316,38 @@ def main():
         raise RuntimeError(f"device error {pkv.DEVICE_ERRORS.get(kind)} at {idx}")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+
+    def timed_loop(split: bool):
+        """K steps, L2 flushed before each (outside the events).  Without
+        `split` only the step's ends are marked, so the decode launch may
+        overlap the write kernel's tail as it does in use; with `split` an
+        event between them gives each kernel's own duration."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            dev.write()
+            if split:
+                ev[i][1].record(stream)
+            dev.decode()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        step = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+        if not split:
+            return step, None, None
+        return (step, sum(e[0].elapsed_time(e[1]) for e in ev) / K,
+                sum(e[1].elapsed_time(e[2]) for e in ev) / K)
+
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
-        for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            dev.write()
-            ev[i][1].record(stream)
-            dev.decode()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
+        step_ms, _, _ = timed_loop(split=False)
         t_wall = time.perf_counter() - t_wall
-    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
-    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
-    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+        _, write_ms, decode_ms = timed_loop(split=True)
     if dist is not None:
-        t = torch.tensor([step_ms], device=f"cuda:{local}")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+        step_ms = max_over_ranks(step_ms, dist, f"cuda:{local}")
         dist.barrier()
 
     # end to end through the public API: pinned host inputs in, output out
@@ -330,7 +358,7 @@ def main():
             dist.destroy_process_group()
         return
     peak, peak_kind = measured_peaks()
-    value = world * kv_bytes / (step_ms * 1e-3) / 1e9
+    value = whole_job_gbs(kv_bytes, world, step_ms)
     achieved = decode_alg_bytes / (decode_ms * 1e-3) / 1e9
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -354,7 +382,8 @@ def main():
         "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
         "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": S * world,
                    "seq_len": int(wl.max_seq_len), "parallelism": f"replicas x{world}",
-                   "l2": "flushed (write of 2x L2) between timed steps; KV read 0.5 GB > L2",
+                   "l2": "flushed between timed steps (write a 2x L2 buffer, then read another "
+                         "2x L2 buffer: cold, clean L2); KV read per step > L2",
                    "kv_cache": "resident in HBM (state), not copied per step",
                    "compute": args.compute, "schedule": args.schedule},
         "pct_hbm_peak": round(100 * value / world / peak, 2),
@@ -384,27 +413,19 @@ def main():
 
 def e2e_measure(dev, wl, steps, stream, flush):
     """Same metric through the public API from pinned host buffers: per step the
-    step's inputs (q, new K/V rows, slot_mapping, block tables, seq_lens) go
-    host -> device, the library runs, the output comes back device -> host.
-    L2 is flushed between steps, outside the timed events."""
+    step's inputs (q, new K/V rows, slot_mapping, block tables, seq_lens,
+    packed in one pinned buffer) go host -> device in one copy, the library
+    runs, the output comes back device -> host.  L2 is flushed between steps,
+    outside the timed events."""
     import torch
 
-    host = {
-        "q": torch.from_numpy(wl.q).pin_memory(),
-        "block_tables": torch.from_numpy(wl.block_tables).pin_memory(),
-        "seq_lens": torch.from_numpy(wl.seq_lens).pin_memory(),
-    }
-    if dev.has_write:
-        host["k_new"] = torch.from_numpy(wl.k_new).pin_memory()
-        host["v_new"] = torch.from_numpy(wl.v_new).pin_memory()
-        host["slot_mapping"] = torch.from_numpy(wl.slot_mapping).pin_memory()
+    host = dev.host_inputs(pinned=True)  # all per-step inputs, packed: one copy in
     out_host = torch.empty(tuple(wl.q.shape), dtype=torch.float16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = host.numel()
     d2h = out_host.numel() * out_host.element_size()
 
     def one():
-        for name, t in host.items():
-            getattr(dev, name).copy_(t, non_blocking=True)
+        dev.inputs.copy_(host, non_blocking=True)
         dev.step()
         out_host.copy_(dev.out, non_blocking=True)
 

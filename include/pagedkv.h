@@ -143,6 +143,12 @@ int pkv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
  *                pkv_decode_workspace_init); every call that records no
  *                PKV_DEVERR_TIMEOUT leaves it zero-filled again.  Calls that
  *                share a workspace must not overlap on the GPU.
+ *  Ordering: the launch may overlap the previous kernel in the stream when
+ *  that kernel signals programmatic launch completion (pkv_cache_write does).
+ *  Before that kernel's completion the call reads only q, block_tables and
+ *  seq_lens; it reads the caches and writes out/workspace only after.  So a
+ *  preceding kernel that signals early must not write q, block_tables or
+ *  seq_lens (kernels that never signal are waited for in full, as usual).
  *  Supported: head_dim in {64, 128}; G in {1, 2, 4, 8}; block_size == 16;
  *  num_seqs <= 65535.
  *  Returns PKV_OK (num_seqs == 0 launches nothing), PKV_ERR_NULL,

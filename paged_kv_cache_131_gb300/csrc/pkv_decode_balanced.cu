@@ -148,9 +148,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
         fence_mbarrier_init();
     }
 
-    // Launched with programmatic stream serialization: nothing below reads an
-    // input before the previous kernel's results are visible.
-    grid_dependency_wait();
+    // Launched with programmatic stream serialization, so this grid may start
+    // while the previous kernel in the stream -- typically the cache write,
+    // which writes nothing but the caches -- is still running.  Lengths, block
+    // tables and queries are read before grid_dependency_wait(); the caches
+    // and the outputs are touched only after it.
 
     // ---- lengths (clamped to the block table) and their block-count prefix sum
     const int cap = p.max_blocks_per_seq * kBS;
@@ -200,14 +202,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
 
     // ---- empty sequences get zeros (no block of theirs is in any range)
     const int64_t T = cum[S];
-    for (int s = blockIdx.x; s < S; s += gridDim.x) {
-        if (lens[s] == 0) {
-            uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(s) * H * D);
-            for (int e = threadIdx.x; e < H * D / 8; e += nthreads) o[e] = make_uint4(0, 0, 0, 0);
+    const int64_t N = min(static_cast<int64_t>(gridDim.x), T);
+    bool zeros_due = false;
+    for (int s = blockIdx.x; s < S && !zeros_due; s += gridDim.x) zeros_due = lens[s] == 0;
+    if (zeros_due && (blockIdx.x >= N || warp < Hk)) {
+        // the consumers (or every warp of a CTA without a range) write them
+        grid_dependency_wait();
+        const int nz = blockIdx.x >= N ? nthreads : Hk * 32;
+        for (int s = blockIdx.x; s < S; s += gridDim.x) {
+            if (lens[s] == 0) {
+                uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(s) * H * D);
+                for (int e = threadIdx.x; e < H * D / 8; e += nz) o[e] = make_uint4(0, 0, 0, 0);
+            }
         }
     }
-    if (T == 0) return;
-    const int64_t N = min(static_cast<int64_t>(gridDim.x), T);
     if (blockIdx.x >= N) return;
     const int64_t f0 = static_cast<int64_t>(blockIdx.x) * T / N;
     const int64_t f1 = (static_cast<int64_t>(blockIdx.x) + 1) * T / N;
@@ -251,6 +259,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
         fetch(0, c_raw, c_seq, c_nv);
         int c_bid = check(0, c_raw, c_seq);
         fetch(32, n_raw, n_seq, n_nv);
+        grid_dependency_wait();  // the caches may have just been written
         int issued = 0;
         bool ok = true;
         for (int i = 0; i < n; ++i) {
@@ -302,6 +311,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
     Policy st;
     float *pbuf = pbuf_all + kvh * kBS * G;
     int cur = -1;
+    {
+        // warm L2 with the query rows of the (up to 8) sequences this range
+        // touches, so a sequence switch does not stall on a cold load
+        const int s_first = find_seq(cum, S, f0), s_last = find_seq(cum, S, f1 - 1);
+        const int bytes = G * D * 2;
+        for (int s = s_first; s <= s_last && s < s_first + 8; ++s) {
+            const char *row = reinterpret_cast<const char *>(
+                p.q + (static_cast<int64_t>(s) * H + kvh * G) * D);
+            for (int off = lane * 128; off < bytes; off += 32 * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+        }
+    }
+    grid_dependency_wait();  // outputs and partials are written below
 
     auto finish = [&](int seq) {
         const int64_t f_s = cum[seq], f_e = cum[seq + 1];

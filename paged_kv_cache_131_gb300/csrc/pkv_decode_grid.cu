@@ -76,10 +76,11 @@ __global__ void __launch_bounds__(kThreads) decode_grid_kernel(const GridParams 
         fence_mbarrier_init();
     }
 
-    // Launched with programmatic stream serialization: the set-up above ran
-    // while the previous kernel (typically the cache write) drained; no input
-    // is read before that kernel's results are visible.
-    grid_dependency_wait();
+    // Launched with programmatic stream serialization, so this grid may start
+    // while the previous kernel in the stream -- typically the cache write,
+    // which writes nothing but the caches -- is still running.  The length and
+    // the block table are read before grid_dependency_wait(); the caches and
+    // the outputs are touched only after it.
 
     // ---- sequence length and block-table slice, loaded together
     const int blk0 = part * p.partition_blocks;
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kThreads) decode_grid_kernel(const GridParams 
         }
     }
     __syncthreads();
+    grid_dependency_wait();
 
     // ---- per-warp pipeline over blocks warp, warp+4, warp+8, ...
     Policy st;
