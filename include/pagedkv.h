@@ -206,6 +206,39 @@ size_t pkv_decode_workspace_bytes_ex(int32_t num_seqs, int32_t num_heads, int32_
                                      int32_t head_dim, int32_t max_seq_len,
                                      int32_t partition_size);
 
+/* Bytes of the built-in scratch of pkv_decode_attention_noalloc (16 MiB). */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * pkv_decode_attention without a workspace, for callers that cannot allocate
+ * device memory: a plugin inside a host runtime that owns the device-memory
+ * budget and passes in only inputs and outputs, or a latency-critical loop
+ * that must never call cudaMalloc (which can synchronise the device).  The
+ * pages have no counterpart; it computes exactly what pkv_decode_attention
+ * computes, with the same arguments minus the workspace.
+ *
+ * Its scratch is a device array of PKV_NOALLOC_SCRATCH_BYTES built into the
+ * library: every device that loads the library holds it until the process
+ * exits.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - Every call clears the array's ticket counters on `stream` before the
+ *    kernel (the array keeps the previous call's contents otherwise).
+ *  - All calls share the one array: calls that overlap on the GPU (other
+ *    streams, other threads) race and corrupt each other's results.
+ *  - A shape whose scratch need exceeds PKV_NOALLOC_SCRATCH_BYTES is refused
+ *    with PKV_ERR_WORKSPACE before anything runs (pkv_last_error_string()
+ *    gives the bytes needed); use pkv_decode_attention for it.
+ */
+int pkv_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *seq_lens, float scale, int32_t num_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int32_t num_seqs, int32_t max_blocks_per_seq,
+                                 int32_t max_seq_len, int64_t num_blocks, pkv_stream_t stream);
+
 /* Zero-fill a workspace on `stream` (cudaMemsetAsync). */
 int pkv_decode_workspace_init(void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 

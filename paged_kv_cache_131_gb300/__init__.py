@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = [
     "pkv_cache_write", "pkv_decode_attention", "pkv_decode_attention_ex",
     "pkv_decode_workspace_bytes", "pkv_decode_workspace_bytes_ex", "pkv_decode_workspace_init",
     "pkv_get_device_error", "pkv_status_string", "pkv_last_error_string", "pkv_version",
+    "pkv_decode_attention_noalloc",
 ]
 
 
@@ -78,6 +79,8 @@ def load(path: str | None = None):
     lib.pkv_decode_attention.argtypes = dec + [_p]
     lib.pkv_decode_attention_ex.restype = ctypes.c_int
     lib.pkv_decode_attention_ex.argtypes = dec + [ctypes.POINTER(pkv_decode_options), _p]
+    lib.pkv_decode_attention_noalloc.restype = ctypes.c_int
+    lib.pkv_decode_attention_noalloc.argtypes = dec[:15] + [_p]
     lib.pkv_decode_workspace_bytes.restype = _sz
     lib.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
     lib.pkv_decode_workspace_bytes_ex.restype = _sz

@@ -30,6 +30,10 @@ int cuda_failure(cudaError_t e, const char *where) {
     return PKV_ERR_CUDA;
 }
 
+void set_last_error(const char *msg) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 ErrorRecord *device_error_record() {
     const int dev = current_device();
     if (dev < 0) {

@@ -15,6 +15,9 @@ ErrorRecord *device_error_record();
 // Remember a CUDA error's text for pkv_last_error_string; returns PKV_ERR_CUDA.
 int cuda_failure(cudaError_t e, const char *where);
 
+// Remember a message for pkv_last_error_string.
+void set_last_error(const char *msg);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
