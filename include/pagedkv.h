@@ -102,6 +102,54 @@ int pkv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
                     int64_t num_tokens, void *k_cache, void *v_cache, pkv_view view,
                     int32_t block_size, int64_t num_blocks, pkv_stream_t stream);
 
+/* One (source rows, cache, view) triple of pkv_cache_write_multi. */
+typedef struct pkv_write_desc {
+    const void *src; /* device: num_tokens rows of view.row_width bytes      */
+    void *cache;     /* device byte allocation holding the view              */
+    pkv_view view;   /* includes the layer written                           */
+} pkv_write_desc;
+
+#define PKV_MAX_WRITE_DESCS 32
+
+/*
+ * Several cache writes that share one slot_mapping, in one launch: for every
+ * token t and descriptor d, the row at d.src + t*d.view.row_width goes to the
+ * address of slot_mapping[t] in d's view, exactly as pkv_cache_write does.
+ * This is how every layer and cache of one block table is written at once:
+ * the two caches (MLA and indexer) of "vLLM KV Cache Layout 可视化" --
+ * 两种 cache 共用一张 block table share a slot_mapping ("MLA 和 indexer 共用
+ * 同一个值", 查一个 token).
+ *  descs       HOST array of num_descs (0..PKV_MAX_WRITE_DESCS) descriptors;
+ *              read during the call only.  Rows of different descriptors must
+ *              not overlap in memory (which lands is then unspecified).
+ *  Other arguments, slot rules and errors as pkv_cache_write.
+ */
+int pkv_cache_write_multi(const pkv_write_desc *descs, int32_t num_descs,
+                          const int64_t *slot_mapping, int64_t num_tokens, int32_t block_size,
+                          int64_t num_blocks, pkv_stream_t stream);
+
+/*
+ * Copy whole physical blocks within one cache view ("vLLM 技术内幕" §2.2,
+ * copy on write: a sequence about to write into a block whose ref_cnt is
+ * above one gets a new block holding a copy of the old one).
+ * For each pair p in [0, num_pairs), with src = block_mapping[2p] and dst =
+ * block_mapping[2p+1], and each layer l in [view.layer, view.layer +
+ * num_layers): the page of block_size*row_width bytes at
+ *     offset + l*layer_stride + src*block_stride
+ * is copied to the same place of block dst.
+ *  cache          device byte allocation holding the view.
+ *  block_mapping  device int64 [num_pairs][2].  A pair with an id outside
+ *                 [0, num_blocks) is skipped and recorded (PKV_DEVERR_BLOCK_ID,
+ *                 index = pair); src == dst is a no-op.  A block must not be
+ *                 both a source and a destination, nor a destination twice
+ *                 (the result is then unspecified).
+ *  Returns PKV_OK (nothing to copy launches nothing), PKV_ERR_NULL,
+ *  PKV_ERR_INVALID, PKV_ERR_ALIGNMENT, PKV_ERR_CUDA.
+ */
+int pkv_copy_blocks(void *cache, pkv_view view, int32_t num_layers, int32_t block_size,
+                    const int64_t *block_mapping, int64_t num_pairs, int64_t num_blocks,
+                    pkv_stream_t stream);
+
 /*
  * Paged decode attention ("deep-dive-into-vllm-05" §2 read loop and §3.2
  * GQA; "vLLM 技术内幕" §2.1: the query is dotted with the keys of each

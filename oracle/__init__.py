@@ -62,6 +62,8 @@ def _bind(lib):
     lib.oracle_split_slot.argtypes = [_i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
     lib.oracle_cache_write.restype = _i64
     lib.oracle_cache_write.argtypes = [_p, _i64, _p, _p, _i64] + [_i64] * 7
+    lib.oracle_copy_blocks.restype = _i64
+    lib.oracle_copy_blocks.argtypes = [_p, _i64, _p] + [_i64] * 9
     lib.oracle_decode_attention.restype = ctypes.c_int
     lib.oracle_decode_attention.argtypes = [_p] * 6 + [ctypes.c_double] + [_i64] * 7 + [_p, _i64]
     return lib
@@ -105,6 +107,20 @@ def cache_write(cache: np.ndarray, src: np.ndarray, slot_mapping: np.ndarray, *,
         layer_stride, block_stride, row_width, block_size, num_blocks)
     if n < 0:
         raise ValueError(f"oracle_cache_write failed with status {n}")
+    return n
+
+
+def copy_blocks(cache: np.ndarray, pairs, *, offset: int, layer: int, num_layers: int,
+                layer_stride: int, block_stride: int, row_width: int, block_size: int,
+                num_blocks: int, lib=None) -> int:
+    """Copy whole block pages (uint8 ``cache``, in place) for each (src, dst) pair."""
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    pa = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    n = (lib or _load()).oracle_copy_blocks(
+        _ptr(cache), cache.nbytes, _ptr(pa), pa.shape[0], offset, layer, num_layers,
+        layer_stride, block_stride, row_width, block_size, num_blocks)
+    if n < 0:
+        raise ValueError(f"oracle_copy_blocks failed with status {n}")
     return n
 
 

@@ -114,6 +114,35 @@ int64_t oracle_cache_write(uint8_t *cache, int64_t cache_bytes, const uint8_t *s
     return written;
 }
 
+/* Copy on write ("vLLM 技术内幕" §2.2): for each (src, dst) pair and each
+ * of num_layers layers starting at `layer`, the page of block_size*row_width
+ * bytes of block src is copied to block dst.  src == dst copies nothing.
+ * Returns the number of pages copied, or ORC_ERR_RANGE for an id outside
+ * [0, num_blocks) or a page outside the cache (nothing after it is copied). */
+int64_t oracle_copy_blocks(uint8_t *cache, int64_t cache_bytes, const int64_t *pairs,
+                           int64_t num_pairs, int64_t offset, int64_t layer, int64_t num_layers,
+                           int64_t layer_stride, int64_t block_stride, int64_t row_width,
+                           int64_t block_size, int64_t num_blocks)
+{
+    int64_t page = block_size * row_width, copied = 0;
+    for (int64_t p = 0; p < num_pairs; ++p) {
+        int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+            return ORC_ERR_RANGE;
+        if (src == dst)
+            continue;
+        for (int64_t l = layer; l < layer + num_layers; ++l) {
+            int64_t a = offset + l * layer_stride + src * block_stride;
+            int64_t b = offset + l * layer_stride + dst * block_stride;
+            if (a < 0 || b < 0 || a + page > cache_bytes || b + page > cache_bytes)
+                return ORC_ERR_RANGE;
+            memcpy(cache + b, cache + a, (size_t)page);
+            ++copied;
+        }
+    }
+    return copied;
+}
+
 /* ------------------------------------------------------------------------ */
 /* The read side: paged decode attention, one query token per sequence. */
 

@@ -14,7 +14,7 @@ import ctypes
 import os
 
 __all__ = [
-    "PkvError", "pkv_view", "pkv_decode_options", "library_path", "load",
+    "PkvError", "pkv_view", "pkv_write_desc", "pkv_decode_options", "library_path", "load",
     "pkv_cache_write", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_get_device_error", "pkv_status_string",
     "pkv_last_error_string", "pkv_version", "EXPORTED_SYMBOLS",
@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = [
     "pkv_cache_write", "pkv_decode_attention", "pkv_decode_attention_ex",
     "pkv_decode_workspace_bytes", "pkv_decode_workspace_bytes_ex", "pkv_decode_workspace_init",
     "pkv_get_device_error", "pkv_status_string", "pkv_last_error_string", "pkv_version",
-    "pkv_decode_attention_noalloc",
+    "pkv_decode_attention_noalloc", "pkv_cache_write_multi", "pkv_copy_blocks",
 ]
 
 
@@ -50,6 +50,10 @@ class pkv_view(ctypes.Structure):
     _fields_ = [("offset", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
                 ("block_stride", ctypes.c_int64), ("row_width", ctypes.c_int64),
                 ("layer", ctypes.c_int32)]
+
+
+class pkv_write_desc(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_void_p), ("cache", ctypes.c_void_p), ("view", pkv_view)]
 
 
 class pkv_decode_options(ctypes.Structure):
@@ -73,6 +77,11 @@ def load(path: str | None = None):
     lib = ctypes.CDLL(path)
     lib.pkv_cache_write.restype = ctypes.c_int
     lib.pkv_cache_write.argtypes = [_p, _p, _p, _i64, _p, _p, pkv_view, _i32, _i64, _p]
+    lib.pkv_cache_write_multi.restype = ctypes.c_int
+    lib.pkv_cache_write_multi.argtypes = [ctypes.POINTER(pkv_write_desc), _i32, _p, _i64, _i32,
+                                          _i64, _p]
+    lib.pkv_copy_blocks.restype = ctypes.c_int
+    lib.pkv_copy_blocks.argtypes = [_p, pkv_view, _i32, _i32, _p, _i64, _i64, _p]
     dec = [_p, _p, _p, _p, _p, _p, ctypes.c_float, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
            _i64, _p, _sz]
     lib.pkv_decode_attention.restype = ctypes.c_int
@@ -152,6 +161,45 @@ def pkv_cache_write(k, v, slot_mapping, k_cache, v_cache, view, block_size: int,
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), view, block_size, num_blocks,
         _stream(stream))
     return _check(st, "pkv_cache_write") if check else st
+
+
+def _as_view(view) -> pkv_view:
+    if isinstance(view, pkv_view):
+        return view
+    return pkv_view(view.offset, view.layer_stride, view.block_stride, view.row_width,
+                    getattr(view, "layer", 0))
+
+
+def pkv_cache_write_multi(writes, slot_mapping, block_size: int, num_blocks: int, stream=None,
+                          check: bool = True) -> int:
+    """One launch for several writes sharing ``slot_mapping``: see pkv_cache_write_multi.
+
+    writes: sequence of (src, cache, view) with CUDA tensors and pkv_view-like views.
+    """
+    import torch
+    n = slot_mapping.numel()
+    arr = (pkv_write_desc * max(1, len(writes)))()
+    for i, (src, cache, view) in enumerate(writes):
+        view = _as_view(view)
+        if src.numel() * src.element_size() != n * view.row_width:
+            raise ValueError(f"write {i}: src must hold num_tokens rows of row_width bytes")
+        arr[i] = pkv_write_desc(_dev(src, f"writes[{i}].src"), _dev(cache, f"writes[{i}].cache"),
+                                view)
+    st = load().pkv_cache_write_multi(arr, len(writes),
+                                      _dev(slot_mapping, "slot_mapping", torch.int64), n,
+                                      block_size, num_blocks, _stream(stream))
+    return _check(st, "pkv_cache_write_multi") if check else st
+
+
+def pkv_copy_blocks(cache, view, num_layers: int, block_size: int, block_mapping,
+                    num_blocks: int, stream=None, check: bool = True) -> int:
+    """Copy whole blocks of a view for each (src, dst) row of ``block_mapping``
+    (CUDA int64 [N, 2]): see pkv_copy_blocks in pagedkv.h."""
+    import torch
+    st = load().pkv_copy_blocks(_dev(cache, "cache"), _as_view(view), num_layers, block_size,
+                                _dev(block_mapping, "block_mapping", torch.int64),
+                                block_mapping.numel() // 2, num_blocks, _stream(stream))
+    return _check(st, "pkv_copy_blocks") if check else st
 
 
 def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float,

@@ -10,8 +10,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (PKV_COMPUTE_AUTO, PKV_SCHEDULE_AUTO, pkv_cache_write, pkv_decode_attention,
-               pkv_decode_workspace_bytes, pkv_view)
+from . import (PKV_COMPUTE_AUTO, PKV_SCHEDULE_AUTO, pkv_cache_write, pkv_cache_write_multi,
+               pkv_decode_attention, pkv_decode_workspace_bytes, pkv_view)
 from .workloads import DecodeWorkload, WriteWorkload
 
 
@@ -128,6 +128,18 @@ class DeviceWrite:
                                 self.wl.block_size, self.wl.num_blocks, stream=stream)
                 n += 1
         return n
+
+    def write_layout_batched(self, layout: str, stream=None) -> int:
+        """All (cache, layer) writes of one layout in one launch."""
+        writes = []
+        for c, v in self.wl.views[layout].items():
+            for layer in range(self.wl.num_layers):
+                writes.append((self.rows[(c, layer)], self.cache,
+                               pkv_view(v.offset, v.layer_stride, v.block_stride, v.row_width,
+                                        layer)))
+        pkv_cache_write_multi(writes, self.slot_mapping, self.wl.block_size, self.wl.num_blocks,
+                              stream=stream)
+        return 1
 
     def layout_bytes(self, layout: str) -> int:
         t = self.wl.slot_mapping.size

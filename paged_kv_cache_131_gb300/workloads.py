@@ -186,6 +186,8 @@ class DecodeWorkload:
     v_new: np.ndarray | None
     slot_mapping: np.ndarray | None  # int64 [T]
     ref_cnt: np.ndarray | None = None
+    cow_pairs: np.ndarray | None = None  # int64 [n, 2] (shared block, private copy)
+    shared_prefix_tokens: int = 0
 
     @property
     def num_seqs(self) -> int:
@@ -277,7 +279,8 @@ def _decode_workload(name, rng, seq_lens, *, H, Hk, D, bs, NB, write_last=True,
         k_new = fp16_normal(rng, (len(live), row))
         v_new = fp16_normal(rng, (len(live), row))
     return DecodeWorkload(name, H, Hk, D, bs, NB, 1.0 / math.sqrt(D), seq_lens, tables, q,
-                          k_cache, v_cache, k_new, v_new, slot_mapping, pool.ref_cnt.copy())
+                          k_cache, v_cache, k_new, v_new, slot_mapping, pool.ref_cnt.copy(),
+                          np.asarray(cows, dtype=np.int64).reshape(-1, 2), shared_prefix_tokens)
 
 
 def config1_tiny() -> DecodeWorkload:

@@ -51,6 +51,11 @@ MUTATIONS = {
         ("q[(i * num_heads + h) * head_dim + d]", "q[(h * num_seqs + i) * head_dim + d]"),
     "negative slots not skipped":
         ("if (slot < 0)\n            continue;", "if (slot < -1000)\n            continue;"),
+    "copy on write copies the wrong way":
+        ("memcpy(cache + b, cache + a, (size_t)page);", "memcpy(cache + a, cache + b, (size_t)page);"),
+    "copy on write ignores the layer":
+        ("int64_t a = offset + l * layer_stride + src * block_stride;",
+         "int64_t a = offset + src * block_stride;"),
 }
 
 
@@ -66,6 +71,7 @@ def _pins(orc, lib):
     yield lambda: P.test_decode_special_cases(orc, lib=lib)
     yield lambda: P.test_decode_gqa_equals_mha_with_duplicated_kv(orc, lib=lib)
     yield lambda: P.test_decode_bad_block_id_is_an_error(orc, lib=lib)
+    yield lambda: P.test_copy_blocks_pages_only(orc, lib=lib)
     for case in (dict(index=102, lens=[3, 20, 40], H=4, Hk=2, D=8),
                  dict(index=103, lens=[0, 2, 31], H=8, Hk=1, D=4)):
         yield lambda case=case: P.test_decode_matches_brute_force(orc, case, lib=lib)

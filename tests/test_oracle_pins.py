@@ -367,3 +367,38 @@ def test_decode_bad_block_id_is_an_error(orc, lib=None):
     bt[0, 1] = wl.num_blocks
     with pytest.raises(ValueError):
         orc.decode_attention(wl.q, wl.k_cache, wl.v_cache, bt, wl.seq_lens, wl.scale, lib=lib)
+
+
+# ---------------------------------------------------------------- copy on write
+
+
+def test_copy_blocks_pages_only(orc, lib=None):
+    """Each pair copies exactly the page (block_size * row_width bytes) of every
+    requested layer of the source block onto the destination block; nothing
+    else changes; src == dst is a no-op (block-outer two-layer view)."""
+    rng = np.random.default_rng(11)
+    bs, R, NB, L = 4, 12, 6, 3
+    page = bs * R
+    block_stride = L * page + 8          # block-outer, with a gap after each block
+    layer_stride = page
+    total = NB * block_stride
+    init = rng.integers(0, 256, size=total, dtype=np.uint8)
+    cache = init.copy()
+    pairs = [(1, 4), (2, 2), (5, 0)]
+    n = orc.copy_blocks(cache, pairs, offset=0, layer=1, num_layers=2, layer_stride=layer_stride,
+                        block_stride=block_stride, row_width=R, block_size=bs, num_blocks=NB,
+                        lib=lib)
+    assert n == 4
+    exp = init.copy()
+    for s, d in pairs:
+        if s == d:
+            continue
+        for layer in (1, 2):
+            a = layer * layer_stride + s * block_stride
+            b = layer * layer_stride + d * block_stride
+            exp[b:b + page] = init[a:a + page]
+    assert np.array_equal(cache, exp)
+    with pytest.raises(ValueError):
+        orc.copy_blocks(cache, [(0, NB)], offset=0, layer=0, num_layers=1,
+                        layer_stride=layer_stride, block_stride=block_stride, row_width=R,
+                        block_size=bs, num_blocks=NB, lib=lib)
