@@ -62,6 +62,16 @@ def _bind(lib):
     lib.oracle_split_slot.argtypes = [_i64, _i64, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
     lib.oracle_cache_write.restype = _i64
     lib.oracle_cache_write.argtypes = [_p, _i64, _p, _p, _i64] + [_i64] * 7
+    lib.oracle_e4m3_value.restype = ctypes.c_double
+    lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_quantize_row.restype = None
+    lib.oracle_quantize_row.argtypes = [_p, _i64, _p, _p]
+    lib.oracle_cache_write_fp8.restype = _i64
+    lib.oracle_cache_write_fp8.argtypes = [_p, _p, _p, _p] + [_i64] * 5
+    lib.oracle_decode_attention_fp8.restype = ctypes.c_int
+    lib.oracle_decode_attention_fp8.argtypes = [_p] * 8 + [ctypes.c_double] + [_i64] * 7 + [_p, _i64]
     lib.oracle_copy_blocks.restype = _i64
     lib.oracle_copy_blocks.argtypes = [_p, _i64, _p] + [_i64] * 9
     lib.oracle_decode_attention.restype = ctypes.c_int
@@ -153,4 +163,68 @@ def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
         S, H, Hk, D, bs, bt.shape[1], NB, pp, npairs)
     if st != 0:
         raise ValueError(f"oracle_decode_attention failed with status {st}")
+    return out
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+
+
+def e4m3_value(code: int, lib=None) -> float:
+    return (lib or _load()).oracle_e4m3_value(int(code) & 0xFF)
+
+
+def e4m3_encode(y: float, lib=None) -> int:
+    return (lib or _load()).oracle_e4m3_encode(float(y))
+
+
+def quantize_row(x: np.ndarray, lib=None):
+    """fp16 row -> (uint8 E4M3 codes, fp32 scale)."""
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    codes = np.empty(x.size, dtype=np.uint8)
+    sc = ctypes.c_float()
+    (lib or _load()).oracle_quantize_row(_ptr(x), x.size, _ptr(codes), ctypes.byref(sc))
+    return codes, sc.value
+
+
+def cache_write_fp8(cache: np.ndarray, scales: np.ndarray, src: np.ndarray,
+                    slot_mapping: np.ndarray, *, block_size: int, lib=None) -> int:
+    """Quantize fp16 rows src [T, Hk, D] into cache uint8 [NB, bs, Hk, D] and
+    scales fp32 [NB, bs, Hk] (both in place)."""
+    assert cache.dtype == np.uint8 and scales.dtype == np.float32
+    assert cache.flags.c_contiguous and scales.flags.c_contiguous
+    NB, bs, Hk, D = cache.shape
+    assert bs == block_size and scales.shape == (NB, bs, Hk)
+    src = np.ascontiguousarray(src, dtype=np.float16).reshape(-1, Hk, D)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    assert src.shape[0] == slots.size
+    n = (lib or _load()).oracle_cache_write_fp8(_ptr(cache), _ptr(scales), _ptr(src),
+                                                _ptr(slots), slots.size, Hk, D, bs, NB)
+    if n < 0:
+        raise ValueError(f"oracle_cache_write_fp8 failed with status {n}")
+    return n
+
+
+def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                         scale: float, *, pairs=None, lib=None) -> np.ndarray:
+    """Textbook paged decode attention in float64 over E4M3 caches (dequantized
+    exactly: value(code) * scale of the row)."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    S, H, D = q.shape
+    NB, bs, Hk, D2 = k_cache.shape
+    assert D2 == D and k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    assert k_scale.dtype == np.float32 and k_scale.shape == (NB, bs, Hk)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.full((S, H, D), np.nan, dtype=np.float64)
+    if pairs is None:
+        pp, npairs = None, 0
+    else:
+        pa = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        pp, npairs = _ptr(pa), pa.shape[0]
+    st = (lib or _load()).oracle_decode_attention_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _ptr(bt), _ptr(sl), float(scale), S, H, Hk, D, bs, bt.shape[1], NB, pp, npairs)
+    if st != 0:
+        raise ValueError(f"oracle_decode_attention_fp8 failed with status {st}")
     return out

@@ -65,6 +65,76 @@ double oracle_half_to_double(uint16_t h)
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP8 KV ("deep-dive-into-vllm-05" §3.4: quantize on write, dequantize on
+ * read, the scale kept with the block; "vLLM KV Cache Layout 可视化" -- 两种
+ * cache: a row of 128 FP8 values carries one FP32 scale).  Format E4M3 as in
+ * the OCP 8-bit floating-point specification: 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN, largest
+ * finite magnitude 448. */
+
+/* Value of an E4M3 code. */
+double oracle_e4m3_value(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int expo = (code >> 3) & 0xf;
+    int mant = code & 0x7;
+    double mag;
+    if (expo == 15 && mant == 7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)mant, -9); /* (mant / 8) * 2^(1-7) */
+    else
+        mag = ldexp((double)(8 + mant), expo - 10); /* (1 + mant/8) * 2^(expo-7) */
+    return sign ? -mag : mag;
+}
+
+/* Nearest E4M3 code to y, ties to the even code, magnitudes above 448
+ * saturating to 448; NaN gives 0x7F.  A brute-force search over the 127
+ * non-negative finite codes. */
+uint8_t oracle_e4m3_encode(float y)
+{
+    if (isnan(y))
+        return 0x7f;
+    double a = fabs((double)y);
+    if (a > 448.0)
+        a = 448.0;
+    int best = 0;
+    double best_err = a;
+    for (int c = 1; c <= 126; ++c) {
+        double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)((signbit(y) ? 0x80 : 0) | best);
+}
+
+/* One row of n fp16 values -> n E4M3 codes and one fp32 scale, all in fp32:
+ * amax = max |x|, s = amax / 448, code = encode(x / s); s == 0 gives zero
+ * codes.  (The pages leave the granularity open; one scale per row of a KV
+ * head is our reading, matching the per-token scale of their indexer rows.) */
+void oracle_quantize_row(const uint16_t *x, int64_t n, uint8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float v = (float)fabs(oracle_half_to_double(x[i]));
+        if (v > amax)
+            amax = v;
+    }
+    float s = amax / 448.0f;
+    *scale = s;
+    for (int64_t i = 0; i < n; ++i) {
+        if (s == 0.0f) {
+            codes[i] = 0;
+        } else {
+            float xi = (float)oracle_half_to_double(x[i]);
+            codes[i] = oracle_e4m3_encode(xi / s);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* The write side ("vLLM KV Cache Layout 可视化", 核心 and "kernel 那一侧"). */
 
 /* Split a slot back into (physical block, position inside the block). */
@@ -110,6 +180,35 @@ int64_t oracle_cache_write(uint8_t *cache, int64_t cache_bytes, const uint8_t *s
             return ORC_ERR_RANGE;
         memcpy(cache + addr, src + t * row_width, (size_t)row_width);
         ++written;
+    }
+    return written;
+}
+
+/* Quantize-on-write of fp16 rows [num_tokens][num_kv_heads][head_dim] into
+ * an E4M3 cache [num_blocks][block_size][num_kv_heads][head_dim] (bytes)
+ * and fp32 scales [num_blocks][block_size][num_kv_heads]: each (token, head)
+ * row is quantized by oracle_quantize_row and stored at its slot.  Negative
+ * slots are skipped.  Returns rows written or ORC_ERR_RANGE. */
+int64_t oracle_cache_write_fp8(uint8_t *cache, float *scales, const uint16_t *src,
+                               const int64_t *slot_mapping, int64_t num_tokens,
+                               int64_t num_kv_heads, int64_t head_dim, int64_t block_size,
+                               int64_t num_blocks)
+{
+    int64_t written = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_blocks * block_size)
+            return ORC_ERR_RANGE;
+        int64_t block, in_block;
+        oracle_split_slot(slot, block_size, &block, &in_block);
+        for (int64_t h = 0; h < num_kv_heads; ++h) {
+            int64_t row = (block * block_size + in_block) * num_kv_heads + h;
+            oracle_quantize_row(src + (t * num_kv_heads + h) * head_dim, head_dim,
+                                cache + row * head_dim, scales + row);
+            ++written;
+        }
     }
     return written;
 }
@@ -257,6 +356,78 @@ int oracle_decode_attention(double *out, const uint16_t *q, const uint16_t *k_ca
                                                        num_kv_heads, head_dim);
                         V[j * head_dim + d] = cache_at(v_cache, phys, in_block, kvh, d, block_size,
                                                        num_kv_heads, head_dim);
+                    }
+                }
+                for (int64_t g = 0; g < group && status == ORC_OK; ++g) {
+                    int64_t h = kvh * group + g;
+                    int wanted = !pairs;
+                    for (int64_t p = 0; pairs && p < num_pairs; ++p)
+                        if (pairs[2 * p] == i && pairs[2 * p + 1] == h)
+                            wanted = 1;
+                    if (!wanted)
+                        continue;
+                    for (int64_t d = 0; d < head_dim; ++d)
+                        qd[d] = oracle_half_to_double(q[(i * num_heads + h) * head_dim + d]);
+                    textbook_attention(out + (i * num_heads + h) * head_dim, qd, K, V, len,
+                                       head_dim, scale, scores);
+                }
+            }
+            free(K);
+            free(V);
+            free(scores);
+            free(qd);
+        }
+    }
+    return status;
+}
+
+/* Paged decode attention over an E4M3 cache: the same textbook computation as
+ * oracle_decode_attention with each key/value element dequantized exactly
+ * (value(code) * scale of its (token, head) row, in float64). */
+int oracle_decode_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
+                                const uint8_t *v_cache, const float *k_scale,
+                                const float *v_scale, const int32_t *block_tables,
+                                const int32_t *seq_lens, double scale, int64_t num_seqs,
+                                int64_t num_heads, int64_t num_kv_heads, int64_t head_dim,
+                                int64_t block_size, int64_t max_blocks_per_seq,
+                                int64_t num_blocks, const int32_t *pairs, int64_t num_pairs)
+{
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks_per_seq < 0 || num_seqs < 0)
+        return ORC_ERR_ARG;
+    int64_t group = num_heads / num_kv_heads;
+    int status = ORC_OK;
+    for (int64_t i = 0; i < num_seqs && status == ORC_OK; ++i) {
+        int64_t len = seq_lens[i];
+        if (len < 0 || len > max_blocks_per_seq * block_size)
+            return ORC_ERR_RANGE;
+        for (int64_t kvh = 0; kvh < num_kv_heads && status == ORC_OK; ++kvh) {
+            int want_any = !pairs;
+            for (int64_t p = 0; pairs && p < num_pairs; ++p)
+                if (pairs[2 * p] == i && pairs[2 * p + 1] / group == kvh)
+                    want_any = 1;
+            if (!want_any)
+                continue;
+            size_t n = (size_t)(len > 0 ? len : 1) * (size_t)head_dim;
+            double *K = (double *)malloc(n * sizeof(double));
+            double *V = (double *)malloc(n * sizeof(double));
+            double *scores = (double *)malloc((size_t)(len > 0 ? len : 1) * sizeof(double));
+            double *qd = (double *)malloc((size_t)head_dim * sizeof(double));
+            if (!K || !V || !scores || !qd) {
+                status = ORC_ERR_NOMEM;
+            } else {
+                for (int64_t j = 0; j < len && status == ORC_OK; ++j) {
+                    int64_t phys = block_tables[i * max_blocks_per_seq + j / block_size];
+                    if (phys < 0 || phys >= num_blocks) {
+                        status = ORC_ERR_RANGE;
+                        break;
+                    }
+                    int64_t row = (phys * block_size + j % block_size) * num_kv_heads + kvh;
+                    for (int64_t d = 0; d < head_dim; ++d) {
+                        K[j * head_dim + d] =
+                            oracle_e4m3_value(k_cache[row * head_dim + d]) * (double)k_scale[row];
+                        V[j * head_dim + d] =
+                            oracle_e4m3_value(v_cache[row * head_dim + d]) * (double)v_scale[row];
                     }
                 }
                 for (int64_t g = 0; g < group && status == ORC_OK; ++g) {

@@ -11,6 +11,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_fp8 as F
 import test_oracle_pins as P
 from paged_kv_cache_131_gb300 import workloads as W
 
@@ -53,6 +54,22 @@ MUTATIONS = {
         ("if (slot < 0)\n            continue;", "if (slot < -1000)\n            continue;"),
     "copy on write copies the wrong way":
         ("memcpy(cache + b, cache + a, (size_t)page);", "memcpy(cache + a, cache + b, (size_t)page);"),
+    "E4M3 exponent bias off by one":
+        ("ldexp((double)(8 + mant), expo - 10)", "ldexp((double)(8 + mant), expo - 9)"),
+    "E4M3 subnormal scale wrong":
+        ("mag = ldexp((double)mant, -9);", "mag = ldexp((double)mant, -8);"),
+    "E4M3 ties to odd":
+        ("(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0"),
+    "FP8 scale for a 240 maximum":
+        ("float s = amax / 448.0f;", "float s = amax / 240.0f;"),
+    "FP8 quantizer multiplies by the scale":
+        ("oracle_e4m3_encode(xi / s)", "oracle_e4m3_encode(xi * s)"),
+    "FP8 decode ignores the value scale":
+        ("oracle_e4m3_value(v_cache[row * head_dim + d]) * (double)v_scale[row]",
+         "oracle_e4m3_value(v_cache[row * head_dim + d]) * 1.0"),
+    "FP8 decode scales values by the key scale":
+        ("oracle_e4m3_value(v_cache[row * head_dim + d]) * (double)v_scale[row]",
+         "oracle_e4m3_value(v_cache[row * head_dim + d]) * (double)k_scale[row]"),
     "copy on write ignores the layer":
         ("int64_t a = offset + l * layer_stride + src * block_stride;",
          "int64_t a = offset + src * block_stride;"),
@@ -72,6 +89,11 @@ def _pins(orc, lib):
     yield lambda: P.test_decode_gqa_equals_mha_with_duplicated_kv(orc, lib=lib)
     yield lambda: P.test_decode_bad_block_id_is_an_error(orc, lib=lib)
     yield lambda: P.test_copy_blocks_pages_only(orc, lib=lib)
+    yield lambda: F.test_e4m3_code_table(orc, lib=lib)
+    yield lambda: F.test_e4m3_rounding_matches_library(orc, lib=lib)
+    yield lambda: F.test_quantize_row_properties(orc, lib=lib)
+    yield lambda: F.test_cache_write_fp8_rows_and_untouched(orc, lib=lib)
+    yield lambda: F.test_decode_fp8_reduces_to_fp16_oracle(orc, lib=lib)
     for case in (dict(index=102, lens=[3, 20, 40], H=4, Hk=2, D=8),
                  dict(index=103, lens=[0, 2, 31], H=8, Hk=1, D=4)):
         yield lambda case=case: P.test_decode_matches_brute_force(orc, case, lib=lib)
