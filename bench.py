@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
     ap.add_argument("--compute", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--schedule", choices=["auto", "grid", "balanced"], default="auto")
+    ap.add_argument("--kv", choices=["fp16", "fp8"], default="fp16",
+                    help="KV cache format (fp8: E4M3 codes + per-row fp32 scales)")
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
@@ -295,16 +297,24 @@ def main():
         dist.barrier()
     compute = {"auto": 0, "simt": 1, "mma": 2}[args.compute]
     schedule = {"auto": 0, "grid": 1, "balanced": 2}[args.schedule]
-    dev = DeviceDecode(wl, device=f"cuda:{local}", partition_size=args.partition, compute=compute,
-                       schedule=schedule)
+    if args.kv == "fp8":
+        from paged_kv_cache_131_gb300.harness import DeviceDecodeFp8
+        dev = DeviceDecodeFp8(wl, device=f"cuda:{local}")
+    else:
+        dev = DeviceDecode(wl, device=f"cuda:{local}", partition_size=args.partition,
+                           compute=compute, schedule=schedule)
     flush = L2Flush(f"cuda:{local}")
     stream = torch.cuda.current_stream()
 
-    kv_bytes = wl.kv_bytes()
+    kv_bytes = dev.kv_bytes() if args.kv == "fp8" else wl.kv_bytes()
     S, H, D = wl.num_seqs, wl.num_heads, wl.head_dim
     nblk = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
     decode_alg_bytes = kv_bytes + S * H * D * 2 * 2 + nblk * 4 + S * 4
-    write_bytes = dev.write_bytes()
+    if args.kv == "fp8":
+        t = wl.slot_mapping.size if dev.has_write else 0
+        write_bytes = t * wl.num_kv_heads * (wl.head_dim * 3 + 4) * 2 + 8 * t
+    else:
+        write_bytes = dev.write_bytes()
     launches_per_step = (1 if dev.has_write else 0) + 1
 
     for _ in range(args.warmup):
@@ -351,7 +361,7 @@ def main():
         dist.barrier()
 
     # end to end through the public API: pinned host inputs in, output out
-    e2e = e2e_measure(dev, wl, args.e2e_steps, stream, flush)
+    e2e = e2e_measure(dev, wl, args.e2e_steps, stream, flush) if args.kv == "fp16" else None
 
     if rank != 0:
         if dist is not None:
@@ -378,14 +388,14 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16xf16->f32",
+        "dtype": "f16xf16->f32" if args.kv == "fp16" else "e4m3 KV (dequantized to f16) -> f32",
         "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
         "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": S * world,
                    "seq_len": int(wl.max_seq_len), "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (write a 2x L2 buffer, then read another "
                          "2x L2 buffer: cold, clean L2); KV read per step > L2",
                    "kv_cache": "resident in HBM (state), not copied per step",
-                   "compute": args.compute, "schedule": args.schedule},
+                   "compute": args.compute, "schedule": args.schedule, "kv": args.kv},
         "pct_hbm_peak": round(100 * value / world / peak, 2),
         "seqs_per_s": round(world * S / (step_ms * 1e-3), 1),
         "decode_tokens_per_s": round(world * S / (step_ms * 1e-3), 1),
@@ -395,11 +405,13 @@ def main():
         "wall_s_timed_loop": round(t_wall, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(f"config{args.config}"),
+                     "traffic": recorded_traffic(f"config{args.config}") if args.kv == "fp16"
+                     else None,
                      "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                      "kernel": ("decode_grid_kernel" if schedule == 1 else
                                 "decode_balanced_kernel") +
-                               (" (SIMT policy)" if compute == 1 else " (MMA policy)"),
+                               (" (FP8 MMA policy)" if args.kv == "fp8" else
+                                " (SIMT policy)" if compute == 1 else " (MMA policy)"),
                      "alg_bytes_per_launch": decode_alg_bytes},
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -254,6 +254,44 @@ size_t pkv_decode_workspace_bytes_ex(int32_t num_seqs, int32_t num_heads, int32_
                                      int32_t head_dim, int32_t max_seq_len,
                                      int32_t partition_size);
 
+/*
+ * FP8 KV cache ("deep-dive-into-vllm-05" §3.4: quantize on write -- the KV is
+ * stored at low precision when written -- and dequantize on read inside the
+ * attention kernel; the scales stay with the blocks).  Format: E4M3 (OCP
+ * FP8: 4 exponent bits, bias 7, 3 mantissa bits, largest finite 448), one
+ * fp32 scale per (token, KV head) row -- the pages' indexer rows carry one
+ * FP32 scale per 128 FP8 values ("vLLM KV Cache Layout 可视化").
+ *
+ * Caches: k_cache, v_cache uint8 [num_blocks, block_size, num_kv_heads,
+ * head_dim]; k_scale, v_scale fp32 [num_blocks, block_size, num_kv_heads].
+ *
+ * pkv_cache_write_fp8 quantizes fp16 rows k, v [num_tokens, num_kv_heads,
+ * head_dim] into their slots, in fp32: amax = max |x| of the row,
+ * s = amax / 448, code = round-to-nearest-even(x / s) saturated to +-448
+ * (s == 0 gives zero codes).  Slot rules and errors as pkv_cache_write;
+ * head_dim in {64, 128}; v, v_cache, v_scale all NULL or all set.
+ */
+int pkv_cache_write_fp8(const void *k, const void *v, const int64_t *slot_mapping,
+                        int64_t num_tokens, void *k_cache, void *v_cache, float *k_scale,
+                        float *v_scale, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int64_t num_blocks, pkv_stream_t stream);
+
+/*
+ * pkv_decode_attention over FP8 caches (balanced schedule, MMA policy): keys
+ * and values are dequantized as value(code) * scale of their row; the result
+ * is the attention of pkv_decode_attention on those values.  Needs
+ * num_kv_heads <= 8, 16-byte aligned caches and scales, and a workspace of
+ * pkv_decode_workspace_bytes(...) bytes (zero-filled before first use, left
+ * zero-filled).  Other arguments and errors as pkv_decode_attention.
+ */
+int pkv_decode_attention_fp8(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const float *k_scale, const float *v_scale,
+                             const int32_t *block_tables, const int32_t *seq_lens, float scale,
+                             int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_seqs, int32_t max_blocks_per_seq,
+                             int32_t max_seq_len, int64_t num_blocks, void *workspace,
+                             size_t workspace_bytes, pkv_stream_t stream);
+
 /* Bytes of the built-in scratch of pkv_decode_attention_noalloc (16 MiB). */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = [
     "pkv_decode_workspace_bytes", "pkv_decode_workspace_bytes_ex", "pkv_decode_workspace_init",
     "pkv_get_device_error", "pkv_status_string", "pkv_last_error_string", "pkv_version",
     "pkv_decode_attention_noalloc", "pkv_cache_write_multi", "pkv_copy_blocks",
+    "pkv_cache_write_fp8", "pkv_decode_attention_fp8",
 ]
 
 
@@ -80,6 +81,9 @@ def load(path: str | None = None):
     lib.pkv_cache_write_multi.restype = ctypes.c_int
     lib.pkv_cache_write_multi.argtypes = [ctypes.POINTER(pkv_write_desc), _i32, _p, _i64, _i32,
                                           _i64, _p]
+    lib.pkv_cache_write_fp8.restype = ctypes.c_int
+    lib.pkv_cache_write_fp8.argtypes = [_p, _p, _p, _i64, _p, _p, _p, _p, _i32, _i32, _i32, _i64,
+                                        _p]
     lib.pkv_copy_blocks.restype = ctypes.c_int
     lib.pkv_copy_blocks.argtypes = [_p, pkv_view, _i32, _i32, _p, _i64, _i64, _p]
     dec = [_p, _p, _p, _p, _p, _p, ctypes.c_float, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
@@ -88,6 +92,8 @@ def load(path: str | None = None):
     lib.pkv_decode_attention.argtypes = dec + [_p]
     lib.pkv_decode_attention_ex.restype = ctypes.c_int
     lib.pkv_decode_attention_ex.argtypes = dec + [ctypes.POINTER(pkv_decode_options), _p]
+    lib.pkv_decode_attention_fp8.restype = ctypes.c_int
+    lib.pkv_decode_attention_fp8.argtypes = dec[:4] + [_p, _p] + dec[4:] + [_p]
     lib.pkv_decode_attention_noalloc.restype = ctypes.c_int
     lib.pkv_decode_attention_noalloc.argtypes = dec[:15] + [_p]
     lib.pkv_decode_workspace_bytes.restype = _sz
@@ -233,6 +239,38 @@ def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, seq_lens, scale
         opts = pkv_decode_options(partition_size, compute, schedule)
         st = lib.pkv_decode_attention_ex(*args, ctypes.byref(opts), _stream(stream))
     return _check(st, "pkv_decode_attention") if check else st
+
+
+def pkv_cache_write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, block_size: int,
+                        num_blocks: int, stream=None, check: bool = True) -> int:
+    """Quantize-on-write of fp16 rows k, v [T, Hk, D] into E4M3 caches
+    (uint8 [NB, bs, Hk, D]) and fp32 scales [NB, bs, Hk]: see pagedkv.h."""
+    import torch
+    NB, bs, Hk, D = k_cache.shape
+    st = load().pkv_cache_write_fp8(
+        _dev(k, "k", torch.float16), _dev(v, "v", torch.float16),
+        _dev(slot_mapping, "slot_mapping", torch.int64), slot_mapping.numel(),
+        _dev(k_cache, "k_cache", torch.uint8), _dev(v_cache, "v_cache", torch.uint8),
+        _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        Hk, D, block_size, num_blocks, _stream(stream))
+    return _check(st, "pkv_cache_write_fp8") if check else st
+
+
+def pkv_decode_attention_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                             scale: float, num_heads: int, num_kv_heads: int, head_dim: int,
+                             block_size: int, max_seq_len: int, num_blocks: int, workspace,
+                             stream=None, check: bool = True) -> int:
+    """Paged decode attention over E4M3 caches: see pkv_decode_attention_fp8."""
+    import torch
+    st = load().pkv_decode_attention_fp8(
+        _dev(out, "out", torch.float16), _dev(q, "q", torch.float16),
+        _dev(k_cache, "k_cache", torch.uint8), _dev(v_cache, "v_cache", torch.uint8),
+        _dev(k_scale, "k_scale", torch.float32), _dev(v_scale, "v_scale", torch.float32),
+        _dev(block_tables, "block_tables", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        float(scale), num_heads, num_kv_heads, head_dim, block_size, q.shape[0],
+        block_tables.shape[1], int(max_seq_len), int(num_blocks), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "pkv_decode_attention_fp8") if check else st
 
 
 def pkv_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,

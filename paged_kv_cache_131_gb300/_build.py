@@ -18,7 +18,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 HEADER = os.path.join(ROOT, "include", "pagedkv.h")
 
-SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_blocks.cu", "pkv_decode_api.cu", "pkv_decode_grid.cu",
+SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_write_fp8.cu", "pkv_blocks.cu", "pkv_decode_api.cu", "pkv_decode_grid.cu",
            "pkv_decode_balanced.cu", "pkv_decode_noalloc.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -45,9 +45,12 @@ size_t pkv_decode_workspace_bytes_ex(int32_t num_seqs, int32_t num_heads, int32_
         return 0;
     const int64_t grid_ws =
         grid_workspace_bytes(num_seqs, num_heads, head_dim, num_partitions(max_seq_len, pt));
-    const BalancedShape b =
-        balanced_shape(num_seqs, num_kv_heads, num_heads / num_kv_heads, head_dim, pkv::sm_count());
-    return static_cast<size_t>(std::max<int64_t>(grid_ws, b.ok ? b.workspace : 0));
+    const int G = num_heads / num_kv_heads;
+    const BalancedShape b = balanced_shape(num_seqs, num_kv_heads, G, head_dim, pkv::sm_count());
+    const BalancedShape b8 =
+        balanced_shape(num_seqs, num_kv_heads, G, head_dim, pkv::sm_count(), true);
+    return static_cast<size_t>(std::max<int64_t>(
+        {grid_ws, b.ok ? b.workspace : 0, b8.ok ? b8.workspace : 0}));
 }
 
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
@@ -129,7 +132,7 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
             p.num_kv_heads = num_kv_heads;
             p.max_blocks_per_seq = max_blocks_per_seq;
             p.num_stages = shape.stages;
-            p.pitch = num_kv_heads * head_dim * 2 + 16;
+            p.pitch = shape.pitch;
             p.num_blocks = num_blocks;
             uint8_t *ws = static_cast<uint8_t *>(workspace);
             const int64_t c_bytes = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
@@ -139,7 +142,7 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
             p.part_o = reinterpret_cast<float *>(ws + c_bytes + align256(slots * 8));
             p.err = device_error_record();
             if (p.err == nullptr) return PKV_ERR_CUDA;
-            return launch_balanced(p, shape, head_dim, G, simt, s);
+            return launch_balanced(p, shape, head_dim, G, simt, false, s);
         }
     }
 
@@ -193,3 +196,65 @@ int pkv_decode_attention(void *out, const void *q, const void *k_cache, const vo
 }
 
 }  // extern "C"
+
+extern "C" int pkv_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                                        const void *v_cache, const float *k_scale,
+                                        const float *v_scale, const int32_t *block_tables,
+                                        const int32_t *seq_lens, float scale, int32_t num_heads,
+                                        int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t block_size, int32_t num_seqs,
+                                        int32_t max_blocks_per_seq, int32_t max_seq_len,
+                                        int64_t num_blocks, void *workspace,
+                                        size_t workspace_bytes, pkv_stream_t stream) {
+    using namespace pkv;
+    using namespace pkv::dec;
+    if (num_seqs < 0) return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !seq_lens)
+        return PKV_ERR_NULL;
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len < 0 ||
+        !std::isfinite(scale))
+        return PKV_ERR_INVALID;
+    const int G = num_heads / num_kv_heads;
+    if (!(G == 1 || G == 2 || G == 4 || G == 8)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || !balanced_fits_index(num_seqs, max_blocks_per_seq))
+        return PKV_ERR_UNSUPPORTED;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_scale, 16) || !aligned(v_scale, 16) || !aligned(block_tables, 4) ||
+        !aligned(seq_lens, 4) || (workspace != nullptr && !aligned(workspace, 16)))
+        return PKV_ERR_ALIGNMENT;
+    const BalancedShape shape = balanced_shape(num_seqs, num_kv_heads, G, head_dim, sm_count(), true);
+    if (!shape.ok) return PKV_ERR_UNSUPPORTED;
+    if (workspace == nullptr || static_cast<int64_t>(workspace_bytes) < shape.workspace)
+        return PKV_ERR_WORKSPACE;
+    BalancedParams p{};
+    p.out = static_cast<__half *>(out);
+    p.q = static_cast<const __half *>(q);
+    p.k_cache = static_cast<const __half *>(k_cache);  // E4M3 bytes, read as such
+    p.v_cache = static_cast<const __half *>(v_cache);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_stages = shape.stages;
+    p.pitch = shape.pitch;
+    p.num_blocks = num_blocks;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t c_bytes = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
+    const int64_t slots = 2 * static_cast<int64_t>(shape.grid) * num_kv_heads * G;
+    p.counters = reinterpret_cast<int *>(ws);
+    p.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
+    p.part_o = reinterpret_cast<float *>(ws + c_bytes + align256(slots * 8));
+    p.err = device_error_record();
+    if (p.err == nullptr) return PKV_ERR_CUDA;
+    return launch_balanced(p, shape, head_dim, G, false, true,
+                           reinterpret_cast<cudaStream_t>(stream));
+}

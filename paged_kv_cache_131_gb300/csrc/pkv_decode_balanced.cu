@@ -38,6 +38,7 @@ namespace dec {
 namespace {
 
 constexpr int kMaxStages = 4;
+constexpr int kMaxStagesFp8 = 6;  // FP8 stages are half the size: keep as many bytes in flight
 constexpr int kMaxThreads = (kMaxBalancedKvHeads + 1) * 32;
 
 // Dynamic shared memory:
@@ -121,13 +122,15 @@ __device__ void combine_partials(const BalancedParams &p, int seq, int kvh, int 
     }
 }
 
-template <int D, int G, class Policy>
+template <int D, int G, class Policy, bool kFp8>
 __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const BalancedParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int Hk = p.num_kv_heads, S = p.num_seqs, NS = p.num_stages, H = p.num_heads;
     const int pitch = p.pitch;
     const int tile_bytes = kBS * pitch;
-    const int stage_bytes = 2 * tile_bytes;
+    // FP8: a stage also holds the block's key and value scales ([16][Hk] fp32 each)
+    const int scale_bytes = kFp8 ? kBS * Hk * 4 : 0;
+    const int stage_bytes = 2 * tile_bytes + 2 * scale_bytes;
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
     uint64_t *empty = full + NS;
@@ -226,8 +229,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
 
     if (warp == Hk) {
         // ================================ producer ================================
-        const int64_t row_elems = static_cast<int64_t>(Hk) * D;
-        const uint32_t row_bytes = static_cast<uint32_t>(Hk) * D * 2;
+        const int64_t row_bytes64 = static_cast<int64_t>(Hk) * D * (kFp8 ? 1 : 2);
+        const uint32_t row_bytes = static_cast<uint32_t>(row_bytes64);
+        const uint8_t *kbytes = reinterpret_cast<const uint8_t *>(p.k_cache);
+        const uint8_t *vbytes = reinterpret_cast<const uint8_t *>(p.v_cache);
         // window of 32 blocks: lane j describes block base + j
         auto fetch = [&](int base, int &raw, int &seq, int &nv) {
             const int i = base + lane;
@@ -281,18 +286,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
             const int seq = __shfl_sync(0xffffffffu, c_seq, i & 31);
             const int nv = __shfl_sync(0xffffffffu, c_nv, i & 31);
             const int ncopy = bid < 0 ? 0 : nv;
+            const uint32_t sbytes = (kFp8 && ncopy > 0) ? 2u * scale_bytes : 0u;
             if (lane == 0) {
                 meta[st] = make_int4(seq, nv, bid, 0);
-                mbar_arrive_expect_tx(full_s + st * 8, static_cast<uint32_t>(ncopy) * row_bytes * 2);
+                mbar_arrive_expect_tx(full_s + st * 8,
+                                      static_cast<uint32_t>(ncopy) * row_bytes * 2 + sbytes);
             }
             __syncwarp();
             const int r = lane & (kBS - 1);
             if (r < ncopy) {
-                const __half *src = (lane < kBS ? p.k_cache : p.v_cache) +
-                                    (static_cast<int64_t>(bid) * kBS + r) * row_elems;
+                const uint8_t *src = (lane < kBS ? kbytes : vbytes) +
+                                     (static_cast<int64_t>(bid) * kBS + r) * row_bytes64;
                 const uint32_t dst =
                     ring_s + st * stage_bytes + (lane < kBS ? 0 : tile_bytes) + r * pitch;
                 bulk_g2s(dst, src, row_bytes, full_s + st * 8);
+            }
+            if (kFp8 && ncopy > 0 && r == 0) {
+                // the block's scales: 16 tokens x Hk heads, contiguous
+                const float *src = (lane < kBS ? p.k_scale : p.v_scale) +
+                                   static_cast<int64_t>(bid) * kBS * Hk;
+                const uint32_t dst =
+                    ring_s + st * stage_bytes + 2 * tile_bytes + (lane < kBS ? 0 : scale_bytes);
+                bulk_g2s(dst, src, scale_bytes, full_s + st * 8);
             }
             issued = i + 1;
         }
@@ -366,14 +381,35 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
             cur = mt.x;
             st.init(p.q + (static_cast<int64_t>(cur) * H + kvh * G) * D, p.scale_log2, lane);
         }
-        if (mt.z >= 0 && mt.y > 0) {
-            const uint32_t kb = ring_s + s * stage_bytes + kvh * D * 2;
-            const uint32_t vb = kb + tile_bytes;
-            if (Policy::kZeroTailRows && mt.y < kBS) zero_tail_rows<D>(vb, pitch, mt.y, lane);
-            st.block(kb, vb, pitch, mt.y, p.scale_log2, lane, pbuf);
+        if constexpr (kFp8) {
+            if (mt.z >= 0 && mt.y > 0) {
+                const uint32_t kb8 = ring_s + s * stage_bytes + kvh * D;
+                const uint32_t vb8 = kb8 + tile_bytes;
+                if (mt.y < kBS) zero_tail_rows_fp8<D>(vb8, pitch, mt.y, lane);
+                const float *sc = reinterpret_cast<const float *>(
+                    ring + s * stage_bytes + 2 * tile_bytes);
+                const int t0 = (lane & 3) * 2;
+                const int toks[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
+                float ks[4], vs[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ks[i] = sc[toks[i] * Hk + kvh];
+                    vs[i] = sc[kBS * Hk + toks[i] * Hk + kvh];
+                }
+                st.block(kb8, vb8, pitch, mt.y, p.scale_log2, lane, ks, vs);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_s + s * 8);
+        } else {
+            if (mt.z >= 0 && mt.y > 0) {
+                const uint32_t kb = ring_s + s * stage_bytes + kvh * D * 2;
+                const uint32_t vb = kb + tile_bytes;
+                if (Policy::kZeroTailRows && mt.y < kBS) zero_tail_rows<D>(vb, pitch, mt.y, lane);
+                st.block(kb, vb, pitch, mt.y, p.scale_log2, lane, pbuf);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_s + s * 8);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_s + s * 8);
     }
     if (!ok) {
         if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
@@ -385,14 +421,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
 using BalancedFn = void (*)(const BalancedParams);
 
 template <int D, int G>
-BalancedFn pick(bool simt) {
-    if (simt) return decode_balanced_kernel<D, G, SimtPolicy<D, G>>;
-    return decode_balanced_kernel<D, G, MmaPolicy<D, G>>;
+BalancedFn pick(bool simt, bool fp8) {
+    if (fp8) return decode_balanced_kernel<D, G, MmaFp8Policy<D, G>, true>;
+    if (simt) return decode_balanced_kernel<D, G, SimtPolicy<D, G>, false>;
+    return decode_balanced_kernel<D, G, MmaPolicy<D, G>, false>;
 }
 
-BalancedFn select(int D, int G, bool simt) {
+BalancedFn select(int D, int G, bool simt, bool fp8) {
 #define PKV_CASE(d, g) \
-    if (D == d && G == g) return pick<d, g>(simt);
+    if (D == d && G == g) return pick<d, g>(simt, fp8);
     PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
 #undef PKV_CASE
@@ -401,21 +438,24 @@ BalancedFn select(int D, int G, bool simt) {
 
 }  // namespace
 
-BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms) {
+BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms,
+                             bool fp8) {
     BalancedShape r{};
     r.ok = num_kv_heads >= 1 && num_kv_heads <= kMaxBalancedKvHeads && num_seqs >= 1 &&
            (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
     if (!r.ok) return r;
-    const int pitch = num_kv_heads * D * 2 + kRowPad;
-    const int stage_bytes = 2 * kBS * pitch;
-    int stages = kMaxStages;
-    while (stages >= 2 && smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G) > kSmemPerSM)
+    const int pitch = num_kv_heads * D * (fp8 ? 1 : 2) + kRowPad;
+    const int stage_bytes = 2 * kBS * pitch + (fp8 ? 2 * kBS * num_kv_heads * 4 : 0);
+    int stages = fp8 ? kMaxStagesFp8 : kMaxStages;
+    while (stages >= 2 &&
+           smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G) > kSmemPerSM)
         --stages;
     if (stages < 2) {
         r.ok = false;
         return r;
     }
     r.stages = stages;
+    r.pitch = pitch;
     r.smem = smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G);
     const int threads = (num_kv_heads + 1) * 32;
     r.ctas_per_sm = std::max(1, std::min({(228 * 1024) / (r.smem + 1024), 2048 / threads, 32}));
@@ -427,8 +467,8 @@ BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int n
 }
 
 int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
-                    cudaStream_t stream) {
-    BalancedFn fn = select(D, G, simt);
+                    bool fp8, cudaStream_t stream) {
+    BalancedFn fn = select(D, G, simt, fp8);
     if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, shape.smem);

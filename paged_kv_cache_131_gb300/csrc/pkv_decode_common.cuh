@@ -16,6 +16,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include <cmath>
@@ -162,6 +163,175 @@ struct MmaPolicy {
         }
     }
 };
+
+// ---------------------------------------------------------------------------
+// MMA policy over FP8 (E4M3) staged tiles, fed to the fp16 MMA without a
+// shared-memory round trip.  Keys: a non-transposed ldmatrix gives lane l
+// the 4 codes of dims 4*(l%4)..+3 of token l/4 (per 16-dim, 8-token
+// matrix); their fp16 conversion is the B fragment of a k16 step under the
+// contraction-index permutation k = 2t+j -> 4t+j, k = 8+2t+j -> 4t+2+j,
+// which the query fragments follow (one 64-bit load per k-step).  Values: a
+// transposed ldmatrix gives lane l the codes of tokens 2*(l%4)+{0,1} at
+// dims 2*(l/4)+{0,1}; byte permutes split them into an even-dim and an
+// odd-dim B fragment, so O's n-tile 2c+e holds dims 16c + 2n + e.
+// The key scale multiplies the score and the value scale the softmax weight
+// (each factors out of its sum); the weights also carry an exact factor of
+// 256, removed on output, to keep them clear of fp16 subnormals.
+
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0u), "r"(sel));
+    return r;
+}
+
+template <int D, int G>
+struct MmaFp8Policy {
+    static constexpr int KS = D / 16;
+    static constexpr int NT = D / 8;
+    static constexpr float kWeightBoost = 256.f;  // exact; removed on output
+    uint32_t qa[KS][2];
+    float o[NT][2];
+    float m, l;
+
+    __device__ __forceinline__ void init(const __half *qg, float /*scale_log2*/, int lane) {
+        const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            if (g < G) {
+                const uint2 w = __ldg(reinterpret_cast<const uint2 *>(qg + g * D + kk * 16 + tig * 4));
+                qa[kk][0] = w.x;
+                qa[kk][1] = w.y;
+            } else {
+                qa[kk][0] = qa[kk][1] = 0u;
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = 0.f;
+        m = kNegInf;
+        l = 0.f;
+    }
+
+    // kb8 / vb8: this head's key / value codes of the staged block (rows
+    // `pitch` bytes apart); value rows >= nv must hold finite codes.
+    __device__ __forceinline__ void block(uint32_t kb8, uint32_t vb8, uint32_t pitch, int nv,
+                                          float scale_log2, int lane, const float (&ks)[4],
+                                          const float (&vs)[4]) {
+        const int tig = lane & 3;
+        const uint32_t row = (((lane >> 3) & 1) * 8 + (lane & 7)) * pitch + (lane >> 4) * 16;
+        float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+#pragma unroll
+        for (int kp = 0; kp < D / 32; ++kp) {
+            uint32_t r0, r1, r2, r3;  // tokens 0-7 / 8-15, dims 32kp.. / 32kp+16..
+            ldsm_x4(r0, r1, r2, r3, kb8 + row + kp * 32);
+            mma_rows0_7(s0[0], s0[1], qa[2 * kp][0], qa[2 * kp][1], e4m3x2_to_half2(r0),
+                        e4m3x2_to_half2(r0 >> 16));
+            mma_rows0_7(s1[0], s1[1], qa[2 * kp][0], qa[2 * kp][1], e4m3x2_to_half2(r1),
+                        e4m3x2_to_half2(r1 >> 16));
+            mma_rows0_7(s0[0], s0[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1], e4m3x2_to_half2(r2),
+                        e4m3x2_to_half2(r2 >> 16));
+            mma_rows0_7(s1[0], s1[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1], e4m3x2_to_half2(r3),
+                        e4m3x2_to_half2(r3 >> 16));
+        }
+        float x[4] = {s0[0], s0[1], s1[0], s1[1]};
+        const int t0 = tig * 2;
+        const int tok[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
+        float mx = kNegInf;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[i] = tok[i] < nv ? (x[i] * ks[i]) * scale_log2 : kNegInf;
+            mx = fmaxf(mx, x[i]);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mnew = fmaxf(m, mx);
+        const float alpha = exp2f(m - mnew);
+        float pw[4], psum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float pi = exp2f(x[i] - mnew);
+            psum += pi;
+            pw[i] = tok[i] < nv ? pi * (vs[i] * kWeightBoost) : 0.f;
+        }
+        const uint32_t pa0 = pack_half2(pw[0], pw[1]);
+        const uint32_t pa2 = pack_half2(pw[2], pw[3]);
+        l = l * alpha + psum;
+        m = mnew;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            o[nt][0] *= alpha;
+            o[nt][1] *= alpha;
+        }
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t r0, r1, r2, r3;  // tokens 0-7 / 8-15, dims 32q.. / 32q+16..
+            ldsm_x4_trans(r0, r1, r2, r3, vb8 + row + q * 32);
+            // even dims: bytes 0 and 2; odd dims: bytes 1 and 3
+            mma_rows0_7(o[4 * q][0], o[4 * q][1], pa0, pa2,
+                        e4m3x2_to_half2(byte_perm(r0, 0x20)), e4m3x2_to_half2(byte_perm(r1, 0x20)));
+            mma_rows0_7(o[4 * q + 1][0], o[4 * q + 1][1], pa0, pa2,
+                        e4m3x2_to_half2(byte_perm(r0, 0x31)), e4m3x2_to_half2(byte_perm(r1, 0x31)));
+            mma_rows0_7(o[4 * q + 2][0], o[4 * q + 2][1], pa0, pa2,
+                        e4m3x2_to_half2(byte_perm(r2, 0x20)), e4m3x2_to_half2(byte_perm(r3, 0x20)));
+            mma_rows0_7(o[4 * q + 3][0], o[4 * q + 3][1], pa0, pa2,
+                        e4m3x2_to_half2(byte_perm(r2, 0x31)), e4m3x2_to_half2(byte_perm(r3, 0x31)));
+        }
+    }
+
+    __device__ __forceinline__ float l_total() const {
+        float ls = l;
+        ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+        return ls;
+    }
+
+    // n-tile pair (2c, 2c+1), element j: dims 16c + 4t + 2j and the next one
+    __device__ __forceinline__ void write_output(__half *out_g0, int lane) {
+        const int g = lane >> 2, tig = lane & 3;
+        const float ls = l_total();
+        if (g < G) {
+            const float inv = ls > 0.f ? (1.f / kWeightBoost) / ls : 0.f;
+#pragma unroll
+            for (int c = 0; c < NT / 2; ++c)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    *reinterpret_cast<__half2 *>(out_g0 + g * D + 16 * c + 4 * tig + 2 * j) =
+                        __floats2half2_rn(o[2 * c][j] * inv, o[2 * c + 1][j] * inv);
+        }
+    }
+
+    __device__ __forceinline__ void write_partial(float2 *ml, float *og, int lane) {
+        const int g = lane >> 2, tig = lane & 3;
+        const float ls = l_total();
+        if (g < G) {
+            if (tig == 0) ml[g] = make_float2(m, ls);
+            const float u = 1.f / kWeightBoost;
+#pragma unroll
+            for (int c = 0; c < NT / 2; ++c)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    *reinterpret_cast<float2 *>(og + g * D + 16 * c + 4 * tig + 2 * j) =
+                        make_float2(o[2 * c][j] * u, o[2 * c + 1][j] * u);
+        }
+    }
+};
+
+// Zero the value codes of rows [nv, 16) of one head (D bytes per row), then
+// order those generic-proxy writes before later bulk copies into the stage.
+template <int D>
+__device__ __forceinline__ void zero_tail_rows_fp8(uint32_t vb8, uint32_t pitch, int nv, int lane) {
+    for (int e = lane; e < (kBS - nv) * (D / 16); e += 32) {
+        const uint32_t a = vb8 + (nv + e / (D / 16)) * pitch + (e % (D / 16)) * 16;
+        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+}
 
 // ---------------------------------------------------------------------------
 // SIMT policy (fp32 FMAs on CUDA cores): lane l owns dims [l*DPL, (l+1)*DPL)

@@ -60,7 +60,9 @@ struct BalancedParams {
     int num_kv_heads;
     int max_blocks_per_seq;
     int num_stages;  // staging ring depth (blocks in flight per CTA)
-    int pitch;       // staged row pitch in bytes: Hk*D*2 + 16
+    int pitch;       // staged row pitch in bytes: Hk*D*elem + 16
+    const float *k_scale;  // FP8 caches: [NB, 16, Hk] per-row scales (else null)
+    const float *v_scale;
     int64_t num_blocks;
     int *counters;    // [S * Hk] tickets, zero between calls
     float2 *part_ml;  // [2 * grid][Hk][G]
@@ -71,15 +73,17 @@ struct BalancedParams {
 struct BalancedShape {
     bool ok;          // the schedule supports this shape
     int stages;       // ring depth
+    int pitch;        // staged row pitch
     int smem;         // dynamic shared memory per CTA
     int ctas_per_sm;  // resident CTAs per SM
     int grid;         // CTAs launched
     int64_t workspace;  // bytes of scratch it needs
 };
 
-BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms);
+BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms,
+                             bool fp8 = false);
 int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
-                    cudaStream_t stream);
+                    bool fp8, cudaStream_t stream);
 
 inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 

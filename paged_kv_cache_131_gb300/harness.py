@@ -10,9 +10,10 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (PKV_COMPUTE_AUTO, PKV_SCHEDULE_AUTO, pkv_cache_write, pkv_cache_write_multi,
-               pkv_decode_attention, pkv_decode_workspace_bytes, pkv_view)
-from .workloads import DecodeWorkload, WriteWorkload
+from . import (PKV_COMPUTE_AUTO, PKV_SCHEDULE_AUTO, pkv_cache_write, pkv_cache_write_fp8,
+               pkv_cache_write_multi, pkv_decode_attention, pkv_decode_attention_fp8,
+               pkv_decode_workspace_bytes, pkv_view)
+from .workloads import DecodeWorkload, WriteWorkload, slot_of
 
 
 def to_dev(a: np.ndarray, device) -> torch.Tensor:
@@ -103,6 +104,80 @@ class DeviceDecode:
             return 0
         t = self.wl.slot_mapping.size
         return 2 * 2 * t * self.row_bytes + 8 * t
+
+
+def prior_token_rows(wl: DecodeWorkload):
+    """Slots and fp16 K/V rows [n, Hk, D] of every token already in the cache
+    before the new tokens (the rows the fp16 workload stored there)."""
+    bs = wl.block_size
+    seen, slots = set(), []
+    new = set(wl.slot_mapping.tolist()) if wl.slot_mapping is not None else set()
+    for i, L in enumerate(wl.seq_lens):
+        for pos in range(int(L)):
+            s = slot_of(wl.block_tables[i], pos, bs)
+            if s not in seen and s not in new:
+                seen.add(s)
+                slots.append(s)
+    slots = np.asarray(slots, dtype=np.int64)
+    rows_k = wl.k_cache.reshape(-1, wl.num_kv_heads, wl.head_dim)[slots]
+    rows_v = wl.v_cache.reshape(-1, wl.num_kv_heads, wl.head_dim)[slots]
+    return slots, rows_k, rows_v
+
+
+class DeviceDecodeFp8:
+    """A decode workload held in FP8 (E4M3) caches: the tokens already in the
+    fp16 workload's cache are quantized into place by the library's FP8 write
+    (unwritten slots keep NaN codes and NaN scales), then each step writes the
+    new tokens (FP8) and decodes."""
+
+    def __init__(self, wl: DecodeWorkload, device="cuda"):
+        self.wl = wl
+        NB, bs, Hk, D = wl.k_cache.shape
+        self.k_cache = torch.full((NB, bs, Hk, D), 0x7F, dtype=torch.uint8, device=device)
+        self.v_cache = torch.full((NB, bs, Hk, D), 0x7F, dtype=torch.uint8, device=device)
+        self.k_scale = torch.full((NB, bs, Hk), float("nan"), dtype=torch.float32, device=device)
+        self.v_scale = torch.full((NB, bs, Hk), float("nan"), dtype=torch.float32, device=device)
+        self.prior_slots, rk, rv = prior_token_rows(wl)
+        if self.prior_slots.size:
+            pkv_cache_write_fp8(to_dev(rk, device), to_dev(rv, device),
+                                to_dev(self.prior_slots, device), self.k_cache, self.v_cache,
+                                self.k_scale, self.v_scale, bs, NB)
+        self.q = to_dev(wl.q, device)
+        self.block_tables = to_dev(wl.block_tables, device)
+        self.seq_lens = to_dev(wl.seq_lens, device)
+        self.out = torch.empty_like(self.q)
+        self.has_write = wl.slot_mapping is not None and wl.slot_mapping.size > 0
+        if self.has_write:
+            self.k_new = to_dev(wl.k_new.reshape(-1, Hk, D), device)
+            self.v_new = to_dev(wl.v_new.reshape(-1, Hk, D), device)
+            self.slot_mapping = to_dev(wl.slot_mapping, device)
+        with torch.cuda.device(torch.device(device)):
+            nbytes = pkv_decode_workspace_bytes(wl.num_seqs, wl.num_heads, wl.num_kv_heads,
+                                                wl.head_dim, max(wl.max_seq_len, 1))
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+    def write(self, stream=None) -> None:
+        if self.has_write:
+            pkv_cache_write_fp8(self.k_new, self.v_new, self.slot_mapping, self.k_cache,
+                                self.v_cache, self.k_scale, self.v_scale, self.wl.block_size,
+                                self.wl.num_blocks, stream=stream)
+
+    def decode(self, stream=None) -> torch.Tensor:
+        wl = self.wl
+        pkv_decode_attention_fp8(self.out, self.q, self.k_cache, self.v_cache, self.k_scale,
+                                 self.v_scale, self.block_tables, self.seq_lens, wl.scale,
+                                 wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                                 wl.max_seq_len, wl.num_blocks, self.workspace, stream=stream)
+        return self.out
+
+    def step(self, stream=None) -> torch.Tensor:
+        self.write(stream)
+        return self.decode(stream)
+
+    def kv_bytes(self) -> int:
+        """Bytes the FP8 decode reads: codes (1 B) + one fp32 scale per row, K and V."""
+        wl = self.wl
+        return int(wl.seq_lens.astype(np.int64).sum()) * wl.num_kv_heads * (wl.head_dim + 4) * 2
 
 
 class DeviceWrite:

@@ -59,7 +59,9 @@ MUTATIONS = {
     "E4M3 subnormal scale wrong":
         ("mag = ldexp((double)mant, -9);", "mag = ldexp((double)mant, -8);"),
     "E4M3 ties to odd":
-        ("(c & 1) == 0 && (best & 1) == 1", "(c & 1) == 1 && (best & 1) == 0"),
+        ("(above == below && ((lo + 1) & 1) == 0)", "(above == below && ((lo + 1) & 1) == 1)"),
+    "E4M3 rounds down always":
+        ("if (above < below ||", "if (0 &&"),
     "FP8 scale for a 240 maximum":
         ("float s = amax / 448.0f;", "float s = amax / 240.0f;"),
     "FP8 quantizer multiplies by the scale":
