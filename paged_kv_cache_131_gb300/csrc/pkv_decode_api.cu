@@ -46,11 +46,13 @@ size_t pkv_decode_workspace_bytes_ex(int32_t num_seqs, int32_t num_heads, int32_
     const int64_t grid_ws =
         grid_workspace_bytes(num_seqs, num_heads, head_dim, num_partitions(max_seq_len, pt));
     const int G = num_heads / num_kv_heads;
-    const BalancedShape b = balanced_shape(num_seqs, num_kv_heads, G, head_dim, pkv::sm_count());
-    const BalancedShape b8 =
-        balanced_shape(num_seqs, num_kv_heads, G, head_dim, pkv::sm_count(), true);
-    return static_cast<size_t>(std::max<int64_t>(
-        {grid_ws, b.ok ? b.workspace : 0, b8.ok ? b8.workspace : 0}));
+    int64_t need = grid_ws;
+    for (const bool fp8 : {false, true}) {
+        const BalancedShape b =
+            balanced_shape(num_seqs, num_kv_heads, G, head_dim, pkv::sm_count(), fp8);
+        if (b.ok) need = std::max(need, b.workspace);
+    }
+    return static_cast<size_t>(need);
 }
 
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
@@ -108,7 +110,7 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
         BalancedShape shape{};
         bool usable = balanced_fits_index(num_seqs, max_blocks_per_seq);
         if (usable) {
-            shape = balanced_shape(num_seqs, num_kv_heads, G, head_dim, sm_count());
+            shape = balanced_shape(num_seqs, num_kv_heads, G, head_dim, sm_count(), false);
             usable = shape.ok && workspace != nullptr &&
                      static_cast<int64_t>(workspace_bytes) >= shape.workspace;
         }
@@ -132,7 +134,7 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
             p.num_kv_heads = num_kv_heads;
             p.max_blocks_per_seq = max_blocks_per_seq;
             p.num_stages = shape.stages;
-            p.pitch = shape.pitch;
+            p.row_bytes = shape.row_bytes;
             p.num_blocks = num_blocks;
             uint8_t *ws = static_cast<uint8_t *>(workspace);
             const int64_t c_bytes = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
@@ -140,6 +142,11 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
             p.counters = reinterpret_cast<int *>(ws);
             p.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
             p.part_o = reinterpret_cast<float *>(ws + c_bytes + align256(slots * 8));
+            const int box = shape.row_bytes / chunk_bytes_for_row(shape.row_bytes);
+            int st = make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, shape.row_bytes, box);
+            if (st == PKV_OK)
+                st = make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, shape.row_bytes, box);
+            if (st != PKV_OK) return st;
             p.err = device_error_record();
             if (p.err == nullptr) return PKV_ERR_CUDA;
             return launch_balanced(p, shape, head_dim, G, simt, false, s);
@@ -175,8 +182,16 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
         p.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
         p.part_o = reinterpret_cast<float *>(ws + c_bytes + ml_bytes);
         // the combine's per-partition weights must fit in the (reused) ring
-        const int ring = kGridWarps * kGridStages * 2 * kBlockSize * (head_dim * 2 + 16);
-        if (static_cast<int64_t>(2 * G * P + 2 * G) * 4 > ring) return PKV_ERR_UNSUPPORTED;
+        if (static_cast<int64_t>(2 * G * P + 2 * G) * 4 > grid_ring_bytes(head_dim))
+            return PKV_ERR_UNSUPPORTED;
+    }
+    {
+        // per-head boxes: kv_head's head_dim*2 bytes are whole 128-byte chunks
+        const int row_bytes = num_kv_heads * head_dim * 2;
+        const int box = head_dim * 2 / chunk_bytes_for_row(row_bytes);
+        int st = make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, row_bytes, box);
+        if (st == PKV_OK) st = make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, row_bytes, box);
+        if (st != PKV_OK) return st;
     }
     p.err = device_error_record();
     if (p.err == nullptr) return PKV_ERR_CUDA;
@@ -245,7 +260,7 @@ extern "C" int pkv_decode_attention_fp8(void *out, const void *q, const void *k_
     p.num_kv_heads = num_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.num_stages = shape.stages;
-    p.pitch = shape.pitch;
+    p.row_bytes = shape.row_bytes;
     p.num_blocks = num_blocks;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const int64_t c_bytes = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
@@ -253,6 +268,10 @@ extern "C" int pkv_decode_attention_fp8(void *out, const void *q, const void *k_
     p.counters = reinterpret_cast<int *>(ws);
     p.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
     p.part_o = reinterpret_cast<float *>(ws + c_bytes + align256(slots * 8));
+    const int box = shape.row_bytes / chunk_bytes_for_row(shape.row_bytes);
+    int st = make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, shape.row_bytes, box);
+    if (st == PKV_OK) st = make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, shape.row_bytes, box);
+    if (st != PKV_OK) return st;
     p.err = device_error_record();
     if (p.err == nullptr) return PKV_ERR_CUDA;
     return launch_balanced(p, shape, head_dim, G, false, true,

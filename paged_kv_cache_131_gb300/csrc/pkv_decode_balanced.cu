@@ -10,10 +10,14 @@
 //  - The producer walks its range.  For each block it takes the next stage
 //    of a `num_stages`-deep ring (waiting on the stage's "empty" mbarrier),
 //    publishes the block's (sequence, valid tokens, block id), and issues
-//    16 + 16 bulk (TMA) copies: key row r and value row r of the block, each
-//    row = all KV heads of one token (num_kv_heads*head_dim*2 contiguous
-//    bytes), completing on the stage's "full" mbarrier.  Block-table entries
-//    are loaded a 32-block window ahead.
+//    one tiled tensor copy (TMA) for the block's 16 key rows and one for its
+//    16 value rows (a row = all KV heads of one token, num_kv_heads*
+//    head_dim*elem contiguous bytes; FP8 adds two bulk copies of the rows'
+//    scales), completing on the stage's "full" mbarrier.  One copy per tile
+//    keeps the producer's issue cost per block small: issuing a copy takes
+//    the warp about as long whatever its size, and per-row copies made the
+//    producer the bottleneck.  Block-table entries are loaded a 32-block
+//    window ahead.
 //  - Consumer warp h waits on "full", folds head h's 16 keys/values into its
 //    online-softmax state (compute policy of pkv_decode_common.cuh) and
 //    arrives on "empty".  When the sequence changes it finishes the previous
@@ -40,9 +44,10 @@ namespace {
 constexpr int kMaxStages = 4;
 constexpr int kMaxStagesFp8 = 6;  // FP8 stages are half the size: keep as many bytes in flight
 constexpr int kMaxThreads = (kMaxBalancedKvHeads + 1) * 32;
-
 // Dynamic shared memory:
-//   ring   stages * 2 * 16 rows * pitch   (key tile, then value tile)
+//   ring   stages * (key tile, value tile[, key scales, value scales]),
+//          each stage 1024-byte aligned; a tile is 16 rows, chunk-major and
+//          swizzled (SwizzledTile)
 //   full   stages mbarriers (1 arrival + transaction bytes)
 //   empty  stages mbarriers (one arrival per consumer warp)
 //   meta   stages int4 {sequence, valid tokens, block id (-1 = skip), 0}
@@ -50,9 +55,16 @@ constexpr int kMaxThreads = (kMaxBalancedKvHeads + 1) * 32;
 //   lens   S int32: sequence lengths (clamped to the block table)
 //   misc   4 int32
 //   pbuf   Hk * 16 * G fp32 (SIMT policy: one block's softmax weights)
+// (plus kTileAlign bytes to align the dynamic shared memory base)
 int smem_bytes(int stages, int stage_bytes, int S, int Hk, int G) {
-    return stages * stage_bytes + stages * 16 + stages * 16 + (2 * S + 1) * 4 + 16 +
+    return kTileAlign + stages * stage_bytes + stages * 16 + stages * 16 + (2 * S + 1) * 4 + 16 +
            Hk * kBS * G * 4;
+}
+
+// Bytes of one stage: key and value tiles (+ FP8 scales), 1024-aligned.
+__host__ __device__ int stage_bytes_for(int row_bytes, int Hk, bool fp8) {
+    const int raw = 2 * kBS * row_bytes + (fp8 ? 2 * kBS * Hk * 4 : 0);
+    return (raw + kTileAlign - 1) / kTileAlign * kTileAlign;
 }
 
 // Largest s in [0, S) with cum[s] <= f (cum non-decreasing, cum[0] = 0).
@@ -123,14 +135,17 @@ __device__ void combine_partials(const BalancedParams &p, int seq, int kvh, int 
 }
 
 template <int D, int G, class Policy, bool kFp8>
-__global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const BalancedParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    decode_balanced_kernel(const __grid_constant__ BalancedParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((kTileAlign - (smem_u32(smem_raw) & (kTileAlign - 1))) &
+                                (kTileAlign - 1));
     const int Hk = p.num_kv_heads, S = p.num_seqs, NS = p.num_stages, H = p.num_heads;
-    const int pitch = p.pitch;
-    const int tile_bytes = kBS * pitch;
+    const SwizzledTile tile{chunk_bytes_for_row(p.row_bytes) == 128 ? 7u : 6u};
+    const int tile_bytes = kBS * p.row_bytes;
     // FP8: a stage also holds the block's key and value scales ([16][Hk] fp32 each)
     const int scale_bytes = kFp8 ? kBS * Hk * 4 : 0;
-    const int stage_bytes = 2 * tile_bytes + 2 * scale_bytes;
+    const int stage_bytes = stage_bytes_for(p.row_bytes, Hk, kFp8);
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
     uint64_t *empty = full + NS;
@@ -229,8 +244,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
 
     if (warp == Hk) {
         // ================================ producer ================================
-        const int64_t row_bytes64 = static_cast<int64_t>(Hk) * D * (kFp8 ? 1 : 2);
-        const uint32_t row_bytes = static_cast<uint32_t>(row_bytes64);
         const uint8_t *kbytes = reinterpret_cast<const uint8_t *>(p.k_cache);
         const uint8_t *vbytes = reinterpret_cast<const uint8_t *>(p.v_cache);
         // window of 32 blocks: lane j describes block base + j
@@ -285,29 +298,26 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
             const int bid = __shfl_sync(0xffffffffu, c_bid, i & 31);
             const int seq = __shfl_sync(0xffffffffu, c_seq, i & 31);
             const int nv = __shfl_sync(0xffffffffu, c_nv, i & 31);
-            const int ncopy = bid < 0 ? 0 : nv;
-            const uint32_t sbytes = (kFp8 && ncopy > 0) ? 2u * scale_bytes : 0u;
+            // the whole 16-row tiles (rows past the last valid token still
+            // belong to the physical block)
+            const bool copy = bid >= 0 && nv > 0;
+            const uint32_t stage = ring_s + st * stage_bytes;
             if (lane == 0) {
                 meta[st] = make_int4(seq, nv, bid, 0);
                 mbar_arrive_expect_tx(full_s + st * 8,
-                                      static_cast<uint32_t>(ncopy) * row_bytes * 2 + sbytes);
+                                      copy ? 2u * tile_bytes + (kFp8 ? 2u * scale_bytes : 0u)
+                                           : 0u);
             }
             __syncwarp();
-            const int r = lane & (kBS - 1);
-            if (r < ncopy) {
-                const uint8_t *src = (lane < kBS ? kbytes : vbytes) +
-                                     (static_cast<int64_t>(bid) * kBS + r) * row_bytes64;
-                const uint32_t dst =
-                    ring_s + st * stage_bytes + (lane < kBS ? 0 : tile_bytes) + r * pitch;
-                bulk_g2s(dst, src, row_bytes, full_s + st * 8);
-            }
-            if (kFp8 && ncopy > 0 && r == 0) {
+            if (copy && lane < 2)
+                tensor_g2s_3d(stage + lane * tile_bytes, lane == 0 ? &p.tm_k : &p.tm_v, 0,
+                              bid * kBS, 0, full_s + st * 8);
+            if (kFp8 && copy && (lane == 2 || lane == 3)) {
                 // the block's scales: 16 tokens x Hk heads, contiguous
-                const float *src = (lane < kBS ? p.k_scale : p.v_scale) +
+                const float *src = (lane == 2 ? p.k_scale : p.v_scale) +
                                    static_cast<int64_t>(bid) * kBS * Hk;
-                const uint32_t dst =
-                    ring_s + st * stage_bytes + 2 * tile_bytes + (lane < kBS ? 0 : scale_bytes);
-                bulk_g2s(dst, src, scale_bytes, full_s + st * 8);
+                bulk_g2s(stage + 2 * tile_bytes + (lane - 2) * scale_bytes, src, scale_bytes,
+                         full_s + st * 8);
             }
             issued = i + 1;
         }
@@ -356,6 +366,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
         int last = 0;
         if (lane == 0) {
             int *ticket = p.counters + static_cast<int64_t>(seq) * Hk + kvh;
+            __threadfence();
             const int prev = atomicAdd(ticket, 1);
             last = prev == c_b - c_a;
             if (last) {
@@ -367,8 +378,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
         if (last) combine_partials<D, G>(p, seq, kvh, c_a, c_b, f_s, T, N, lane);
     };
 
+    // FP8 scales of this lane's tokens in a staged block
+    auto load_scales = [&](int s, float (&ks)[4], float (&vs)[4]) {
+        const float *sc = reinterpret_cast<const float *>(ring + s * stage_bytes + 2 * tile_bytes);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int tok = MmaFp8Policy<D, G>::token_of(lane, t);
+            ks[t] = sc[tok * Hk + kvh];
+            vs[t] = sc[kBS * Hk + tok * Hk + kvh];
+        }
+    };
+
     bool ok = true;
-    for (int i = 0; i < n; ++i) {
+    for (int i = 0; i < n;) {
         const int s = i % NS;
         const bool landed = mbar_wait_bounded(full_s + s * 8, (i / NS) & 1);
         if (!__all_sync(0xffffffffu, landed)) {
@@ -381,35 +403,61 @@ __global__ void __launch_bounds__(kMaxThreads, 1) decode_balanced_kernel(const B
             cur = mt.x;
             st.init(p.q + (static_cast<int64_t>(cur) * H + kvh * G) * D, p.scale_log2, lane);
         }
+        int used = 1;
+        int s2 = 0;
         if constexpr (kFp8) {
-            if (mt.z >= 0 && mt.y > 0) {
-                const uint32_t kb8 = ring_s + s * stage_bytes + kvh * D;
-                const uint32_t vb8 = kb8 + tile_bytes;
-                if (mt.y < kBS) zero_tail_rows_fp8<D>(vb8, pitch, mt.y, lane);
-                const float *sc = reinterpret_cast<const float *>(
-                    ring + s * stage_bytes + 2 * tile_bytes);
-                const int t0 = (lane & 3) * 2;
-                const int toks[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
-                float ks[4], vs[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    ks[i] = sc[toks[i] * Hk + kvh];
-                    vs[i] = sc[kBS * Hk + toks[i] * Hk + kvh];
+            // A full block takes its successor along when that one is of the
+            // same sequence: one softmax step over 32 tokens.  (Waiting for
+            // the successor while holding this stage cannot stall the
+            // producer: the successor's stage was released before.)
+            int4 mt2 = make_int4(-1, 0, -1, 0);
+            if (mt.z >= 0 && mt.y == kBS && i + 1 < n) {
+                s2 = (i + 1) % NS;
+                const bool landed2 = mbar_wait_bounded(full_s + s2 * 8, ((i + 1) / NS) & 1);
+                if (!__all_sync(0xffffffffu, landed2)) {
+                    ok = false;
+                    break;
                 }
-                st.block(kb8, vb8, pitch, mt.y, p.scale_log2, lane, ks, vs);
+                mt2 = meta[s2];
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_s + s * 8);
+            const uint32_t kb8 = ring_s + s * stage_bytes;
+            const uint32_t head = kvh * D;
+            if (mt2.x == mt.x && mt2.z >= 0 && mt2.y > 0) {
+                const uint32_t kb8b = ring_s + s2 * stage_bytes;
+                if (mt2.y < kBS) zero_tail_bytes<D>(kb8b + tile_bytes, tile, head, mt2.y, lane);
+                float ks[2][4], vs[2][4];
+                load_scales(s, ks[0], vs[0]);
+                load_scales(s2, ks[1], vs[1]);
+                const uint32_t kbs[2] = {kb8, kb8b};
+                const uint32_t vbs[2] = {kb8 + tile_bytes, kb8b + tile_bytes};
+                const int nvs[2] = {mt.y, mt2.y};
+                st.template step<2>(kbs, vbs, tile, head, nvs, p.scale_log2, lane, ks, vs);
+                used = 2;
+            } else if (mt.z >= 0 && mt.y > 0) {
+                if (mt.y < kBS) zero_tail_bytes<D>(kb8 + tile_bytes, tile, head, mt.y, lane);
+                float ks[1][4], vs[1][4];
+                load_scales(s, ks[0], vs[0]);
+                const uint32_t kbs[1] = {kb8};
+                const uint32_t vbs[1] = {kb8 + tile_bytes};
+                const int nvs[1] = {mt.y};
+                st.template step<1>(kbs, vbs, tile, head, nvs, p.scale_log2, lane, ks, vs);
+            }
         } else {
             if (mt.z >= 0 && mt.y > 0) {
-                const uint32_t kb = ring_s + s * stage_bytes + kvh * D * 2;
+                const uint32_t kb = ring_s + s * stage_bytes;
                 const uint32_t vb = kb + tile_bytes;
-                if (Policy::kZeroTailRows && mt.y < kBS) zero_tail_rows<D>(vb, pitch, mt.y, lane);
-                st.block(kb, vb, pitch, mt.y, p.scale_log2, lane, pbuf);
+                const uint32_t head = kvh * D * 2;
+                if (Policy::kZeroTailRows && mt.y < kBS)
+                    zero_tail_rows<D>(vb, tile, head, mt.y, lane);
+                st.block(kb, vb, tile, head, mt.y, p.scale_log2, lane, pbuf);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_s + s * 8);
         }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(empty_s + s * 8);
+            if (used == 2) mbar_arrive(empty_s + s2 * 8);
+        }
+        i += used;
     }
     if (!ok) {
         if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
@@ -444,8 +492,8 @@ BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int n
     r.ok = num_kv_heads >= 1 && num_kv_heads <= kMaxBalancedKvHeads && num_seqs >= 1 &&
            (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
     if (!r.ok) return r;
-    const int pitch = num_kv_heads * D * (fp8 ? 1 : 2) + kRowPad;
-    const int stage_bytes = 2 * kBS * pitch + (fp8 ? 2 * kBS * num_kv_heads * 4 : 0);
+    const int row_bytes = num_kv_heads * D * (fp8 ? 1 : 2);
+    const int stage_bytes = stage_bytes_for(row_bytes, num_kv_heads, fp8);
     int stages = fp8 ? kMaxStagesFp8 : kMaxStages;
     while (stages >= 2 &&
            smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G) > kSmemPerSM)
@@ -455,7 +503,7 @@ BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int n
         return r;
     }
     r.stages = stages;
-    r.pitch = pitch;
+    r.row_bytes = row_bytes;
     r.smem = smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G);
     const int threads = (num_kv_heads + 1) * 32;
     r.ctas_per_sm = std::max(1, std::min({(228 * 1024) / (r.smem + 1024), 2048 / threads, 32}));

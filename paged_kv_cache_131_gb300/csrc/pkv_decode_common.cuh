@@ -10,31 +10,52 @@
 // into the state:
 //     m' = max(m, max_t s_t),  alpha = 2^(m - m'),  p_t = 2^(s_t - m'),
 //     l' = alpha*l + sum_t p_t,  o' = alpha*o + sum_t p_t v_t.
-// Staged rows sit `pitch` bytes apart in shared memory; the pitch is 16
-// bytes more than a multiple of 128 so that 8 consecutive rows start in 8
-// different 16-byte bank groups (conflict-free ldmatrix / vector loads).
+// A staged tile is the 16 token rows of one block, brought by one tiled
+// tensor copy (TMA) and laid out chunk-major with the copy's swizzle
+// (SwizzledTile): 8 tokens reading the same 16 bytes of their rows hit 8
+// different 16-byte bank groups, so every ldmatrix is conflict-free.
 #pragma once
 
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include <cmath>
 
+#include "pkv_decode_host.h"
 #include "pkv_device.cuh"
 
 namespace pkv {
 namespace dec {
 
-constexpr int kBS = 16;      // tokens per physical block on the decode path
-constexpr int kRowPad = 16;  // staged row pitch = row bytes + 16
+constexpr int kBS = 16;  // tokens per physical block on the decode path
 constexpr float kNegInf = -INFINITY;
+
+// Where byte b of token t's row sits in a staged tile.  The tensor copy
+// stores the tile chunk-major -- chunk c (bytes [c*C, (c+1)*C) of every row)
+// is 16 rows of C bytes -- and swizzles the 16-byte units of each row: unit
+// u of token t lands at u ^ (t & 7) for C = 128 (the 128-byte swizzle) or
+// u ^ ((t >> 1) & 3) for C = 64 (the 64-byte swizzle).  The tile base is
+// 1024-byte aligned.  b keeps its low 4 bits.
+struct SwizzledTile {
+    uint32_t log_c;  // log2 of the chunk bytes: 7 or 6
+    __device__ __forceinline__ uint32_t at(int t, uint32_t b) const {
+        const uint32_t c = b >> log_c;
+        const uint32_t u = (b >> 4) & ((1u << (log_c - 4)) - 1u);
+        const uint32_t x = log_c == 7 ? (t & 7) : ((t >> 1) & 3);
+        return (c << (log_c + 4)) + (static_cast<uint32_t>(t) << log_c) + ((u ^ x) << 4) +
+               (b & 15u);
+    }
+};
 
 // ---------------------------------------------------------------------------
 // MMA policy: the G (<= 8) query heads are rows 0..G-1 of the 16-row A
 // operand of m16n8k16 fp16 MMAs with fp32 accumulation; rows 8..15 are zero
 // and never carried.  Lane l owns head row g = l/4 and columns 2*(l%4)+{0,1}
 // of every 8-wide n-tile (tokens for S = Q K^T, head dims for O += P V).
+// Token n-tile 0 holds tokens 0-7 and n-tile 1 tokens 8-15: lane l's scores
+// are those of tokens 2*(l%4) + {0, 1} and + {8, 9}, which is exactly lane
+// l's A fragment of O += P V (k-slot = token), so scores never move between
+// lanes.
 
 template <int D, int G>
 struct MmaPolicy {
@@ -63,19 +84,23 @@ struct MmaPolicy {
         l = 0.f;
     }
 
-    // One staged block: keys at kb, values at vb (rows `pitch` bytes apart),
-    // nv valid tokens (1..16).  Key rows >= nv may hold anything (their
-    // scores become -inf); value rows >= nv must hold finite numbers.
-    __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, uint32_t pitch, int nv,
-                                          float scale_log2, int lane, float * /*pbuf*/) {
+    // One staged block: key tile at kb, value tile at vb, this head's bytes
+    // starting at `head` within each row; nv valid tokens (1..16).  Key rows
+    // >= nv may hold anything (their scores become -inf); value rows >= nv
+    // must hold finite numbers.
+    __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, SwizzledTile tile,
+                                          uint32_t head, int nv, float scale_log2, int lane,
+                                          float * /*pbuf*/) {
         const int tig = lane & 3;
         float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
-        // S = Q K^T: B fragments straight from the row-major key tile
-        const uint32_t krow = kb + ((lane >> 4) * 8 + (lane & 7)) * pitch + ((lane >> 3) & 1) * 16;
+        // S = Q K^T: B fragments straight from the key tile; matrices 0/1:
+        // tokens 0-7, dims 0-7 / 8-15 of the k-step; 2/3: tokens 8-15
+        const int kt = (lane >> 4) * 8 + (lane & 7);
+        const uint32_t kcol = head + ((lane >> 3) & 1) * 16;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(b0, b1, b2, b3, krow + kk * 32);
+            ldsm_x4(b0, b1, b2, b3, kb + tile.at(kt, kcol + kk * 32));
             mma_rows0_7(s0[0], s0[1], qa[kk][0], qa[kk][1], b0, b1);
             mma_rows0_7(s1[0], s1[1], qa[kk][0], qa[kk][1], b2, b3);
         }
@@ -103,12 +128,14 @@ struct MmaPolicy {
             o[nt][0] *= alpha;
             o[nt][1] *= alpha;
         }
-        // O += P V: B fragments from the row-major value tile, transposed
-        const uint32_t vrow = vb + (((lane >> 3) & 1) * 8 + (lane & 7)) * pitch + (lane >> 4) * 16;
+        // O += P V: B fragments from the value tile, transposed; matrices
+        // 0/1: tokens 0-7 / 8-15, dims 0-7; 2/3: the same for dims 8-15
+        const int vt = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const uint32_t vcol = head + (lane >> 4) * 16;
 #pragma unroll
         for (int nd = 0; nd < D / 16; ++nd) {
             uint32_t v0, v1, v2, v3;
-            ldsm_x4_trans(v0, v1, v2, v3, vrow + nd * 32);
+            ldsm_x4_trans(v0, v1, v2, v3, vb + tile.at(vt, vcol + nd * 32));
             mma_rows0_7(o[2 * nd][0], o[2 * nd][1], pa0, pa2, v0, v1);
             mma_rows0_7(o[2 * nd + 1][0], o[2 * nd + 1][1], pa0, pa2, v2, v3);
         }
@@ -166,120 +193,180 @@ struct MmaPolicy {
 
 // ---------------------------------------------------------------------------
 // MMA policy over FP8 (E4M3) staged tiles, fed to the fp16 MMA without a
-// shared-memory round trip.  Keys: a non-transposed ldmatrix gives lane l
-// the 4 codes of dims 4*(l%4)..+3 of token l/4 (per 16-dim, 8-token
-// matrix); their fp16 conversion is the B fragment of a k16 step under the
-// contraction-index permutation k = 2t+j -> 4t+j, k = 8+2t+j -> 4t+2+j,
-// which the query fragments follow (one 64-bit load per k-step).  Values: a
-// transposed ldmatrix gives lane l the codes of tokens 2*(l%4)+{0,1} at
-// dims 2*(l/4)+{0,1}; byte permutes split them into an even-dim and an
-// odd-dim B fragment, so O's n-tile 2c+e holds dims 16c + 2n + e.
+// shared-memory round trip.  Tokens are tiled 0-7 / 8-15 as in MmaPolicy.
+//
+// Codes become fp16 by integer bit moves, not by a conversion instruction:
+// an E4M3 code s.eeee.mmm with its sign moved to bit 15 and its 7 other bits
+// placed at bits 7..13 is the fp16 s.0eeee.mmm0000000, whose value is the
+// code's value times 2^-8 exactly -- for normal codes (exponent bias 7
+// against fp16's 15) and subnormal ones alike.  A 32-bit word of 4 codes
+// gives two f16x2: its even bytes (0, 2) and its odd bytes (1, 3).
+//
+// Keys: a non-transposed ldmatrix gives lane l the 4 codes of dims
+// 4*(l%4)..+3 of the matrix's token l/4 (per 16-dim, 8-token matrix); the
+// even-byte pair is the low B fragment of a k16 step and the odd-byte pair
+// the high one under the contraction-index permutation k = 2t -> 4t,
+// 2t+1 -> 4t+2, 8+2t -> 4t+1, 9+2t -> 4t+3, which the query fragments follow
+// (one 64-bit load and two byte permutes per k-step).  Values: a transposed
+// ldmatrix gives lane l the codes of k-slots 2*(l%4)+{0,1} at dims
+// 2*(l/4)+{0,1}.  The values go in as the A operand of O^T = V^T P^T (16
+// head dims by 16 tokens, so no MMA row is wasted): the even-byte pair is
+// A row l/4 (dim 2*(l/4)) and the odd-byte pair A row l/4 + 8 (the next
+// dim).  The softmax weights, as S = Q K^T leaves them in lane l (head
+// l/4, k-slots 2*(l%4)+{0,1} and +8), are exactly the B operand, one
+// column per query head.
 // The key scale multiplies the score and the value scale the softmax weight
-// (each factors out of its sum); the weights also carry an exact factor of
-// 256, removed on output, to keep them clear of fp16 subnormals.
+// (each factors out of its sum).  The weights carry an exact factor 256,
+// which keeps them clear of fp16 subnormals and cancels the values' 2^-8;
+// the keys' 2^-8 is folded into the key scale.
 
-__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// f16x2 of the codes in bytes 0 and 2, times 2^-8.
+__device__ __forceinline__ uint32_t e4m3_even_to_half2(uint32_t x) {
+    return ((x & 0x00ff00ffu) + (x & 0x00800080u)) << 7;  // the sign bit moves up one
 }
 
-__device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t sel) {
+// f16x2 of the codes in bytes 1 and 3, times 2^-8.
+__device__ __forceinline__ uint32_t e4m3_odd_to_half2(uint32_t x) {
+    const uint32_t z = (x >> 1) & 0x7f807f80u;
+    return z + (z & 0x40004000u);
+}
+
+__device__ __forceinline__ uint32_t byte_perm2(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0u), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
 }
 
 template <int D, int G>
 struct MmaFp8Policy {
-    static constexpr int KS = D / 16;
-    static constexpr int NT = D / 8;
-    static constexpr float kWeightBoost = 256.f;  // exact; removed on output
+    static constexpr int KS = D / 16;  // k-steps of S = Q K^T
+    static constexpr int MT = D / 16;  // m-tiles (16 head dims each) of O^T
+    static constexpr float kWeightBoost = 256.f;  // exact; cancels the values' 2^-8
+    static constexpr float kKeyUnscale = 256.f;   // undoes the keys' 2^-8
     uint32_t qa[KS][2];
-    float o[NT][2];
-    float m, l;
+    // O^T, m-tile mt: c0 / c2 = dims 16mt + 2g / +1 of head 2t, c1 / c3 the
+    // same dims of head 2t+1 (g = lane/4, t = lane%4)
+    float o[MT][4];
+    float m, l;  // online-softmax state of head g (row g of S)
+
+    // Token whose score is lane's i-th (s0[0], s0[1], s1[0], s1[1]).
+    __device__ __forceinline__ static int token_of(int lane, int i) {
+        return 2 * (lane & 3) + (i & 1) + 8 * (i >> 1);
+    }
 
     __device__ __forceinline__ void init(const __half *qg, float /*scale_log2*/, int lane) {
         const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             if (g < G) {
-                const uint2 w = __ldg(reinterpret_cast<const uint2 *>(qg + g * D + kk * 16 + tig * 4));
-                qa[kk][0] = w.x;
-                qa[kk][1] = w.y;
+                // q dims 4t..4t+3 -> (4t, 4t+2) and (4t+1, 4t+3)
+                const uint2 w =
+                    __ldg(reinterpret_cast<const uint2 *>(qg + g * D + kk * 16 + tig * 4));
+                qa[kk][0] = byte_perm2(w.x, w.y, 0x5410);
+                qa[kk][1] = byte_perm2(w.x, w.y, 0x7632);
             } else {
                 qa[kk][0] = qa[kk][1] = 0u;
             }
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = 0.f;
+        for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         m = kNegInf;
         l = 0.f;
     }
 
-    // kb8 / vb8: this head's key / value codes of the staged block (rows
-    // `pitch` bytes apart); value rows >= nv must hold finite codes.
-    __device__ __forceinline__ void block(uint32_t kb8, uint32_t vb8, uint32_t pitch, int nv,
-                                          float scale_log2, int lane, const float (&ks)[4],
-                                          const float (&vs)[4]) {
-        const int tig = lane & 3;
-        const uint32_t row = (((lane >> 3) & 1) * 8 + (lane & 7)) * pitch + (lane >> 4) * 16;
-        float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
+    // NB (1 or 2) staged blocks of one sequence in one online-softmax step.
+    // kb8 / vb8: the key / value code tiles of each block, this head's codes
+    // starting at byte `head` of each row; value rows >= nv must hold finite
+    // codes.  ks / vs: the key / value scales of this lane's tokens
+    // (token_of) in each block.
+    template <int NB>
+    __device__ __forceinline__ void step(const uint32_t (&kb8)[NB], const uint32_t (&vb8)[NB],
+                                         SwizzledTile tile, uint32_t head, const int (&nv)[NB],
+                                         float scale_log2, int lane, const float (&ks)[NB][4],
+                                         const float (&vs)[NB][4]) {
+        // matrices 0/1: tokens 0-7 / 8-15, codes 0-15 of a 32-code step;
+        // 2/3: the same for codes 16-31
+        const int rt = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const uint32_t col = head + (lane >> 4) * 16;
+        // S = Q K^T, two accumulator chains per n-tile
+        float x[NB][4];
 #pragma unroll
-        for (int kp = 0; kp < D / 32; ++kp) {
-            uint32_t r0, r1, r2, r3;  // tokens 0-7 / 8-15, dims 32kp.. / 32kp+16..
-            ldsm_x4(r0, r1, r2, r3, kb8 + row + kp * 32);
-            mma_rows0_7(s0[0], s0[1], qa[2 * kp][0], qa[2 * kp][1], e4m3x2_to_half2(r0),
-                        e4m3x2_to_half2(r0 >> 16));
-            mma_rows0_7(s1[0], s1[1], qa[2 * kp][0], qa[2 * kp][1], e4m3x2_to_half2(r1),
-                        e4m3x2_to_half2(r1 >> 16));
-            mma_rows0_7(s0[0], s0[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1], e4m3x2_to_half2(r2),
-                        e4m3x2_to_half2(r2 >> 16));
-            mma_rows0_7(s1[0], s1[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1], e4m3x2_to_half2(r3),
-                        e4m3x2_to_half2(r3 >> 16));
+        for (int b = 0; b < NB; ++b) {
+            float s0a[2] = {0.f, 0.f}, s1a[2] = {0.f, 0.f}, s0b[2] = {0.f, 0.f},
+                  s1b[2] = {0.f, 0.f};
+#pragma unroll
+            for (int kp = 0; kp < D / 32; ++kp) {
+                uint32_t r0, r1, r2, r3;  // tokens 0-7 / 8-15, dims 32kp.. / 32kp+16..
+                ldsm_x4(r0, r1, r2, r3, kb8[b] + tile.at(rt, col + kp * 32));
+                mma_rows0_7(s0a[0], s0a[1], qa[2 * kp][0], qa[2 * kp][1], e4m3_even_to_half2(r0),
+                            e4m3_odd_to_half2(r0));
+                mma_rows0_7(s1a[0], s1a[1], qa[2 * kp][0], qa[2 * kp][1], e4m3_even_to_half2(r1),
+                            e4m3_odd_to_half2(r1));
+                mma_rows0_7(s0b[0], s0b[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1],
+                            e4m3_even_to_half2(r2), e4m3_odd_to_half2(r2));
+                mma_rows0_7(s1b[0], s1b[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1],
+                            e4m3_even_to_half2(r3), e4m3_odd_to_half2(r3));
+            }
+            x[b][0] = s0a[0] + s0b[0];
+            x[b][1] = s0a[1] + s0b[1];
+            x[b][2] = s1a[0] + s1b[0];
+            x[b][3] = s1a[1] + s1b[1];
         }
-        float x[4] = {s0[0], s0[1], s1[0], s1[1]};
-        const int t0 = tig * 2;
-        const int tok[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
         float mx = kNegInf;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            x[i] = tok[i] < nv ? (x[i] * ks[i]) * scale_log2 : kNegInf;
-            mx = fmaxf(mx, x[i]);
-        }
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[b][i] = token_of(lane, i) < nv[b]
+                              ? (x[b][i] * (ks[b][i] * kKeyUnscale)) * scale_log2
+                              : kNegInf;
+                mx = fmaxf(mx, x[b][i]);
+            }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float mnew = fmaxf(m, mx);
         const float alpha = exp2f(m - mnew);
-        float pw[4], psum = 0.f;
+        float psum = 0.f;
+        uint32_t pa[NB][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float pi = exp2f(x[i] - mnew);
-            psum += pi;
-            pw[i] = tok[i] < nv ? pi * (vs[i] * kWeightBoost) : 0.f;
+        for (int b = 0; b < NB; ++b) {
+            float pw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float pi = exp2f(x[b][i] - mnew);
+                psum += pi;
+                pw[i] = token_of(lane, i) < nv[b] ? pi * (vs[b][i] * kWeightBoost) : 0.f;
+            }
+            pa[b][0] = pack_half2(pw[0], pw[1]);
+            pa[b][1] = pack_half2(pw[2], pw[3]);
         }
-        const uint32_t pa0 = pack_half2(pw[0], pw[1]);
-        const uint32_t pa2 = pack_half2(pw[2], pw[3]);
         l = l * alpha + psum;
         m = mnew;
+        // O^T += V^T P^T: the weight fragments pa are already the B operand
+        // (column n = head g); O^T's columns are heads 2t, 2t+1, whose
+        // rescale factors live in rows 2t, 2t+1 of S
+        const int t = lane & 3;
+        const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) << 2);
+        const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) << 2);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            o[nt][0] *= alpha;
-            o[nt][1] *= alpha;
+        for (int mt = 0; mt < MT; ++mt) {
+            o[mt][0] *= a_lo;
+            o[mt][1] *= a_hi;
+            o[mt][2] *= a_lo;
+            o[mt][3] *= a_hi;
         }
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-            uint32_t r0, r1, r2, r3;  // tokens 0-7 / 8-15, dims 32q.. / 32q+16..
-            ldsm_x4_trans(r0, r1, r2, r3, vb8 + row + q * 32);
-            // even dims: bytes 0 and 2; odd dims: bytes 1 and 3
-            mma_rows0_7(o[4 * q][0], o[4 * q][1], pa0, pa2,
-                        e4m3x2_to_half2(byte_perm(r0, 0x20)), e4m3x2_to_half2(byte_perm(r1, 0x20)));
-            mma_rows0_7(o[4 * q + 1][0], o[4 * q + 1][1], pa0, pa2,
-                        e4m3x2_to_half2(byte_perm(r0, 0x31)), e4m3x2_to_half2(byte_perm(r1, 0x31)));
-            mma_rows0_7(o[4 * q + 2][0], o[4 * q + 2][1], pa0, pa2,
-                        e4m3x2_to_half2(byte_perm(r2, 0x20)), e4m3x2_to_half2(byte_perm(r3, 0x20)));
-            mma_rows0_7(o[4 * q + 3][0], o[4 * q + 3][1], pa0, pa2,
-                        e4m3x2_to_half2(byte_perm(r2, 0x31)), e4m3x2_to_half2(byte_perm(r3, 0x31)));
+        for (int b = 0; b < NB; ++b) {
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t r0, r1, r2, r3;  // k-slots 0-7 / 8-15, dims 32q.. / 32q+16..
+                ldsm_x4_trans(r0, r1, r2, r3, vb8[b] + tile.at(rt, col + q * 32));
+                // A = V^T: row g <- even dims (even bytes), row g+8 <- odd dims
+                mma_16816(o[2 * q], e4m3_even_to_half2(r0), e4m3_odd_to_half2(r0),
+                          e4m3_even_to_half2(r1), e4m3_odd_to_half2(r1), pa[b][0], pa[b][1]);
+                mma_16816(o[2 * q + 1], e4m3_even_to_half2(r2), e4m3_odd_to_half2(r2),
+                          e4m3_even_to_half2(r3), e4m3_odd_to_half2(r3), pa[b][0], pa[b][1]);
+            }
         }
     }
 
@@ -290,48 +377,40 @@ struct MmaFp8Policy {
         return ls;
     }
 
-    // n-tile pair (2c, 2c+1), element j: dims 16c + 4t + 2j and the next one
+    // Final fp16 output o / l of heads h < G at out_g0 + h*D (zeros if empty).
     __device__ __forceinline__ void write_output(__half *out_g0, int lane) {
-        const int g = lane >> 2, tig = lane & 3;
+        const int g = lane >> 2, t = lane & 3;
         const float ls = l_total();
-        if (g < G) {
-            const float inv = ls > 0.f ? (1.f / kWeightBoost) / ls : 0.f;
+        const float l0 = __shfl_sync(0xffffffffu, ls, (2 * t) << 2);
+        const float l1 = __shfl_sync(0xffffffffu, ls, (2 * t + 1) << 2);
+        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
-            for (int c = 0; c < NT / 2; ++c)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    *reinterpret_cast<__half2 *>(out_g0 + g * D + 16 * c + 4 * tig + 2 * j) =
-                        __floats2half2_rn(o[2 * c][j] * inv, o[2 * c + 1][j] * inv);
+        for (int mt = 0; mt < MT; ++mt) {
+            if (2 * t < G)
+                *reinterpret_cast<__half2 *>(out_g0 + (2 * t) * D + 16 * mt + 2 * g) =
+                    __floats2half2_rn(o[mt][0] * i0, o[mt][2] * i0);
+            if (2 * t + 1 < G)
+                *reinterpret_cast<__half2 *>(out_g0 + (2 * t + 1) * D + 16 * mt + 2 * g) =
+                    __floats2half2_rn(o[mt][1] * i1, o[mt][3] * i1);
         }
     }
 
+    // Partial state to global memory: ml[h] = (m, l), o[h*D + d] for h < G.
     __device__ __forceinline__ void write_partial(float2 *ml, float *og, int lane) {
-        const int g = lane >> 2, tig = lane & 3;
+        const int g = lane >> 2, t = lane & 3;
         const float ls = l_total();
-        if (g < G) {
-            if (tig == 0) ml[g] = make_float2(m, ls);
-            const float u = 1.f / kWeightBoost;
+        if (g < G && t == 0) ml[g] = make_float2(m, ls);
 #pragma unroll
-            for (int c = 0; c < NT / 2; ++c)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    *reinterpret_cast<float2 *>(og + g * D + 16 * c + 4 * tig + 2 * j) =
-                        make_float2(o[2 * c][j] * u, o[2 * c + 1][j] * u);
+        for (int mt = 0; mt < MT; ++mt) {
+            if (2 * t < G)
+                *reinterpret_cast<float2 *>(og + (2 * t) * D + 16 * mt + 2 * g) =
+                    make_float2(o[mt][0], o[mt][2]);
+            if (2 * t + 1 < G)
+                *reinterpret_cast<float2 *>(og + (2 * t + 1) * D + 16 * mt + 2 * g) =
+                    make_float2(o[mt][1], o[mt][3]);
         }
     }
 };
-
-// Zero the value codes of rows [nv, 16) of one head (D bytes per row), then
-// order those generic-proxy writes before later bulk copies into the stage.
-template <int D>
-__device__ __forceinline__ void zero_tail_rows_fp8(uint32_t vb8, uint32_t pitch, int nv, int lane) {
-    for (int e = lane; e < (kBS - nv) * (D / 16); e += 32) {
-        const uint32_t a = vb8 + (nv + e / (D / 16)) * pitch + (e % (D / 16)) * 16;
-        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-}
 
 // ---------------------------------------------------------------------------
 // SIMT policy (fp32 FMAs on CUDA cores): lane l owns dims [l*DPL, (l+1)*DPL)
@@ -411,9 +490,10 @@ struct SimtPolicy {
         }
     }
 
-    __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, uint32_t pitch, int nv,
-                                          float /*scale*/, int lane, float *pbuf) {
-        const uint32_t lane_off = lane * DPL * 2;
+    __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, SwizzledTile tile,
+                                          uint32_t head, int nv, float /*scale*/, int lane,
+                                          float *pbuf) {
+        const uint32_t lane_off = head + lane * DPL * 2;
         const int idx = lane / R;  // result index held by this lane: token*G + head
         float s[NCH];
 #pragma unroll
@@ -422,7 +502,7 @@ struct SimtPolicy {
 #pragma unroll
             for (int t = 0; t < TC; ++t) {
                 float kx[DPL];
-                load_row(kb + (c * TC + t) * pitch + lane_off, kx);
+                load_row(kb + tile.at(c * TC + t, lane_off), kx);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float acc = 0.f;
@@ -466,7 +546,7 @@ struct SimtPolicy {
             for (int i = 0; i < DPL; ++i) o[g][i] *= alpha[g];
         for (int t = 0; t < nv; ++t) {
             float vx[DPL];
-            load_row(vb + t * pitch + lane_off, vx);
+            load_row(vb + tile.at(t, lane_off), vx);
             float pt[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) pt[g] = pbuf[t * G + g];
@@ -523,16 +603,26 @@ struct SimtPolicy {
     }
 };
 
-// Zero value rows [nv, 16) of one head's staged tile (row bytes D*2), then
-// order those generic-proxy writes before later bulk copies into the stage.
-template <int D>
-__device__ __forceinline__ void zero_tail_rows(uint32_t vb, uint32_t pitch, int nv, int lane) {
-    for (int e = lane; e < (kBS - nv) * (D / 8); e += 32) {
-        const uint32_t a = vb + (nv + e / (D / 8)) * pitch + (e % (D / 8)) * 16;
+// Zero bytes [head, head + ROW_BYTES) of value rows [nv, 16) of a staged
+// tile (one head's slice), then order those generic-proxy writes before
+// later bulk copies into the stage.
+template <int ROW_BYTES>
+__device__ __forceinline__ void zero_tail_bytes(uint32_t vb, SwizzledTile tile, uint32_t head,
+                                                int nv, int lane) {
+    constexpr int kUnits = ROW_BYTES / 16;
+    for (int e = lane; e < (kBS - nv) * kUnits; e += 32) {
+        const uint32_t a = vb + tile.at(nv + e / kUnits, head + (e % kUnits) * 16);
         asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
     }
     fence_proxy_async_smem();
     __syncwarp();
+}
+
+// Zero value rows [nv, 16) of one head's fp16 slice (D*2 bytes at `head`).
+template <int D>
+__device__ __forceinline__ void zero_tail_rows(uint32_t vb, SwizzledTile tile, uint32_t head,
+                                               int nv, int lane) {
+    zero_tail_bytes<D * 2>(vb, tile, head, nv, lane);
 }
 
 }  // namespace dec

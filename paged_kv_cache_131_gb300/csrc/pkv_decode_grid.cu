@@ -8,8 +8,8 @@
 //      length), then keeps the ids of the partition's blocks, checking each
 //      against [0, num_blocks);
 //   2. gives each warp every 4th block of the partition and a private
-//      2-stage ring: 16 lanes each issue one bulk (TMA) copy of a key row
-//      (head_dim*2 bytes of kv_head) and 16 lanes one of a value row,
+//      2-stage ring: one tiled tensor copy (TMA) brings kv_head's slice
+//      (head_dim*2 bytes) of the block's 16 key rows and one its value rows,
 //      completing on the stage's mbarrier;
 //   3. folds each block into the warp's online-softmax state (compute
 //      policy of pkv_decode_common.cuh);
@@ -40,13 +40,13 @@ constexpr int kMaxBtPerThread = (kMaxPartitionTokens / kBS + kThreads - 1) / kTh
 
 template <int D>
 struct Geo {
-    static constexpr int kRowBytes = D * 2 + kRowPad;
+    static constexpr int kRowBytes = D * 2;  // one head's row of a token
     static constexpr int kTileBytes = kBS * kRowBytes;  // one K (or V) block tile
     static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
     static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
 };
 
-// Shared-memory layout (dynamic):
+// Shared-memory layout (dynamic, from a 1024-byte aligned base):
 //   ring    kWarps * kStages * (K tile + V tile) -- reused after the main loop
 //           by the warp merge and the partition combine
 //   bars    kWarps * kStages mbarriers
@@ -55,9 +55,12 @@ struct Geo {
 //   pbuf    kWarps * 16 * G fp32 (SIMT policy: one block's softmax weights)
 
 template <int D, int G, class Policy>
-__global__ void __launch_bounds__(kThreads) decode_grid_kernel(const GridParams p) {
+__global__ void __launch_bounds__(kThreads)
+    decode_grid_kernel(const __grid_constant__ GridParams p) {
     using Gm = Geo<D>;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((kTileAlign - (smem_u32(smem_raw) & (kTileAlign - 1))) &
+                                (kTileAlign - 1));
     uint8_t *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Gm::kRingBytes);
     int *bt_s = reinterpret_cast<int *>(bars + kWarps * kStages);
@@ -127,11 +130,11 @@ __global__ void __launch_bounds__(kThreads) decode_grid_kernel(const GridParams 
     float *pbuf = pbuf_all + warp * kBS * G;
 
     const int nw = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+    // the map's chunks are those of the whole row (all heads), a multiple of 128 bytes
+    const SwizzledTile tile{7u};
+    const int head_chunk = kvh * (Gm::kRowBytes / 128);
     const uint32_t ring_s = smem_u32(ring + warp * kStages * Gm::kStageBytes);
     const uint32_t bar_s = smem_u32(&bars[warp * kStages]);
-    const int64_t row_elems = static_cast<int64_t>(p.num_kv_heads) * D;
-    const __half *kbase = p.k_cache + kvh * D;
-    const __half *vbase = p.v_cache + kvh * D;
 
     auto valid_tokens = [&](int i) -> int {
         const int j = warp + i * kWarps;
@@ -142,16 +145,14 @@ __global__ void __launch_bounds__(kThreads) decode_grid_kernel(const GridParams 
         const int nv = valid_tokens(i);
         const int s = i % kStages;
         const uint32_t bar = bar_s + s * 8;
-        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nv) * D * 2 * 2);
+        // whole 16-row tiles: rows past the last valid token still belong to
+        // the physical block
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar, nv > 0 ? 2u * Gm::kTileBytes : 0u);
         __syncwarp();
-        const int r = lane & (kBS - 1);
-        if (r < nv) {
-            const int64_t row = (static_cast<int64_t>(bt_s[j]) * kBS + r) * row_elems;
-            const __half *src = (lane < kBS ? kbase : vbase) + row;
-            const uint32_t dst = ring_s + s * Gm::kStageBytes + (lane < kBS ? 0 : Gm::kTileBytes) +
-                                 r * Gm::kRowBytes;
-            bulk_g2s(dst, src, D * 2, bar);
-        }
+        if (nv > 0 && lane < 2)
+            tensor_g2s_3d(ring_s + s * Gm::kStageBytes + lane * Gm::kTileBytes,
+                          lane == 0 ? &p.tm_k : &p.tm_v, 0, bt_s[j] * kBS, head_chunk, bar);
     };
 
     const int npre = nw < kStages ? nw : kStages;
@@ -169,8 +170,8 @@ __global__ void __launch_bounds__(kThreads) decode_grid_kernel(const GridParams 
         if (nv > 0) {
             const uint32_t kb = ring_s + s * Gm::kStageBytes;
             if (Policy::kZeroTailRows && nv < kBS)
-                zero_tail_rows<D>(kb + Gm::kTileBytes, Gm::kRowBytes, nv, lane);
-            st.block(kb, kb + Gm::kTileBytes, Gm::kRowBytes, nv, p.scale_log2, lane, pbuf);
+                zero_tail_rows<D>(kb + Gm::kTileBytes, tile, 0u, nv, lane);
+            st.block(kb, kb + Gm::kTileBytes, tile, 0u, nv, p.scale_log2, lane, pbuf);
         }
         __syncwarp();
         if (i + kStages < nw) {
@@ -303,9 +304,11 @@ GridFn select(int D, int G, bool simt) {
 
 }  // namespace
 
+int grid_ring_bytes(int D) { return kWarps * kStages * 2 * kBS * D * 2; }
+
 int grid_smem_bytes(int D, int G, int partition_blocks) {
-    const int ring = kWarps * kStages * 2 * kBS * (D * 2 + kRowPad);
-    return ring + kWarps * kStages * 8 + partition_blocks * 4 + 4 * 4 + kWarps * kBS * G * 4;
+    return kTileAlign + grid_ring_bytes(D) + kWarps * kStages * 8 + partition_blocks * 4 +
+           4 * 4 + kWarps * kBS * G * 4;
 }
 
 int64_t grid_workspace_bytes(int64_t S, int64_t H, int64_t D, int64_t P) {

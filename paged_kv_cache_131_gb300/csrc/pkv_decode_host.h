@@ -3,6 +3,7 @@
 // CTAs over equal ranges of the (sequence, block) space).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (a 128-byte descriptor; no driver call here)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -19,9 +20,26 @@ constexpr int kMaxPartitionTokens = 8192;
 constexpr int kDefaultPartitionTokens = 512;
 constexpr int kMaxBalancedKvHeads = 8;   // consumer warps per CTA (+1 producer)
 constexpr int kSmemPerSM = 227 * 1024;   // opt-in dynamic shared memory per CTA
+constexpr int kTileAlign = 1024;         // staged tiles start 1024-byte aligned (swizzle)
+
+// Bytes of a staged row's swizzle chunk: 128 when the row is a multiple of
+// 128 bytes, else 64 (rows are always a multiple of 64).
+__host__ __device__ constexpr int chunk_bytes_for_row(int row_bytes) {
+    return row_bytes % 128 == 0 ? 128 : 64;
+}
+
+// Tensor map over a token-major cache [num_blocks * 16 rows][row_bytes]
+// viewed as {chunk bytes, token rows, chunks} (the chunk stride is smaller
+// than the row stride), with a box of {chunk, 16 tokens, box_chunks} and the
+// chunk's swizzle.  A box lands in shared memory as 16 * box_chunks * chunk
+// bytes, chunk-major.  Returns a PKV status.
+int make_kv_tensor_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int row_bytes,
+                       int box_chunks);
 
 // Grid schedule.
 struct GridParams {
+    CUtensorMap tm_k;  // per-head boxes of the key / value caches
+    CUtensorMap tm_v;
     __half *out;
     const __half *q;
     const __half *k_cache;
@@ -41,6 +59,8 @@ struct GridParams {
     ErrorRecord *err;
 };
 
+// Bytes of the grid schedule's staging rings (reused by its combine).
+int grid_ring_bytes(int D);
 int grid_smem_bytes(int D, int G, int partition_blocks);
 int64_t grid_workspace_bytes(int64_t S, int64_t H, int64_t D, int64_t P);
 int launch_grid(const GridParams &p, int D, int G, bool simt, int num_seqs,
@@ -48,6 +68,8 @@ int launch_grid(const GridParams &p, int D, int G, bool simt, int num_seqs,
 
 // Balanced schedule.
 struct BalancedParams {
+    CUtensorMap tm_k;  // whole-row boxes of the key / value caches
+    CUtensorMap tm_v;
     __half *out;
     const __half *q;
     const __half *k_cache;
@@ -60,7 +82,7 @@ struct BalancedParams {
     int num_kv_heads;
     int max_blocks_per_seq;
     int num_stages;  // staging ring depth (blocks in flight per CTA)
-    int pitch;       // staged row pitch in bytes: Hk*D*elem + 16
+    int row_bytes;   // staged row: all KV heads of one token, Hk*D*elem bytes
     const float *k_scale;  // FP8 caches: [NB, 16, Hk] per-row scales (else null)
     const float *v_scale;
     int64_t num_blocks;
@@ -73,15 +95,16 @@ struct BalancedParams {
 struct BalancedShape {
     bool ok;          // the schedule supports this shape
     int stages;       // ring depth
-    int pitch;        // staged row pitch
+    int row_bytes;    // staged row bytes
     int smem;         // dynamic shared memory per CTA
     int ctas_per_sm;  // resident CTAs per SM
     int grid;         // CTAs launched
     int64_t workspace;  // bytes of scratch it needs
 };
 
+// Shape of the balanced launch for fp16 or FP8 caches.
 BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms,
-                             bool fp8 = false);
+                             bool fp8);
 int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
                     bool fp8, cudaStream_t stream);
 

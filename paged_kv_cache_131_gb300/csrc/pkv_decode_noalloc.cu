@@ -75,7 +75,7 @@ extern "C" int pkv_decode_attention_noalloc(void *out, const void *q, const void
     // the grid schedule's.  Larger shapes are refused before anything runs.
     const int G = num_heads / num_kv_heads;
     const dec::BalancedShape bal =
-        dec::balanced_shape(num_seqs, num_kv_heads, G, head_dim, sm_count());
+        dec::balanced_shape(num_seqs, num_kv_heads, G, head_dim, sm_count(), false);
     const int64_t P = std::max<int64_t>(
         1, (static_cast<int64_t>(max_seq_len) + dec::kDefaultPartitionTokens - 1) /
                dec::kDefaultPartitionTokens);

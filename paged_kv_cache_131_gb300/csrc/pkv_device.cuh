@@ -97,6 +97,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Tiled tensor copy global -> shared through a 3-d tensor map (TMA): the box
+// at coordinates (c0, c1, c2) lands at dst laid out and swizzled as the map
+// says, completion signalled on `bar` as transaction bytes.  `tmap` is the
+// generic address of a CUtensorMap held in kernel parameter space.
+__device__ __forceinline__ void tensor_g2s_3d(uint32_t dst, const void *tmap, int c0, int c1,
+                                              int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 // Same with an L2 cache-policy hint (createpolicy).
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes,
                                               uint32_t bar, uint64_t policy) {
@@ -151,16 +164,31 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t &r0, uint32_t &r1, uint32
                  : "r"(addr));
 }
 
+// The MMAs are pure register operations (no volatile), so the compiler may
+// interleave independent ones; the ldmatrix loads above stay volatile, which
+// keeps them after the mbarrier waits that make their data valid.
+
 // D(16x8) += A(16x16) * B(16x8) with A rows 8..15 zero: only the first
 // two accumulators (row lane/4) are carried; a1/a3 (rows 8..15) are zero.
 __device__ __forceinline__ void mma_rows0_7(float &c0, float &c1, uint32_t a0, uint32_t a2,
                                             uint32_t b0, uint32_t b1) {
     float d2, d3;
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%10,%11};"
         : "+f"(c0), "+f"(c1), "=f"(d2), "=f"(d3)
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f), "f"(0.f));
+}
+
+// D(16x8) += A(16x16) * B(16x8), all 16 rows.  Fragments (g = lane/4,
+// t = lane%4): a0 = A[g][2t..2t+1], a1 = A[g+8][2t..], a2 = A[g][2t+8..],
+// a3 = A[g+8][2t+8..]; b0 = B[2t..2t+1][g], b1 = B[2t+8..2t+9][g];
+// c = {D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]}.
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
