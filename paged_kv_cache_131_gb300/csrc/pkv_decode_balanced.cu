@@ -379,11 +379,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     };
 
     // FP8 scales of this lane's tokens in a staged block
-    auto load_scales = [&](int s, float (&ks)[4], float (&vs)[4]) {
+    using Fp8 = MmaFp8Policy<D, G>;
+    constexpr int kLT = Fp8::kLaneTokens;
+    auto load_scales = [&](int s, float (&ks)[kLT], float (&vs)[kLT]) {
         const float *sc = reinterpret_cast<const float *>(ring + s * stage_bytes + 2 * tile_bytes);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int tok = MmaFp8Policy<D, G>::token_of(lane, t);
+        for (int t = 0; t < kLT; ++t) {
+            const int tok = Fp8::token_of(lane, t);
             ks[t] = sc[tok * Hk + kvh];
             vs[t] = sc[kBS * Hk + tok * Hk + kvh];
         }
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             if (mt2.x == mt.x && mt2.z >= 0 && mt2.y > 0) {
                 const uint32_t kb8b = ring_s + s2 * stage_bytes;
                 if (mt2.y < kBS) zero_tail_bytes<D>(kb8b + tile_bytes, tile, head, mt2.y, lane);
-                float ks[2][4], vs[2][4];
+                float ks[2][kLT], vs[2][kLT];
                 load_scales(s, ks[0], vs[0]);
                 load_scales(s2, ks[1], vs[1]);
                 const uint32_t kbs[2] = {kb8, kb8b};
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 used = 2;
             } else if (mt.z >= 0 && mt.y > 0) {
                 if (mt.y < kBS) zero_tail_bytes<D>(kb8 + tile_bytes, tile, head, mt.y, lane);
-                float ks[1][4], vs[1][4];
+                float ks[1][kLT], vs[1][kLT];
                 load_scales(s, ks[0], vs[0]);
                 const uint32_t kbs[1] = {kb8};
                 const uint32_t vbs[1] = {kb8 + tile_bytes};

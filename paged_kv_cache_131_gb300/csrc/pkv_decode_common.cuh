@@ -195,83 +195,78 @@ struct MmaPolicy {
 // MMA policy over FP8 (E4M3) staged tiles, fed to the fp16 MMA without a
 // shared-memory round trip.  Tokens are tiled 0-7 / 8-15 as in MmaPolicy.
 //
-// Codes become fp16 by integer bit moves, not by a conversion instruction:
-// an E4M3 code s.eeee.mmm with its sign moved to bit 15 and its 7 other bits
-// placed at bits 7..13 is the fp16 s.0eeee.mmm0000000, whose value is the
-// code's value times 2^-8 exactly -- for normal codes (exponent bias 7
-// against fp16's 15) and subnormal ones alike.  A 32-bit word of 4 codes
-// gives two f16x2: its even bytes (0, 2) and its odd bytes (1, 3).
+// Codes become fp16 through the hardware conversion of an E4M3 pair to an
+// f16 pair (exact: every E4M3 value is an fp16 value).  Measured against an
+// all-integer conversion (moving the sign and the 7 other bits of each code
+// into place, ~3.5 ALU operations a pair) it is the faster: the conversions
+// are most of the FP8 consumer's extra work.
 //
-// Keys: a non-transposed ldmatrix gives lane l the 4 codes of dims
-// 4*(l%4)..+3 of the matrix's token l/4 (per 16-dim, 8-token matrix); the
-// even-byte pair is the low B fragment of a k16 step and the odd-byte pair
-// the high one under the contraction-index permutation k = 2t -> 4t,
-// 2t+1 -> 4t+2, 8+2t -> 4t+1, 9+2t -> 4t+3, which the query fragments follow
-// (one 64-bit load and two byte permutes per k-step).  Values: a transposed
-// ldmatrix gives lane l the codes of k-slots 2*(l%4)+{0,1} at dims
-// 2*(l/4)+{0,1}.  The values go in as the A operand of O^T = V^T P^T (16
-// head dims by 16 tokens, so no MMA row is wasted): the even-byte pair is
-// A row l/4 (dim 2*(l/4)) and the odd-byte pair A row l/4 + 8 (the next
-// dim).  The softmax weights, as S = Q K^T leaves them in lane l (head
-// l/4, k-slots 2*(l%4)+{0,1} and +8), are exactly the B operand, one
-// column per query head.
+// Scores are computed transposed, S^T = K Q^T (16 tokens by 8 query-head
+// columns per MMA, so no row is wasted on keys): a non-transposed ldmatrix
+// gives lane l the 4 codes of dims 4*(l%4)..+3 of the matrix's token l/4
+// (per 16-dim, 8-token matrix); the low code pair is A row l/4 at k-slots
+// 2*(l%4)+{0,1} and the high pair the same row at k-slots +8, under the
+// contraction-index permutation k = 2t+j -> 4t+j, k = 8+2t+j -> 4t+2+j,
+// which the query fragments (the B operand, one 64-bit load per k-step)
+// follow.  Lane l then holds the scores of tokens l/4 and l/4+8 for heads
+// 2*(l%4) and 2*(l%4)+1, and keeps the online-softmax state of those two
+// heads (the max over tokens is a butterfly over the lanes of one l%4).
+// Values: a transposed ldmatrix gives lane l the codes of k-slots
+// 2*(l%4)+{0,1} at dims 2*(l/4)+{0,1}.  They go in as the A operand of
+// O^T = V^T P^T (16 head dims by 16 tokens): a byte permute gathers the two
+// k-slots of the even dim, which become A row l/4, and those of the odd dim,
+// A row l/4 + 8.  The fp16 weights, transposed per 8x8 half by movmatrix,
+// are the B operand, one column per query head; O^T's columns are then the
+// same two heads whose softmax state the lane keeps.
 // The key scale multiplies the score and the value scale the softmax weight
-// (each factors out of its sum).  The weights carry an exact factor 256,
-// which keeps them clear of fp16 subnormals and cancels the values' 2^-8;
-// the keys' 2^-8 is folded into the key scale.
+// (each factors out of its sum); the weights also carry an exact factor of
+// 256, removed on output, to keep them clear of fp16 subnormals.
 
-// f16x2 of the codes in bytes 0 and 2, times 2^-8.
-__device__ __forceinline__ uint32_t e4m3_even_to_half2(uint32_t x) {
-    return ((x & 0x00ff00ffu) + (x & 0x00800080u)) << 7;  // the sign bit moves up one
-}
-
-// f16x2 of the codes in bytes 1 and 3, times 2^-8.
-__device__ __forceinline__ uint32_t e4m3_odd_to_half2(uint32_t x) {
-    const uint32_t z = (x >> 1) & 0x7f807f80u;
-    return z + (z & 0x40004000u);
-}
-
-__device__ __forceinline__ uint32_t byte_perm2(uint32_t a, uint32_t b, uint32_t sel) {
+// f16x2 of the E4M3 codes in the low 16 bits of x (low code -> low half).
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t x) {
     uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(x)));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0u), "r"(sel));
     return r;
 }
 
 template <int D, int G>
 struct MmaFp8Policy {
-    static constexpr int KS = D / 16;  // k-steps of S = Q K^T
+    static constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
     static constexpr int MT = D / 16;  // m-tiles (16 head dims each) of O^T
-    static constexpr float kWeightBoost = 256.f;  // exact; cancels the values' 2^-8
-    static constexpr float kKeyUnscale = 256.f;   // undoes the keys' 2^-8
-    uint32_t qa[KS][2];
+    static constexpr int kLaneTokens = 2;  // tokens whose scales a lane needs per block
+    static constexpr float kWeightBoost = 256.f;  // exact; removed on output
+    uint32_t qb[KS][2];  // B operand of S^T: query dims of head l/4
     // O^T, m-tile mt: c0 / c2 = dims 16mt + 2g / +1 of head 2t, c1 / c3 the
     // same dims of head 2t+1 (g = lane/4, t = lane%4)
     float o[MT][4];
-    float m, l;  // online-softmax state of head g (row g of S)
+    float m[2], l[2];  // online-softmax state of heads 2t, 2t+1 (l: this lane's tokens)
 
-    // Token whose score is lane's i-th (s0[0], s0[1], s1[0], s1[1]).
-    __device__ __forceinline__ static int token_of(int lane, int i) {
-        return 2 * (lane & 3) + (i & 1) + 8 * (i >> 1);
-    }
+    // Token of this lane's i-th score row (i = 0, 1).
+    __device__ __forceinline__ static int token_of(int lane, int i) { return (lane >> 2) + 8 * i; }
 
     __device__ __forceinline__ void init(const __half *qg, float /*scale_log2*/, int lane) {
         const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
             if (g < G) {
-                // q dims 4t..4t+3 -> (4t, 4t+2) and (4t+1, 4t+3)
                 const uint2 w =
                     __ldg(reinterpret_cast<const uint2 *>(qg + g * D + kk * 16 + tig * 4));
-                qa[kk][0] = byte_perm2(w.x, w.y, 0x5410);
-                qa[kk][1] = byte_perm2(w.x, w.y, 0x7632);
+                qb[kk][0] = w.x;
+                qb[kk][1] = w.y;
             } else {
-                qa[kk][0] = qa[kk][1] = 0u;
+                qb[kk][0] = qb[kk][1] = 0u;
             }
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-        m = kNegInf;
-        l = 0.f;
+        m[0] = m[1] = kNegInf;
+        l[0] = l[1] = 0.f;
     }
 
     // NB (1 or 2) staged blocks of one sequence in one online-softmax step.
@@ -282,78 +277,78 @@ struct MmaFp8Policy {
     template <int NB>
     __device__ __forceinline__ void step(const uint32_t (&kb8)[NB], const uint32_t (&vb8)[NB],
                                          SwizzledTile tile, uint32_t head, const int (&nv)[NB],
-                                         float scale_log2, int lane, const float (&ks)[NB][4],
-                                         const float (&vs)[NB][4]) {
+                                         float scale_log2, int lane,
+                                         const float (&ks)[NB][kLaneTokens],
+                                         const float (&vs)[NB][kLaneTokens]) {
         // matrices 0/1: tokens 0-7 / 8-15, codes 0-15 of a 32-code step;
         // 2/3: the same for codes 16-31
         const int rt = ((lane >> 3) & 1) * 8 + (lane & 7);
         const uint32_t col = head + (lane >> 4) * 16;
-        // S = Q K^T, two accumulator chains per n-tile
-        float x[NB][4];
+        // S^T = K Q^T, two accumulator chains per block
+        float x[NB][4];  // token g: heads 2t, 2t+1; token g+8: heads 2t, 2t+1
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            float s0a[2] = {0.f, 0.f}, s1a[2] = {0.f, 0.f}, s0b[2] = {0.f, 0.f},
-                  s1b[2] = {0.f, 0.f};
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kp = 0; kp < D / 32; ++kp) {
                 uint32_t r0, r1, r2, r3;  // tokens 0-7 / 8-15, dims 32kp.. / 32kp+16..
                 ldsm_x4(r0, r1, r2, r3, kb8[b] + tile.at(rt, col + kp * 32));
-                mma_rows0_7(s0a[0], s0a[1], qa[2 * kp][0], qa[2 * kp][1], e4m3_even_to_half2(r0),
-                            e4m3_odd_to_half2(r0));
-                mma_rows0_7(s1a[0], s1a[1], qa[2 * kp][0], qa[2 * kp][1], e4m3_even_to_half2(r1),
-                            e4m3_odd_to_half2(r1));
-                mma_rows0_7(s0b[0], s0b[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1],
-                            e4m3_even_to_half2(r2), e4m3_odd_to_half2(r2));
-                mma_rows0_7(s1b[0], s1b[1], qa[2 * kp + 1][0], qa[2 * kp + 1][1],
-                            e4m3_even_to_half2(r3), e4m3_odd_to_half2(r3));
+                mma_16816(sa, e4m3x2_to_half2(r0), e4m3x2_to_half2(r1),
+                          e4m3x2_to_half2(r0 >> 16), e4m3x2_to_half2(r1 >> 16), qb[2 * kp][0],
+                          qb[2 * kp][1]);
+                mma_16816(sb, e4m3x2_to_half2(r2), e4m3x2_to_half2(r3),
+                          e4m3x2_to_half2(r2 >> 16), e4m3x2_to_half2(r3 >> 16),
+                          qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
             }
-            x[b][0] = s0a[0] + s0b[0];
-            x[b][1] = s0a[1] + s0b[1];
-            x[b][2] = s1a[0] + s1b[0];
-            x[b][3] = s1a[1] + s1b[1];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[b][j] = sa[j] + sb[j];
         }
-        float mx = kNegInf;
+        // scale, mask, and the block max of each of the lane's two heads
+        float mx[2] = {kNegInf, kNegInf};
 #pragma unroll
         for (int b = 0; b < NB; ++b)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                x[b][i] = token_of(lane, i) < nv[b]
-                              ? (x[b][i] * (ks[b][i] * kKeyUnscale)) * scale_log2
-                              : kNegInf;
-                mx = fmaxf(mx, x[b][i]);
+            for (int j = 0; j < 4; ++j) {
+                const int r = j >> 1;  // token row: g or g+8
+                x[b][j] = token_of(lane, r) < nv[b] ? (x[b][j] * ks[b][r]) * scale_log2 : kNegInf;
+                mx[j & 1] = fmaxf(mx[j & 1], x[b][j]);
             }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mnew = fmaxf(m, mx);
-        const float alpha = exp2f(m - mnew);
-        float psum = 0.f;
-        uint32_t pa[NB][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+        }
+        float alpha[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float mnew = fmaxf(m[h], mx[h]);  // finite: some token is valid
+            alpha[h] = exp2f(m[h] - mnew);
+            m[h] = mnew;
+            l[h] *= alpha[h];
+        }
+        uint32_t pb[NB][2];  // B fragments of O^T += V^T P^T
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             float pw[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float pi = exp2f(x[b][i] - mnew);
-                psum += pi;
-                pw[i] = token_of(lane, i) < nv[b] ? pi * (vs[b][i] * kWeightBoost) : 0.f;
+            for (int j = 0; j < 4; ++j) {
+                const int r = j >> 1;
+                const float p = exp2f(x[b][j] - m[j & 1]);
+                l[j & 1] += p;
+                pw[j] = token_of(lane, r) < nv[b] ? p * (vs[b][r] * kWeightBoost) : 0.f;
             }
-            pa[b][0] = pack_half2(pw[0], pw[1]);
-            pa[b][1] = pack_half2(pw[2], pw[3]);
+            // rows = tokens 0-7 / 8-15, columns = heads; transposed to
+            // (token pair, head) B fragments
+            pb[b][0] = movmatrix_trans(pack_half2(pw[0], pw[1]));
+            pb[b][1] = movmatrix_trans(pack_half2(pw[2], pw[3]));
         }
-        l = l * alpha + psum;
-        m = mnew;
-        // O^T += V^T P^T: the weight fragments pa are already the B operand
-        // (column n = head g); O^T's columns are heads 2t, 2t+1, whose
-        // rescale factors live in rows 2t, 2t+1 of S
-        const int t = lane & 3;
-        const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) << 2);
-        const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) << 2);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            o[mt][0] *= a_lo;
-            o[mt][1] *= a_hi;
-            o[mt][2] *= a_lo;
-            o[mt][3] *= a_hi;
+            o[mt][0] *= alpha[0];
+            o[mt][1] *= alpha[1];
+            o[mt][2] *= alpha[0];
+            o[mt][3] *= alpha[1];
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
@@ -361,29 +356,34 @@ struct MmaFp8Policy {
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t r0, r1, r2, r3;  // k-slots 0-7 / 8-15, dims 32q.. / 32q+16..
                 ldsm_x4_trans(r0, r1, r2, r3, vb8[b] + tile.at(rt, col + q * 32));
-                // A = V^T: row g <- even dims (even bytes), row g+8 <- odd dims
-                mma_16816(o[2 * q], e4m3_even_to_half2(r0), e4m3_odd_to_half2(r0),
-                          e4m3_even_to_half2(r1), e4m3_odd_to_half2(r1), pa[b][0], pa[b][1]);
-                mma_16816(o[2 * q + 1], e4m3_even_to_half2(r2), e4m3_odd_to_half2(r2),
-                          e4m3_even_to_half2(r3), e4m3_odd_to_half2(r3), pa[b][0], pa[b][1]);
+                // A = V^T: row g <- the even dim (bytes 0, 2), row g+8 <- the odd one
+                mma_16816(o[2 * q], e4m3x2_to_half2(byte_perm(r0, 0x20)),
+                          e4m3x2_to_half2(byte_perm(r0, 0x31)),
+                          e4m3x2_to_half2(byte_perm(r1, 0x20)),
+                          e4m3x2_to_half2(byte_perm(r1, 0x31)), pb[b][0], pb[b][1]);
+                mma_16816(o[2 * q + 1], e4m3x2_to_half2(byte_perm(r2, 0x20)),
+                          e4m3x2_to_half2(byte_perm(r2, 0x31)),
+                          e4m3x2_to_half2(byte_perm(r3, 0x20)),
+                          e4m3x2_to_half2(byte_perm(r3, 0x31)), pb[b][0], pb[b][1]);
             }
         }
     }
 
-    __device__ __forceinline__ float l_total() const {
-        float ls = l;
-        ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-        ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    // Softmax sum of head 2t + h over all tokens (every lane of one t).
+    __device__ __forceinline__ float l_total(int h) const {
+        float ls = l[h];
+        ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 16);
         return ls;
     }
 
     // Final fp16 output o / l of heads h < G at out_g0 + h*D (zeros if empty).
     __device__ __forceinline__ void write_output(__half *out_g0, int lane) {
         const int g = lane >> 2, t = lane & 3;
-        const float ls = l_total();
-        const float l0 = __shfl_sync(0xffffffffu, ls, (2 * t) << 2);
-        const float l1 = __shfl_sync(0xffffffffu, ls, (2 * t + 1) << 2);
-        const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+        const float l0 = l_total(0), l1 = l_total(1);
+        const float u = 1.f / kWeightBoost;
+        const float i0 = l0 > 0.f ? u / l0 : 0.f, i1 = l1 > 0.f ? u / l1 : 0.f;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             if (2 * t < G)
@@ -398,16 +398,20 @@ struct MmaFp8Policy {
     // Partial state to global memory: ml[h] = (m, l), o[h*D + d] for h < G.
     __device__ __forceinline__ void write_partial(float2 *ml, float *og, int lane) {
         const int g = lane >> 2, t = lane & 3;
-        const float ls = l_total();
-        if (g < G && t == 0) ml[g] = make_float2(m, ls);
+        const float l0 = l_total(0), l1 = l_total(1);
+        if (g == 0) {
+            if (2 * t < G) ml[2 * t] = make_float2(m[0], l0);
+            if (2 * t + 1 < G) ml[2 * t + 1] = make_float2(m[1], l1);
+        }
+        const float u = 1.f / kWeightBoost;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             if (2 * t < G)
                 *reinterpret_cast<float2 *>(og + (2 * t) * D + 16 * mt + 2 * g) =
-                    make_float2(o[mt][0], o[mt][2]);
+                    make_float2(o[mt][0] * u, o[mt][2] * u);
             if (2 * t + 1 < G)
                 *reinterpret_cast<float2 *>(og + (2 * t + 1) * D + 16 * mt + 2 * g) =
-                    make_float2(o[mt][1], o[mt][3]);
+                    make_float2(o[mt][1] * u, o[mt][3] * u);
         }
     }
 };
