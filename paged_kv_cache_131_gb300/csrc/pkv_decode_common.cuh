@@ -48,23 +48,28 @@ struct SwizzledTile {
 };
 
 // ---------------------------------------------------------------------------
-// MMA policy: the G (<= 8) query heads are rows 0..G-1 of the 16-row A
-// operand of m16n8k16 fp16 MMAs with fp32 accumulation; rows 8..15 are zero
-// and never carried.  Lane l owns head row g = l/4 and columns 2*(l%4)+{0,1}
-// of every 8-wide n-tile (tokens for S = Q K^T, head dims for O += P V).
-// Token n-tile 0 holds tokens 0-7 and n-tile 1 tokens 8-15: lane l's scores
-// are those of tokens 2*(l%4) + {0, 1} and + {8, 9}, which is exactly lane
-// l's A fragment of O += P V (k-slot = token), so scores never move between
-// lanes.
+// MMA policy (fp16 tiles, m16n8k16 MMAs with fp32 accumulation), both
+// products transposed so that the 16 MMA rows are tokens or head dims and
+// the G (<= 8) query heads are the 8 columns:
+//   S^T = K Q^T: A = the key tile (ldmatrix, rows = tokens), B = the query
+//     (loaded once per sequence).  Lane l holds the scores of tokens l/4 and
+//     l/4 + 8 for heads 2*(l%4) and 2*(l%4)+1 and keeps the online-softmax
+//     state of those two heads (max over tokens: a butterfly over the lanes
+//     of one l%4).
+//   O^T = V^T P^T: A = the value tile (transposed ldmatrix, rows = dims),
+//     B = the fp16 weights, transposed per 8x8 half by movmatrix.  O^T's
+//     columns are the same two heads.
 
 template <int D, int G>
 struct MmaPolicy {
-    static constexpr int KS = D / 16;  // k-steps of S = Q K^T
-    static constexpr int NT = D / 8;   // n-tiles of O
+    static constexpr int KS = D / 16;  // k-steps of S^T (16 head dims each)
+    static constexpr int MT = D / 16;  // m-tiles (16 head dims each) of O^T
     static constexpr bool kZeroTailRows = true;  // reads all 16 value rows
-    uint32_t qa[KS][2];
-    float o[NT][2];
-    float m, l;
+    uint32_t qb[KS][2];  // B operand of S^T: query dims of head l/4
+    // O^T, m-tile mt: c0 / c2 = dims 16mt + g / + g + 8 of head 2t, c1 / c3
+    // the same dims of head 2t+1 (g = lane/4, t = lane%4)
+    float o[MT][4];
+    float m[2], l[2];  // softmax state of heads 2t, 2t+1 (l: this lane's tokens)
 
     __device__ __forceinline__ void init(const __half *qg, float /*scale_log2*/, int lane) {
         const int g = lane >> 2, tig = lane & 3;
@@ -72,16 +77,16 @@ struct MmaPolicy {
         for (int kk = 0; kk < KS; ++kk) {
             if (g < G) {
                 const uint32_t *row = reinterpret_cast<const uint32_t *>(qg + g * D + kk * 16);
-                qa[kk][0] = __ldg(row + tig);
-                qa[kk][1] = __ldg(row + 4 + tig);
+                qb[kk][0] = __ldg(row + tig);
+                qb[kk][1] = __ldg(row + 4 + tig);
             } else {
-                qa[kk][0] = qa[kk][1] = 0u;
+                qb[kk][0] = qb[kk][1] = 0u;
             }
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = 0.f;
-        m = kNegInf;
-        l = 0.f;
+        for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m[0] = m[1] = kNegInf;
+        l[0] = l[1] = 0.f;
     }
 
     // One staged block: key tile at kb, value tile at vb, this head's bytes
@@ -91,102 +96,134 @@ struct MmaPolicy {
     __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, SwizzledTile tile,
                                           uint32_t head, int nv, float scale_log2, int lane,
                                           float * /*pbuf*/) {
-        const int tig = lane & 3;
-        float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
-        // S = Q K^T: B fragments straight from the key tile; matrices 0/1:
-        // tokens 0-7, dims 0-7 / 8-15 of the k-step; 2/3: tokens 8-15
-        const int kt = (lane >> 4) * 8 + (lane & 7);
-        const uint32_t kcol = head + ((lane >> 3) & 1) * 16;
+        const int g = lane >> 2;
+        // S^T = K Q^T; ldmatrix matrices: tokens 0-7 / 8-15 (rows g / g+8 of
+        // A) at dims 0-7, then the same at dims 8-15; two accumulator chains
+        const int rt = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const uint32_t kcol = head + (lane >> 4) * 16;
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(b0, b1, b2, b3, kb + tile.at(kt, kcol + kk * 32));
-            mma_rows0_7(s0[0], s0[1], qa[kk][0], qa[kk][1], b0, b1);
-            mma_rows0_7(s1[0], s1[1], qa[kk][0], qa[kk][1], b2, b3);
+        for (int kk = 0; kk < KS; kk += 2) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(a0, a1, a2, a3, kb + tile.at(rt, kcol + kk * 32));
+            mma_16816(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+            if (kk + 1 < KS) {
+                ldsm_x4(a0, a1, a2, a3, kb + tile.at(rt, kcol + kk * 32 + 32));
+                mma_16816(sb, a0, a1, a2, a3, qb[kk + 1][0], qb[kk + 1][1]);
+            }
         }
-        float x[4] = {s0[0], s0[1], s1[0], s1[1]};
-        const int t0 = tig * 2;
-        const int tok[4] = {t0, t0 + 1, t0 + 8, t0 + 9};
-        float mx = kNegInf;
+        float x[4];  // token g: heads 2t, 2t+1; token g+8: heads 2t, 2t+1
+        float mx[2] = {kNegInf, kNegInf};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            x[i] = tok[i] < nv ? x[i] * scale_log2 : kNegInf;
-            mx = fmaxf(mx, x[i]);
+        for (int j = 0; j < 4; ++j) {
+            const int tok = g + 8 * (j >> 1);
+            x[j] = tok < nv ? (sa[j] + sb[j]) * scale_log2 : kNegInf;
+            mx[j & 1] = fmaxf(mx[j & 1], x[j]);
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mnew = fmaxf(m, mx);  // finite: nv >= 1
-        const float alpha = exp2f(m - mnew);
-        const uint32_t pa0 = pack_half2(exp2f(x[0] - mnew), exp2f(x[1] - mnew));
-        const uint32_t pa2 = pack_half2(exp2f(x[2] - mnew), exp2f(x[3] - mnew));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+        }
+        float alpha[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float mnew = fmaxf(m[h], mx[h]);  // finite: nv >= 1
+            alpha[h] = exp2f(m[h] - mnew);
+            m[h] = mnew;
+        }
+        // weights rows = tokens 0-7 / 8-15, columns = heads
+        const uint32_t p0 = pack_half2(exp2f(x[0] - m[0]), exp2f(x[1] - m[1]));
+        const uint32_t p1 = pack_half2(exp2f(x[2] - m[0]), exp2f(x[3] - m[1]));
         // the normaliser sums the same fp16-rounded weights the MMA applies
-        const float2 u0 = unpack_half2(pa0), u2 = unpack_half2(pa2);
-        l = l * alpha + ((u0.x + u0.y) + (u2.x + u2.y));
-        m = mnew;
+        const float2 u0 = unpack_half2(p0), u1 = unpack_half2(p1);
+        l[0] = l[0] * alpha[0] + (u0.x + u1.x);
+        l[1] = l[1] * alpha[1] + (u0.y + u1.y);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            o[nt][0] *= alpha;
-            o[nt][1] *= alpha;
+        for (int mt = 0; mt < MT; ++mt) {
+            o[mt][0] *= alpha[0];
+            o[mt][1] *= alpha[1];
+            o[mt][2] *= alpha[0];
+            o[mt][3] *= alpha[1];
         }
-        // O += P V: B fragments from the value tile, transposed; matrices
-        // 0/1: tokens 0-7 / 8-15, dims 0-7; 2/3: the same for dims 8-15
-        const int vt = ((lane >> 3) & 1) * 8 + (lane & 7);
-        const uint32_t vcol = head + (lane >> 4) * 16;
+        const uint32_t pb0 = movmatrix_trans(p0), pb1 = movmatrix_trans(p1);
+        // O^T += V^T P^T; transposed-ldmatrix matrices: tokens 0-7 at dims
+        // 0-7 (A row g) and 8-15 (row g+8), then tokens 8-15 at the same
+        const int vt = (lane >> 4) * 8 + (lane & 7);
+        const uint32_t vcol = head + ((lane >> 3) & 1) * 16;
 #pragma unroll
-        for (int nd = 0; nd < D / 16; ++nd) {
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_trans(v0, v1, v2, v3, vb + tile.at(vt, vcol + nd * 32));
-            mma_rows0_7(o[2 * nd][0], o[2 * nd][1], pa0, pa2, v0, v1);
-            mma_rows0_7(o[2 * nd + 1][0], o[2 * nd + 1][1], pa0, pa2, v2, v3);
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(a0, a1, a2, a3, vb + tile.at(vt, vcol + mt * 32));
+            mma_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
         }
     }
 
-    __device__ __forceinline__ float l_total() const {
-        float ls = l;
-        ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-        ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    // Softmax sum of head 2t + h over all tokens (every lane of one t).
+    __device__ __forceinline__ float l_total(int h) const {
+        float ls = l[h];
+        ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 16);
         return ls;
     }
 
-    // Shared-memory export for a CTA merge: m[g], l[g], o[g][D] for g < G.
+    // Shared-memory export for a CTA merge: m[h], l[h], o[h][D] for h < G.
     __device__ __forceinline__ void export_state(float *mw, float *lw, float *ow, int lane) {
-        const int g = lane >> 2, tig = lane & 3;
-        const float ls = l_total();
-        if (g < G) {
-            if (tig == 0) {
-                mw[g] = m;
-                lw[g] = ls;
+        const int g = lane >> 2, t = lane & 3;
+        const float l0 = l_total(0), l1 = l_total(1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int hd = 2 * t + h;
+            if (hd < G) {
+                if (g == 0) {
+                    mw[hd] = m[h];
+                    lw[hd] = h ? l1 : l0;
+                }
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    ow[hd * D + 16 * mt + g] = o[mt][h];
+                    ow[hd * D + 16 * mt + g + 8] = o[mt][2 + h];
+                }
             }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<float2 *>(ow + g * D + nt * 8 + tig * 2) =
-                    make_float2(o[nt][0], o[nt][1]);
         }
     }
 
-    // Final fp16 output o / l of heads g < G at out_g0 + g*D (zeros if empty).
+    // Final fp16 output o / l of heads h < G at out_g0 + h*D (zeros if empty).
     __device__ __forceinline__ void write_output(__half *out_g0, int lane) {
-        const int g = lane >> 2, tig = lane & 3;
-        const float ls = l_total();
-        if (g < G) {
-            const float inv = ls > 0.f ? 1.f / ls : 0.f;
+        const int g = lane >> 2, t = lane & 3;
+        const float l0 = l_total(0), l1 = l_total(1);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<__half2 *>(out_g0 + g * D + nt * 8 + tig * 2) =
-                    __floats2half2_rn(o[nt][0] * inv, o[nt][1] * inv);
+        for (int h = 0; h < 2; ++h) {
+            const int hd = 2 * t + h;
+            const float ls = h ? l1 : l0;
+            const float inv = ls > 0.f ? 1.f / ls : 0.f;
+            if (hd < G) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    out_g0[hd * D + 16 * mt + g] = __float2half_rn(o[mt][h] * inv);
+                    out_g0[hd * D + 16 * mt + g + 8] = __float2half_rn(o[mt][2 + h] * inv);
+                }
+            }
         }
     }
 
-    // Partial state to global memory: ml[g] = (m, l), o[g*D + d].
+    // Partial state to global memory: ml[h] = (m, l), o[h*D + d] for h < G.
     __device__ __forceinline__ void write_partial(float2 *ml, float *og, int lane) {
-        const int g = lane >> 2, tig = lane & 3;
-        const float ls = l_total();
-        if (g < G) {
-            if (tig == 0) ml[g] = make_float2(m, ls);
+        const int g = lane >> 2, t = lane & 3;
+        const float l0 = l_total(0), l1 = l_total(1);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<float2 *>(og + g * D + nt * 8 + tig * 2) =
-                    make_float2(o[nt][0], o[nt][1]);
+        for (int h = 0; h < 2; ++h) {
+            const int hd = 2 * t + h;
+            if (hd < G) {
+                if (g == 0) ml[hd] = make_float2(m[h], h ? l1 : l0);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    og[hd * D + 16 * mt + g] = o[mt][h];
+                    og[hd * D + 16 * mt + g + 8] = o[mt][2 + h];
+                }
+            }
         }
     }
 };
