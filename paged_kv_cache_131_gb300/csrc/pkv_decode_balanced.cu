@@ -84,45 +84,99 @@ __device__ __forceinline__ int cta_of(int64_t f, int64_t T, int64_t N) {
 }
 
 // Merge the partials of (seq, kvh) left by CTAs c_a..c_b and write fp16 out.
+// One warp.  The contributors' (m, l) are loaded together (lane j holds
+// contributor j of each 32-wide chunk) and reduced with shuffles; the
+// partial outputs are then accumulated U contributors at a time (32 floats
+// in flight per lane), so their loads overlap instead of forming a chain of
+// L2 round trips.
 template <int D, int G>
 __device__ void combine_partials(const BalancedParams &p, int seq, int kvh, int c_a, int c_b,
                                  int64_t f_s, int64_t T, int64_t N, int lane) {
     constexpr int DPL = D / 32;
+    constexpr int U = (32 / (G * DPL)) < 1 ? 1 : ((32 / (G * DPL)) > 4 ? 4 : 32 / (G * DPL));
     const int Hk = p.num_kv_heads;
-    float M[G], den[G], acc[G][DPL];
+    const int nc = c_b - c_a + 1;
+    // first (head-0) partial row of contributor c_a + j
+    auto row_of = [&](int j) -> int64_t {
+        const int c = c_a + j;
+        const int64_t fc = static_cast<int64_t>(c) * T / N;
+        const int64_t slot = 2 * static_cast<int64_t>(c) + ((j == 0 && fc < f_s) ? 1 : 0);
+        return (slot * Hk + kvh) * G;
+    };
+    // pass 1: the running maximum of every head over all contributors
+    float M[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) M[g] = kNegInf;
+    for (int j0 = 0; j0 < nc; j0 += 32) {
+        if (j0 + lane < nc) {
+            const int64_t r = row_of(j0 + lane);
+#pragma unroll
+            for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], __ldcg(p.part_ml + r + g).x);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
+    // pass 2: per chunk, each lane's contributor weight 2^(m - M) (0 for a
+    // contributor whose blocks were all skipped), the normaliser, and the
+    // weighted partial outputs
+    float den[G], acc[G][DPL];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        M[g] = kNegInf;
         den[g] = 0.f;
 #pragma unroll
         for (int i = 0; i < DPL; ++i) acc[g][i] = 0.f;
     }
-    for (int c = c_a; c <= c_b; ++c) {
-        const int64_t fc = static_cast<int64_t>(c) * T / N;
-        const int64_t slot = 2 * static_cast<int64_t>(c) + ((c == c_a && fc < f_s) ? 1 : 0);
-        const int64_t base = (slot * Hk + kvh) * G;
+    for (int j0 = 0; j0 < nc; j0 += 32) {
+        float w[G];
+        int64_t r = 0;
+        if (j0 + lane < nc) {
+            r = row_of(j0 + lane);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float2 ml = __ldcg(p.part_ml + base + g);
-            if (ml.x == kNegInf) continue;  // a contributor whose blocks were all skipped
-            const float mn = fmaxf(M[g], ml.x);
-            const float a = M[g] == kNegInf ? 0.f : exp2f(M[g] - mn);
-            const float b = exp2f(ml.x - mn);
-            den[g] = fmaf(den[g], a, ml.y * b);
-            const float *po = p.part_o + (base + g) * D + lane * DPL;
-            float o[DPL];
-            if constexpr (DPL == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
-                o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-            } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(po));
-                o[0] = v.x; o[1] = v.y;
+            for (int g = 0; g < G; ++g) {
+                const float2 ml = __ldcg(p.part_ml + r + g);
+                w[g] = ml.x == kNegInf ? 0.f : exp2f(ml.x - M[g]);
+                den[g] = fmaf(ml.y, w[g], den[g]);
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) w[g] = 0.f;
+        }
+        const int cnt = min(32, nc - j0);
+        for (int k0 = 0; k0 < cnt; k0 += U) {
+            float o[U][G][DPL];
+            float wk[U][G];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = min(k0 + u, cnt - 1);  // a repeated contributor gets weight 0
+                const int64_t rk = __shfl_sync(0xffffffffu, r, k);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float wg = __shfl_sync(0xffffffffu, w[g], k);
+                    wk[u][g] = k0 + u < cnt ? wg : 0.f;
+                    const float *po = p.part_o + (rk + g) * D + lane * DPL;
+                    if constexpr (DPL == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
+                        o[u][g][0] = v.x; o[u][g][1] = v.y; o[u][g][2] = v.z; o[u][g][3] = v.w;
+                    } else {
+                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(po));
+                        o[u][g][0] = v.x; o[u][g][1] = v.y;
+                    }
+                }
             }
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) acc[g][i] = fmaf(acc[g][i], a, o[i] * b);
-            M[g] = mn;
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int i = 0; i < DPL; ++i) acc[g][i] = fmaf(o[u][g][i], wk[u][g], acc[g][i]);
         }
     }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den[g] += __shfl_xor_sync(0xffffffffu, den[g], o);
     __half *out = p.out + (static_cast<int64_t>(seq) * p.num_heads + kvh * G) * D + lane * DPL;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
