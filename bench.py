@@ -52,7 +52,8 @@ WORKLOAD_NAMES = {
 }
 
 DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_131_gb300", "csrc", f)
-                  for f in ("pkv_decode_balanced.cu", "pkv_decode_common.cuh", "pkv_device.cuh")]
+                  for f in ("pkv_decode_balanced.cu", "pkv_decode_common.cuh", "pkv_device.cuh",
+                            "pkv_tensor_map.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_dram_traffic.txt")
 
 
@@ -345,8 +346,10 @@ def main():
         step = sum(e[0].elapsed_time(e[2]) for e in ev) / K
         if not split:
             return step, None, None
-        return (step, sum(e[0].elapsed_time(e[1]) for e in ev) / K,
-                sum(e[1].elapsed_time(e[2]) for e in ev) / K)
+        # per-kernel durations: medians, so a step where the host fell behind
+        # the GPU (launch latency landing between two events) does not skew them
+        return (step, float(np.median([e[0].elapsed_time(e[1]) for e in ev])),
+                float(np.median([e[1].elapsed_time(e[2]) for e in ev])))
 
     if dist is not None:
         dist.barrier()
@@ -405,8 +408,9 @@ def main():
         "wall_s_timed_loop": round(t_wall, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(f"config{args.config}") if args.kv == "fp16"
-                     else None,
+                     # recorded for the balanced schedule with the MMA policies only
+                     "traffic": recorded_traffic(f"config{args.config}.{args.kv}")
+                     if schedule != 1 and compute != 1 else None,
                      "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
                      "kernel": ("decode_grid_kernel" if schedule == 1 else
                                 "decode_balanced_kernel") +

@@ -2,6 +2,7 @@
 // of libpagedkv (the C ABI declared in include/pagedkv.h).
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/pagedkv.h"
 #include "pkv_device.cuh"
@@ -67,6 +68,47 @@ int sm_count() {
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];
+}
+
+namespace {
+struct KernelShape {
+    int device;
+    const void *fn;
+    int threads;
+    int smem;
+    int ctas_per_sm;
+};
+constexpr int kKernelCache = 128;
+KernelShape g_kernel_cache[kKernelCache];
+int g_kernel_cache_used = 0;
+std::mutex g_kernel_cache_mutex;
+}  // namespace
+
+int prepare_kernel(const void *fn, int threads, int smem, int *ctas_per_sm) {
+    const int dev = current_device();
+    if (dev < 0) return cuda_failure(cudaGetLastError(), "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_kernel_cache_mutex);
+    int opened = -1;  // the largest dynamic shared memory this kernel is opened to
+    for (int i = 0; i < g_kernel_cache_used; ++i) {
+        const KernelShape &k = g_kernel_cache[i];
+        if (k.device != dev || k.fn != fn) continue;
+        if (k.threads == threads && k.smem == smem) {
+            if (ctas_per_sm) *ctas_per_sm = k.ctas_per_sm;
+            return PKV_OK;
+        }
+        opened = opened > k.smem ? opened : k.smem;
+    }
+    cudaError_t e = cudaSuccess;
+    if (smem > opened)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute");
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+    if (e != cudaSuccess) return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (g_kernel_cache_used < kKernelCache)
+        g_kernel_cache[g_kernel_cache_used++] = KernelShape{dev, fn, threads, smem, per_sm};
+    if (ctas_per_sm) *ctas_per_sm = per_sm;
+    return PKV_OK;
 }
 
 }  // namespace pkv

@@ -298,8 +298,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
     if (warp == Hk) {
         // ================================ producer ================================
-        const uint8_t *kbytes = reinterpret_cast<const uint8_t *>(p.k_cache);
-        const uint8_t *vbytes = reinterpret_cast<const uint8_t *>(p.v_cache);
         // window of 32 blocks: lane j describes block base + j
         auto fetch = [&](int base, int &raw, int &seq, int &nv) {
             const int i = base + lane;
@@ -574,13 +572,10 @@ int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, 
                     bool fp8, cudaStream_t stream) {
     BalancedFn fn = select(D, G, simt, fp8);
     if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, shape.smem);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode balanced)");
     const int threads = (p.num_kv_heads + 1) * 32;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, shape.smem);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    const int st = prepare_kernel(reinterpret_cast<const void *>(fn), threads, shape.smem, &per_sm);
+    if (st != PKV_OK) return st;
     per_sm = std::max(1, std::min(per_sm, shape.ctas_per_sm));
     const int grid = std::min(shape.grid, per_sm * std::max(1, shape.grid / shape.ctas_per_sm));
     cudaLaunchConfig_t cfg = {};
@@ -593,7 +588,7 @@ int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_failure(e, "decode balanced launch");
 }

@@ -321,9 +321,8 @@ int launch_grid(const GridParams &p, int D, int G, bool simt, int num_seqs,
     GridFn fn = select(D, G, simt);
     if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
     const int smem = grid_smem_bytes(D, G, p.partition_blocks);
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return cuda_failure(e, "cudaFuncSetAttribute(decode grid)");
+    const int st = prepare_kernel(reinterpret_cast<const void *>(fn), kThreads, smem, nullptr);
+    if (st != PKV_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_kv_heads, num_seqs, p.num_partitions);
     cfg.blockDim = dim3(kThreads);
@@ -334,7 +333,7 @@ int launch_grid(const GridParams &p, int D, int G, bool simt, int num_seqs,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_failure(e, "decode grid launch");
 }

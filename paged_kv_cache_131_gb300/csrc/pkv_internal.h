@@ -21,6 +21,13 @@ void set_last_error(const char *msg);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Readies kernel `fn` for launches of `threads` threads with `smem` bytes of
+// dynamic shared memory on the current device and returns (in *ctas_per_sm,
+// if not null) how many such CTAs fit on an SM.  The attribute call and the
+// occupancy query run once per (device, kernel, shape); later calls hit a
+// small cache, so a launch costs the host little more than the launch itself.
+int prepare_kernel(const void *fn, int threads, int smem, int *ctas_per_sm);
+
 inline bool aligned(const void *p, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "../../include/pagedkv.h"
 #include "pkv_decode_host.h"
@@ -34,10 +35,55 @@ EncodeTiled encoder() {
     return fn;
 }
 
+// Recently encoded maps (a map only encodes an address and sizes, so a hit
+// is exact whatever happened to the memory in between).
+struct MapEntry {
+    int device;
+    const void *cache;
+    int64_t num_blocks;
+    int row_bytes;
+    int box_chunks;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 32;
+MapEntry g_maps[kMapCache];
+int g_maps_used = 0, g_maps_next = 0;
+std::mutex g_maps_mutex;
+
+int encode(CUtensorMap *map, const void *cache, int64_t num_blocks, int row_bytes,
+           int box_chunks);
+
 }  // namespace
 
 int make_kv_tensor_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int row_bytes,
                        int box_chunks) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_failure(cudaGetLastError(), "cudaGetDevice");
+    {
+        std::lock_guard<std::mutex> lock(g_maps_mutex);
+        for (int i = 0; i < g_maps_used; ++i) {
+            const MapEntry &e = g_maps[i];
+            if (e.device == dev && e.cache == cache && e.num_blocks == num_blocks &&
+                e.row_bytes == row_bytes && e.box_chunks == box_chunks) {
+                *map = e.map;
+                return PKV_OK;
+            }
+        }
+    }
+    const int st = encode(map, cache, num_blocks, row_bytes, box_chunks);
+    if (st != PKV_OK) return st;
+    std::lock_guard<std::mutex> lock(g_maps_mutex);
+    MapEntry &e = g_maps[g_maps_next];
+    e = MapEntry{dev, cache, num_blocks, row_bytes, box_chunks, *map};
+    g_maps_next = (g_maps_next + 1) % kMapCache;
+    if (g_maps_used < kMapCache) ++g_maps_used;
+    return PKV_OK;
+}
+
+namespace {
+
+int encode(CUtensorMap *map, const void *cache, int64_t num_blocks, int row_bytes,
+           int box_chunks) {
     const int C = chunk_bytes_for_row(row_bytes);
     const int64_t rows = num_blocks * 16;
     // (tile coordinates are signed 32-bit: every row index must fit)
@@ -70,5 +116,6 @@ int make_kv_tensor_map(CUtensorMap *map, const void *cache, int64_t num_blocks, 
     return PKV_OK;
 }
 
+}  // namespace
 }  // namespace dec
 }  // namespace pkv

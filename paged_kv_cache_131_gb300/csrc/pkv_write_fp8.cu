@@ -5,8 +5,9 @@
 // Each (token, KV head) row of head_dim fp16 values becomes head_dim E4M3
 // codes and one fp32 scale, all computed in fp32: amax = max |x|,
 // s = amax / 448 (448 is E4M3's largest finite value), code = RNE(x / s)
-// saturated to +-448; s == 0 gives zero codes.  One warp per token
-// (grid-stride); head_dim/32 values per lane; amax by a warp max-reduction.
+// saturated to +-448; s == 0 gives zero codes.  One warp per row (token,
+// cache, KV head), grid-stride, so the rows of a token quantize in parallel;
+// head_dim/32 values per lane; amax by a warp max-reduction.
 // For the token-major cache [num_blocks, block_size, Hk, D] a slot is also
 // the row index: row (slot, h) sits at (slot*Hk + h)*D.
 #include <cuda_fp16.h>
@@ -83,18 +84,21 @@ __global__ void __launch_bounds__(kThreads)
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int Hk = p.num_kv_heads;
-    for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         t < p.num_tokens; t += nwarps) {
+    const int64_t rows_per_token = static_cast<int64_t>(p.num_caches) * Hk;
+    const int64_t nrows = p.num_tokens * rows_per_token;
+    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         r < nrows; r += nwarps) {
+        const int64_t t = r / rows_per_token;
+        const int c = static_cast<int>((r - t * rows_per_token) / Hk);
+        const int h = static_cast<int>(r - t * rows_per_token - static_cast<int64_t>(c) * Hk);
         const int64_t slot = __ldg(p.slot_mapping + t);
         if (slot < 0) continue;  // padding
         if (slot >= p.num_slots) {
-            if (lane == 0) record_error(p.err, PKV_DEVERR_SLOT, t);
+            if (lane == 0 && c == 0 && h == 0) record_error(p.err, PKV_DEVERR_SLOT, t);
             continue;
         }
-        for (int c = 0; c < p.num_caches; ++c)
-            for (int h = 0; h < Hk; ++h)
-                quantize_row<D>(p.src[c] + (t * Hk + h) * D, p.cache[c] + (slot * Hk + h) * D,
-                                p.scale[c] + slot * Hk + h, lane);
+        quantize_row<D>(p.src[c] + (t * Hk + h) * D, p.cache[c] + (slot * Hk + h) * D,
+                        p.scale[c] + slot * Hk + h, lane);
     }
 }
 
@@ -113,7 +117,7 @@ extern "C" int pkv_cache_write_fp8(const void *k, const void *v, const int64_t *
     if ((v == nullptr) != (v_cache == nullptr) || (v == nullptr) != (v_scale == nullptr))
         return PKV_ERR_NULL;
     if (num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0 ||
-        num_blocks > INT64_MAX / block_size)
+        num_blocks > INT64_MAX / block_size || num_tokens > INT64_MAX / (2 * num_kv_heads))
         return PKV_ERR_INVALID;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     const uintptr_t need = head_dim == 128 ? 8 : 4;  // fp16 source vector
@@ -138,7 +142,8 @@ extern "C" int pkv_cache_write_fp8(const void *k, const void *v, const int64_t *
     p.num_kv_heads = num_kv_heads;
     p.err = device_error_record();
     if (p.err == nullptr) return PKV_ERR_CUDA;
-    const int64_t want = (num_tokens + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t rows = num_tokens * p.num_caches * num_kv_heads;
+    const int64_t want = (rows + kThreads / 32 - 1) / (kThreads / 32);
     const int grid = static_cast<int>(
         std::max<int64_t>(1, std::min<int64_t>(want, static_cast<int64_t>(sm_count()) * 16)));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
