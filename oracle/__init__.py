@@ -76,6 +76,8 @@ def _bind(lib):
     lib.oracle_copy_blocks.argtypes = [_p, _i64, _p] + [_i64] * 9
     lib.oracle_decode_attention.restype = ctypes.c_int
     lib.oracle_decode_attention.argtypes = [_p] * 6 + [ctypes.c_double] + [_i64] * 7 + [_p, _i64]
+    lib.oracle_chunk_attention.restype = ctypes.c_int
+    lib.oracle_chunk_attention.argtypes = [_p] * 7 + [ctypes.c_double] + [_i64] * 7 + [_p, _i64]
     return lib
 
 
@@ -227,4 +229,44 @@ def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, se
         _ptr(bt), _ptr(sl), float(scale), S, H, Hk, D, bs, bt.shape[1], NB, pp, npairs)
     if st != 0:
         raise ValueError(f"oracle_decode_attention_fp8 failed with status {st}")
+    return out
+
+
+# --------------------------------------------------------------------------
+# Chunk of new tokens per sequence (chunked prefill / draft verification)
+
+
+def chunk_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                    block_tables: np.ndarray, seq_lens: np.ndarray, query_start: np.ndarray,
+                    scale: float, *, rows=None, lib=None) -> np.ndarray:
+    """Causal attention of each sequence's last Q_i = query_start[i+1] -
+    query_start[i] tokens over its cache, in float64.
+
+    q: fp16 [Tq, H, D] (Tq = query_start[-1]); caches fp16 [NB, bs, Hk, D];
+    block_tables int32 [S, MB]; seq_lens int32 [S] (tokens in the cache,
+    the new ones included).  Returns float64 [Tq, H, D]; with ``rows`` only
+    those query rows are computed (the others are NaN).
+    """
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    assert k_cache.dtype == np.float16 and v_cache.dtype == np.float16
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    Tq, H, D = q.shape
+    NB, bs, Hk, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    S = sl.size
+    assert bt.shape[0] == S and qs.shape == (S + 1,) and int(qs[-1]) == Tq
+    out = np.full((Tq, H, D), np.nan, dtype=np.float64)
+    if rows is None:
+        rp, nr = None, 0
+    else:
+        ra = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        rp, nr = _ptr(ra), ra.size
+    st = (lib or _load()).oracle_chunk_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(sl), _ptr(qs),
+        float(scale), S, H, Hk, D, bs, bt.shape[1], NB, rp, nr)
+    if st != 0:
+        raise ValueError(f"oracle_chunk_attention failed with status {st}")
     return out

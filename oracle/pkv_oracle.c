@@ -465,3 +465,96 @@ int oracle_decode_attention_fp8(double *out, const uint16_t *q, const uint8_t *k
     }
     return status;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Attention of a chunk of new tokens per sequence ("vLLM 技术内幕" §3.2: V1
+ * schedules prompt and output tokens alike, {request: num_tokens} per step,
+ * a long prompt cut into chunks across steps beside running decodes; §7.4:
+ * draft tokens are scheduled with their request and verified together).
+ * Sequence i holds seq_lens[i] = L tokens in the cache after this step's
+ * write; the last Q = query_start[i+1] - query_start[i] of them are new.  New
+ * token j (0 <= j < Q) sits at position L - Q + j and attends to the cached
+ * positions 0 .. L - Q + j (itself and everything before it).  q and out are
+ * [query_start[S], H, D]; row r of q is new token r - query_start[i] of the
+ * sequence i with query_start[i] <= r < query_start[i+1].  With `rows`
+ * (a list of query rows) only those rows are computed; the others are left
+ * untouched. */
+int oracle_chunk_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, const int32_t *block_tables,
+                           const int32_t *seq_lens, const int32_t *query_start, double scale,
+                           int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
+                           int64_t head_dim, int64_t block_size, int64_t max_blocks_per_seq,
+                           int64_t num_blocks, const int64_t *rows, int64_t num_rows)
+{
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks_per_seq < 0 || num_seqs < 0 || query_start[0] != 0)
+        return ORC_ERR_ARG;
+    int64_t group = num_heads / num_kv_heads;
+    int status = ORC_OK;
+    for (int64_t i = 0; i < num_seqs && status == ORC_OK; ++i) {
+        int64_t len = seq_lens[i];
+        int64_t r0 = query_start[i], r1 = query_start[i + 1];
+        int64_t nq = r1 - r0;
+        if (len < 0 || len > max_blocks_per_seq * block_size || nq < 0 || nq > len)
+            return ORC_ERR_RANGE;
+        /* any wanted row in this sequence? */
+        int want_any = 0;
+        for (int64_t r = r0; r < r1 && !want_any; ++r) {
+            if (!rows) {
+                want_any = 1;
+            } else {
+                for (int64_t k = 0; k < num_rows; ++k)
+                    if (rows[k] == r)
+                        want_any = 1;
+            }
+        }
+        if (!want_any)
+            continue;
+        for (int64_t kvh = 0; kvh < num_kv_heads && status == ORC_OK; ++kvh) {
+            size_t n = (size_t)(len > 0 ? len : 1) * (size_t)head_dim;
+            double *K = (double *)malloc(n * sizeof(double));
+            double *V = (double *)malloc(n * sizeof(double));
+            double *scores = (double *)malloc((size_t)(len > 0 ? len : 1) * sizeof(double));
+            double *qd = (double *)malloc((size_t)head_dim * sizeof(double));
+            if (!K || !V || !scores || !qd) {
+                status = ORC_ERR_NOMEM;
+            } else {
+                for (int64_t j = 0; j < len && status == ORC_OK; ++j) {
+                    int64_t phys = block_tables[i * max_blocks_per_seq + j / block_size];
+                    if (phys < 0 || phys >= num_blocks) {
+                        status = ORC_ERR_RANGE;
+                        break;
+                    }
+                    for (int64_t d = 0; d < head_dim; ++d) {
+                        K[j * head_dim + d] = cache_at(k_cache, phys, j % block_size, kvh, d,
+                                                       block_size, num_kv_heads, head_dim);
+                        V[j * head_dim + d] = cache_at(v_cache, phys, j % block_size, kvh, d,
+                                                       block_size, num_kv_heads, head_dim);
+                    }
+                }
+                for (int64_t r = r0; r < r1 && status == ORC_OK; ++r) {
+                    int wanted = !rows;
+                    for (int64_t k = 0; rows && k < num_rows; ++k)
+                        if (rows[k] == r)
+                            wanted = 1;
+                    if (!wanted)
+                        continue;
+                    int64_t pos = len - nq + (r - r0); /* the new token's position */
+                    for (int64_t g = 0; g < group; ++g) {
+                        int64_t h = kvh * group + g;
+                        for (int64_t d = 0; d < head_dim; ++d)
+                            qd[d] = oracle_half_to_double(q[(r * num_heads + h) * head_dim + d]);
+                        /* causal: positions 0 .. pos */
+                        textbook_attention(out + (r * num_heads + h) * head_dim, qd, K, V,
+                                           pos + 1, head_dim, scale, scores);
+                    }
+                }
+            }
+            free(K);
+            free(V);
+            free(scores);
+            free(qd);
+        }
+    }
+    return status;
+}

@@ -333,6 +333,134 @@ def small_decode(index: int, seq_lens, *, H, Hk, D, bs=16, NB=None, write_last=T
 
 
 # --------------------------------------------------------------------------
+# Chunk workloads: several new tokens per sequence (chunked prefill, draft
+# verification).  The new tokens' rows are written (slot_mapping) before the
+# attention, as in config 1; sequence i's query rows are
+# query_start[i] .. query_start[i+1]-1, new token j at position L_i - Q_i + j.
+
+
+@dataclass
+class ChunkWorkload:
+    name: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    seq_lens: np.ndarray  # int32 [S], new tokens included
+    query_start: np.ndarray  # int32 [S+1]
+    block_tables: np.ndarray  # int32 [S, MB]
+    q: np.ndarray  # fp16 [Tq, H, D]
+    k_cache: np.ndarray  # fp16 [NB, bs, Hk, D] (state before the write)
+    v_cache: np.ndarray
+    k_new: np.ndarray  # fp16 [Tq, Hk*D] rows of the new tokens
+    v_new: np.ndarray
+    slot_mapping: np.ndarray  # int64 [Tq]
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def num_query_tokens(self) -> int:
+        return int(self.query_start[-1])
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max()) if self.seq_lens.size else 0
+
+    @property
+    def max_query_len(self) -> int:
+        return int(np.diff(self.query_start).max()) if self.seq_lens.size else 0
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    def kv_bytes(self) -> int:
+        """K+V bytes of every sequence's cache: sum_i L_i * Hk * D * 2 B * 2."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 4
+
+    def flops(self) -> int:
+        """2 * (QK + PV) multiply-adds of the causal attention: each new token at
+        position p attends p + 1 keys, for all H heads: sum 4 * (p+1) * D * H."""
+        total = 0
+        for i in range(self.num_seqs):
+            L = int(self.seq_lens[i])
+            nq = int(self.query_start[i + 1] - self.query_start[i])
+            # positions L-nq .. L-1 attend L-nq+1 .. L keys
+            total += (nq * (2 * L - nq + 1)) // 2
+        return 4 * total * self.head_dim * self.num_heads
+
+
+def chunk_workload(index: int, seq_lens, query_lens, *, H, Hk, D, bs=16, NB=None,
+                   order=None) -> ChunkWorkload:
+    """Sequences of total lengths ``seq_lens`` whose last ``query_lens`` tokens
+    are new this step (seeded by ``index``)."""
+    rng = rng_for(index)
+    S = len(seq_lens)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    query_lens = np.asarray(query_lens, dtype=np.int32)
+    assert query_lens.shape == seq_lens.shape and (query_lens <= seq_lens).all()
+    need = sum(blocks_needed(int(L), bs) for L in seq_lens) + 8
+    NB = NB or max(need, 4)
+    pool = BlockPool(NB, rng=None if order is not None else rng,
+                     order=order if order is not None else rng.permutation(NB))
+    seqs = [Sequence() for _ in range(S)]
+    for seq, L, nq in zip(seqs, seq_lens, query_lens):
+        prefill(pool, seq, int(L - nq), bs)
+        for _ in range(int(nq)):
+            append_slot(pool, seq, bs)
+    tables = pad_tables([s.block_table for s in seqs])
+    query_start = np.zeros(S + 1, dtype=np.int32)
+    query_start[1:] = np.cumsum(query_lens)
+    Tq = int(query_start[-1])
+    row = Hk * D
+    k_cache = np.full((NB, bs, Hk, D), FP16_NAN_BITS, dtype=np.uint16).view(np.float16)
+    v_cache = np.full((NB, bs, Hk, D), FP16_NAN_BITS, dtype=np.uint16).view(np.float16)
+    kr = k_cache.reshape(NB * bs, row)
+    vr = v_cache.reshape(NB * bs, row)
+    prior = np.asarray([slot_of(seq.block_table, p, bs) for seq, L, nq in
+                        zip(seqs, seq_lens, query_lens) for p in range(int(L - nq))],
+                       dtype=np.int64)
+    _fill_rows(rng, kr, prior, row)
+    _fill_rows(rng, vr, prior, row)
+    slot_mapping = np.asarray([slot_of(seq.block_table, p, bs) for seq, L, nq in
+                               zip(seqs, seq_lens, query_lens) for p in range(int(L - nq), int(L))],
+                              dtype=np.int64)
+    q = fp16_normal(rng, (Tq, H, D))
+    k_new = fp16_normal(rng, (Tq, row))
+    v_new = fp16_normal(rng, (Tq, row))
+    return ChunkWorkload(f"chunk{index}", H, Hk, D, bs, NB, 1.0 / math.sqrt(D), seq_lens,
+                         query_start, tables, q, k_cache, v_cache, k_new, v_new, slot_mapping)
+
+
+def config6_chunked_prefill(num_decodes: int = 63) -> ChunkWorkload:
+    """One engine step of "vLLM 技术内幕" §3.2's example under a 2048-token
+    budget: the second chunk of a 3000-token prompt (positions 2048..2999, 952
+    new tokens) beside ``num_decodes`` running decode requests (one new token
+    each, lengths U[256, 4096] as in config 2); H 32 / Hk 8, D 128, bs 16,
+    16384 shuffled blocks."""
+    rng = rng_for(6)
+    L_dec = rng.integers(256, 4097, size=num_decodes)
+    seq_lens = [3000] + [int(x) for x in L_dec]
+    query_lens = [952] + [1] * num_decodes
+    return chunk_workload(6, seq_lens, query_lens, H=32, Hk=8, D=128, bs=16, NB=16384,
+                          order=rng.permutation(16384))
+
+
+def config7_draft_verify(num_seqs: int = 64, num_query: int = 4) -> ChunkWorkload:
+    """Speculative-decode verification ("vLLM 技术内幕" §7.4): every sequence
+    checks ``num_query`` new tokens at once; lengths U[256, 4096] as in config
+    2, H 32 / Hk 8, D 128, bs 16, 16384 shuffled blocks."""
+    rng = rng_for(7)
+    seq_lens = [int(x) for x in rng.integers(256, 4097, size=num_seqs)]
+    return chunk_workload(7, seq_lens, [num_query] * num_seqs, H=32, Hk=8, D=128, bs=16,
+                          NB=16384, order=rng.permutation(16384))
+
+
+# --------------------------------------------------------------------------
 # Byte-strided two-cache write workload (config 5)
 
 
@@ -404,4 +532,4 @@ def config5_dsa_write(num_tokens: int = 16384, num_blocks: int = 4096) -> WriteW
 
 def config(index: int):
     return {1: config1_tiny, 2: config2_llama8b, 3: config3_long, 4: config4_shared_prefix,
-            5: config5_dsa_write}[index]()
+            5: config5_dsa_write, 6: config6_chunked_prefill, 7: config7_draft_verify}[index]()

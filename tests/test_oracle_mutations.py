@@ -11,6 +11,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_chunk as C
 import test_oracle_fp8 as F
 import test_oracle_pins as P
 from paged_kv_cache_131_gb300 import workloads as W
@@ -75,6 +76,16 @@ MUTATIONS = {
     "copy on write ignores the layer":
         ("int64_t a = offset + l * layer_stride + src * block_stride;",
          "int64_t a = offset + src * block_stride;"),
+    "chunk token attends one key too many":
+        ("pos + 1, head_dim, scale, scores);", "pos + 2 <= len ? pos + 2 : len, head_dim, scale, scores);"),
+    "chunk token attends one key too few":
+        ("pos + 1, head_dim, scale, scores);", "pos > 0 ? pos : 1, head_dim, scale, scores);"),
+    "chunk positions counted from the sequence start":
+        ("int64_t pos = len - nq + (r - r0);", "int64_t pos = r - r0;"),
+    "chunk attention not causal":
+        ("pos + 1, head_dim, scale, scores);", "len, head_dim, scale, scores);"),
+    "chunk query rows taken in reverse":
+        ("int64_t pos = len - nq + (r - r0);", "int64_t pos = len - 1 - (r - r0);"),
 }
 
 
@@ -96,6 +107,8 @@ def _pins(orc, lib):
     yield lambda: F.test_quantize_row_properties(orc, lib=lib)
     yield lambda: F.test_cache_write_fp8_rows_and_untouched(orc, lib=lib)
     yield lambda: F.test_decode_fp8_reduces_to_fp16_oracle(orc, lib=lib)
+    yield lambda: C.test_each_new_token_is_a_decode_of_its_prefix(orc, lib=lib)
+    yield lambda: C.test_chunk_matches_brute_force(orc, lib=lib)
     for case in (dict(index=102, lens=[3, 20, 40], H=4, Hk=2, D=8),
                  dict(index=103, lens=[0, 2, 31], H=8, Hk=1, D=4)):
         yield lambda case=case: P.test_decode_matches_brute_force(orc, case, lib=lib)
