@@ -292,6 +292,49 @@ int pkv_decode_attention_fp8(void *out, const void *q, const void *k_cache, cons
                              int32_t max_seq_len, int64_t num_blocks, void *workspace,
                              size_t workspace_bytes, pkv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Attention of a chunk of new tokens per sequence ("vLLM 技术内幕" §3.2: V1
+ * schedules prompt and output tokens alike -- {request: num_tokens} per step
+ * -- and cuts a long prompt into chunks that run beside the decodes; §7.4:
+ * draft tokens are scheduled with their request and verified together).
+ *
+ * Sequence i holds seq_lens[i] = L tokens in the cache, this step's new
+ * tokens included (write them first, e.g. with pkv_cache_write); its last
+ * Q = query_start[i+1] - query_start[i] tokens are the new ones.  New token
+ * j (0 <= j < Q) sits at position L - Q + j and attends causally to the
+ * cache positions 0 .. L - Q + j.  A chunk of one token is a decode.
+ *   out, q          fp16 [num_query_tokens, num_heads, head_dim]; query row r
+ *                   is new token r - query_start[i] of the sequence i with
+ *                   query_start[i] <= r < query_start[i+1]
+ *   k_cache, v_cache, block_tables, seq_lens, scale, num_heads,
+ *   num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks:
+ *                   as for pkv_decode_attention
+ *   query_start     int32 [num_seqs + 1], device: query_start[0] = 0,
+ *                   non-decreasing, query_start[num_seqs] = num_query_tokens
+ *   max_query_len   host bound on every Q (sizes the launch)
+ *   max_seq_len     host bound on every L (sizes the launch and workspace)
+ *   workspace       pkv_chunk_workspace_bytes(...) bytes, zeroed once
+ *                   (pkv_decode_workspace_init); every call leaves it zeroed
+ * Supported: head_dim 64 or 128, block_size 16, group size 1, 2, 4 or 8.
+ * Rows of a sequence whose Q exceeds max_query_len or L, or whose L exceeds
+ * its block table or max_seq_len, are skipped and recorded as
+ * PKV_DEVERR_SEQ_LEN; a bad block id is skipped and recorded.
+ * Returns PKV_ERR_WORKSPACE when the workspace is missing or too small. */
+int pkv_chunk_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens,
+                        const int32_t *query_start, float scale, int32_t num_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int32_t num_seqs, int32_t max_blocks_per_seq, int32_t num_query_tokens,
+                        int32_t max_query_len, int32_t max_seq_len, int64_t num_blocks,
+                        void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Workspace bytes pkv_chunk_attention needs for these bounds (0 for an
+ * invalid shape): tickets plus fp32 partial states of every query row for
+ * each 512-token KV partition. */
+size_t pkv_chunk_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t num_query_tokens,
+                                 int32_t max_query_len, int32_t max_seq_len);
+
 /* Bytes of the built-in scratch of pkv_decode_attention_noalloc (16 MiB). */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

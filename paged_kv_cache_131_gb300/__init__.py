@@ -17,7 +17,8 @@ __all__ = [
     "PkvError", "pkv_view", "pkv_write_desc", "pkv_decode_options", "library_path", "load",
     "pkv_cache_write", "pkv_decode_attention", "pkv_decode_workspace_bytes",
     "pkv_decode_workspace_init", "pkv_get_device_error", "pkv_status_string",
-    "pkv_last_error_string", "pkv_version", "EXPORTED_SYMBOLS",
+    "pkv_last_error_string", "pkv_version", "EXPORTED_SYMBOLS", "pkv_chunk_attention",
+    "pkv_chunk_workspace_bytes",
     "PKV_COMPUTE_AUTO", "PKV_COMPUTE_SIMT", "PKV_COMPUTE_MMA", "PKV_SCHEDULE_AUTO",
     "PKV_SCHEDULE_GRID", "PKV_SCHEDULE_BALANCED", "DEVICE_ERRORS",
 ]
@@ -34,7 +35,8 @@ EXPORTED_SYMBOLS = [
     "pkv_decode_workspace_bytes", "pkv_decode_workspace_bytes_ex", "pkv_decode_workspace_init",
     "pkv_get_device_error", "pkv_status_string", "pkv_last_error_string", "pkv_version",
     "pkv_decode_attention_noalloc", "pkv_cache_write_multi", "pkv_copy_blocks",
-    "pkv_cache_write_fp8", "pkv_decode_attention_fp8",
+    "pkv_cache_write_fp8", "pkv_decode_attention_fp8", "pkv_chunk_attention",
+    "pkv_chunk_workspace_bytes",
 ]
 
 
@@ -96,6 +98,12 @@ def load(path: str | None = None):
     lib.pkv_decode_attention_fp8.argtypes = dec[:4] + [_p, _p] + dec[4:] + [_p]
     lib.pkv_decode_attention_noalloc.restype = ctypes.c_int
     lib.pkv_decode_attention_noalloc.argtypes = dec[:15] + [_p]
+    lib.pkv_chunk_attention.restype = ctypes.c_int
+    lib.pkv_chunk_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, ctypes.c_float, _i32, _i32,
+                                        _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _p, _sz,
+                                        _p]
+    lib.pkv_chunk_workspace_bytes.restype = _sz
+    lib.pkv_chunk_workspace_bytes.argtypes = [_i32] * 7
     lib.pkv_decode_workspace_bytes.restype = _sz
     lib.pkv_decode_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32, _i32]
     lib.pkv_decode_workspace_bytes_ex.restype = _sz
@@ -239,6 +247,42 @@ def pkv_decode_attention(out, q, k_cache, v_cache, block_tables, seq_lens, scale
         opts = pkv_decode_options(partition_size, compute, schedule)
         st = lib.pkv_decode_attention_ex(*args, ctypes.byref(opts), _stream(stream))
     return _check(st, "pkv_decode_attention") if check else st
+
+
+def pkv_chunk_attention(out, q, k_cache, v_cache, block_tables, seq_lens, query_start,
+                        scale: float, num_heads: int, num_kv_heads: int, head_dim: int,
+                        block_size: int, max_query_len: int, max_seq_len: int, num_blocks: int,
+                        workspace=None, stream=None, check: bool = True) -> int:
+    """Causal attention of each sequence's new tokens: see pkv_chunk_attention in
+    pagedkv.h.
+
+    out, q: CUDA fp16 [Tq, H, D]; caches: CUDA fp16 [NB, bs, Hk, D];
+    block_tables: CUDA int32 [S, MB]; seq_lens: CUDA int32 [S];
+    query_start: CUDA int32 [S + 1]; workspace: CUDA uint8 tensor (zero-filled
+    before first use).
+    """
+    import torch
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    S = seq_lens.numel()
+    st = load().pkv_chunk_attention(
+        _dev(out, "out", torch.float16), _dev(q, "q", torch.float16),
+        _dev(k_cache, "k_cache", torch.float16), _dev(v_cache, "v_cache", torch.float16),
+        _dev(block_tables, "block_tables", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(query_start, "query_start", torch.int32), float(scale), num_heads, num_kv_heads,
+        head_dim, block_size, S, block_tables.shape[1] if block_tables.dim() == 2 else 0,
+        q.shape[0], int(max_query_len), int(max_seq_len), int(num_blocks), ws_ptr, ws_bytes,
+        _stream(stream))
+    return _check(st, "pkv_chunk_attention") if check else st
+
+
+def pkv_chunk_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                              num_query_tokens: int, max_query_len: int, max_seq_len: int) -> int:
+    return load().pkv_chunk_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim,
+                                            num_query_tokens, max_query_len, max_seq_len)
 
 
 def pkv_cache_write_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, block_size: int,

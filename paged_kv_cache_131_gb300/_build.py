@@ -19,7 +19,8 @@ LIB = os.path.join(PKG, "libpagedkv.so")
 HEADER = os.path.join(ROOT, "include", "pagedkv.h")
 
 SOURCES = ["pkv_api.cu", "pkv_write.cu", "pkv_write_fp8.cu", "pkv_blocks.cu", "pkv_decode_api.cu", "pkv_decode_grid.cu",
-           "pkv_decode_balanced.cu", "pkv_decode_noalloc.cu", "pkv_tensor_map.cu"]
+           "pkv_decode_balanced.cu", "pkv_decode_noalloc.cu", "pkv_tensor_map.cu",
+           "pkv_chunk.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

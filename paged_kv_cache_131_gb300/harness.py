@@ -11,9 +11,10 @@ import numpy as np
 import torch
 
 from . import (PKV_COMPUTE_AUTO, PKV_SCHEDULE_AUTO, pkv_cache_write, pkv_cache_write_fp8,
-               pkv_cache_write_multi, pkv_decode_attention, pkv_decode_attention_fp8,
-               pkv_decode_workspace_bytes, pkv_view)
-from .workloads import DecodeWorkload, WriteWorkload, slot_of
+               pkv_cache_write_multi, pkv_chunk_attention, pkv_chunk_workspace_bytes,
+               pkv_decode_attention, pkv_decode_attention_fp8, pkv_decode_workspace_bytes,
+               pkv_view)
+from .workloads import ChunkWorkload, DecodeWorkload, WriteWorkload, slot_of
 
 
 def to_dev(a: np.ndarray, device) -> torch.Tensor:
@@ -220,6 +221,52 @@ class DeviceWrite:
         t = self.wl.slot_mapping.size
         per = sum(v.row_width for v in self.wl.views[layout].values()) * self.wl.num_layers
         return 2 * t * per + 8 * t * len(self.wl.views[layout]) * self.wl.num_layers
+
+
+class DeviceChunk:
+    """A chunk workload on the device: each step writes the new tokens' rows
+    (pkv_cache_write), then runs the causal attention of every sequence's new
+    tokens (pkv_chunk_attention)."""
+
+    def __init__(self, wl: ChunkWorkload, device="cuda"):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.k_cache = to_dev(wl.k_cache, device)
+        self.v_cache = to_dev(wl.v_cache, device)
+        self.q = to_dev(wl.q, device)
+        self.block_tables = to_dev(wl.block_tables, device)
+        self.seq_lens = to_dev(wl.seq_lens, device)
+        self.query_start = to_dev(wl.query_start, device)
+        self.k_new = to_dev(wl.k_new, device)
+        self.v_new = to_dev(wl.v_new, device)
+        self.slot_mapping = to_dev(wl.slot_mapping, device)
+        self.out = torch.empty_like(self.q)
+        with torch.cuda.device(self.device):
+            nbytes = pkv_chunk_workspace_bytes(wl.num_seqs, wl.num_heads, wl.num_kv_heads,
+                                               wl.head_dim, wl.num_query_tokens,
+                                               max(wl.max_query_len, 1), max(wl.max_seq_len, 1))
+        self.workspace = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+    def view(self) -> pkv_view:
+        r = self.wl.num_kv_heads * self.wl.head_dim * 2
+        return pkv_view(0, 0, self.wl.block_size * r, r, 0)
+
+    def write(self, stream=None) -> None:
+        pkv_cache_write(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                        self.view(), self.wl.block_size, self.wl.num_blocks, stream=stream)
+
+    def attend(self, stream=None) -> torch.Tensor:
+        wl = self.wl
+        pkv_chunk_attention(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                            self.seq_lens, self.query_start, wl.scale, wl.num_heads,
+                            wl.num_kv_heads, wl.head_dim, wl.block_size, max(wl.max_query_len, 1),
+                            max(wl.max_seq_len, 1), wl.num_blocks, workspace=self.workspace,
+                            stream=stream)
+        return self.out
+
+    def step(self, stream=None) -> torch.Tensor:
+        self.write(stream)
+        return self.attend(stream)
 
 
 class L2Flush:

@@ -120,6 +120,51 @@ def test_decode_validation(lib):
     assert _decode(lib, H=64, Hk=16, ws=FAKE, wsb=1 << 30, opts=bal) == -3
 
 
+def _chunk(lib, out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, qs=FAKE, scale=0.1, H=32,
+           Hk=8, D=128, bs=16, S=4, MB=8, Tq=10, maxq=7, maxL=100, NB=64, ws=None, wsb=0):
+    return lib.pkv_chunk_attention(out, q, k, v, bt, sl, qs, scale, H, Hk, D, bs, S, MB, Tq,
+                                   maxq, maxL, NB, ws, wsb, None)
+
+
+def test_chunk_validation(lib):
+    # every case is refused (or a no-op) on the host, before any CUDA call
+    assert _chunk(lib, S=-1) == -2
+    assert _chunk(lib, Tq=-1) == -2
+    assert _chunk(lib, S=0) == 0 and _chunk(lib, Tq=0) == 0
+    for key in ("out", "q", "k", "v", "bt", "sl", "qs"):
+        assert _chunk(lib, **{key: None}) == -1, key
+    assert _chunk(lib, H=30) == -2
+    assert _chunk(lib, H=24, Hk=8) == -3
+    assert _chunk(lib, D=96) == -3
+    assert _chunk(lib, bs=32) == -3
+    assert _chunk(lib, maxq=0) == -2
+    assert _chunk(lib, maxL=0) == -2
+    assert _chunk(lib, MB=0) == -2
+    assert _chunk(lib, NB=0) == -2
+    assert _chunk(lib, scale=float("inf")) == -2
+    assert _chunk(lib, q=FAKE + 8) == -4
+    assert _chunk(lib, qs=FAKE + 2) == -4
+    assert _chunk(lib) == -5                      # no workspace
+    need = lib.pkv_chunk_workspace_bytes(4, 32, 8, 128, 10, 7, 100)
+    assert need > 0
+    assert _chunk(lib, ws=FAKE, wsb=need - 1) == -5
+
+
+def test_chunk_workspace_bytes(lib):
+    def a256(x):
+        return (x + 255) // 256 * 256
+
+    assert lib.pkv_chunk_workspace_bytes(4, 30, 8, 128, 10, 7, 100) == 0
+    assert lib.pkv_chunk_workspace_bytes(4, 32, 8, 128, 10, 0, 100) == 0
+    # tickets per (sequence, KV head, 64-row tile); one 512-token partition: no partials
+    S, H, Hk, D = 4, 32, 8, 128
+    assert lib.pkv_chunk_workspace_bytes(S, H, Hk, D, 10, 7, 512) == a256(S * Hk * 1 * 4)
+    # 952 new tokens x 4 heads per KV head = 60 tiles; 3000 tokens = 6 partitions
+    Tq, P, tiles = 1015, 6, 60
+    assert lib.pkv_chunk_workspace_bytes(64, H, Hk, D, Tq, 952, 3000) == \
+        a256(64 * Hk * tiles * 4) + a256(P * Tq * H * 8) + P * Tq * H * D * 4
+
+
 def test_workspace_bytes(lib):
     def a256(x):
         return (x + 255) // 256 * 256

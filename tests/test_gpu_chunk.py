@@ -1,0 +1,116 @@
+"""GPU parity of pkv_chunk_attention against the oracle (chunked prefill /
+draft verification: each sequence's new tokens attend causally to its cache).
+
+Every case writes the new tokens' rows with pkv_cache_write first, as a step
+does, then compares the attention element by element with the float64 oracle
+at the benchmark spec tolerance (|gpu - ref| <= 2e-3 + 1e-2 |ref|)."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import paged_kv_cache_131_gb300 as pkv  # noqa: E402
+from paged_kv_cache_131_gb300 import workloads as W  # noqa: E402
+from paged_kv_cache_131_gb300.harness import DeviceChunk  # noqa: E402
+from test_oracle_chunk import written_caches  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+ATOL, RTOL = 2e-3, 1e-2
+
+
+@pytest.fixture(scope="module")
+def pkv_lib():
+    from paged_kv_cache_131_gb300 import _build
+    _build.build()
+    assert torch.cuda.is_available()
+    pkv.pkv_get_device_error()
+    return pkv
+
+
+def assert_close(got, ref, what=""):
+    got = got.astype(np.float64)
+    bad = np.abs(got - ref) > ATOL + RTOL * np.abs(ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite outputs"
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} out of tolerance, max err "
+                           f"{np.abs(got - ref).max():.3e}")
+
+
+def run(wl, reps=1):
+    dev = DeviceChunk(wl)
+    out = None
+    for _ in range(reps):
+        dev.step()
+        out = dev.out.float().cpu().numpy()
+    kind, idx = pkv.pkv_get_device_error()
+    assert kind == 0, f"device error {pkv.DEVICE_ERRORS.get(kind)} at {idx}"
+    return dev, out
+
+
+def oracle(orc, wl, rows=None):
+    k, v = written_caches(wl)
+    return orc.chunk_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.query_start,
+                               wl.scale, rows=rows)
+
+
+SMALL = [
+    # (index, lens, query lens, H, Hk, D)
+    (301, [5, 16, 33, 40, 19], [5, 3, 1, 7, 16], 4, 2, 64),           # pure prefill, ragged
+    (302, [1, 17, 50, 2], [1, 1, 1, 1], 32, 8, 128),                  # one-token chunks
+    (303, [700, 1100, 40], [60, 300, 40], 32, 8, 128),                # tiles and partitions
+    (304, [1300, 613], [513, 97], 8, 8, 128),                         # G = 1, many tiles
+    (305, [530, 1040, 77], [17, 9, 77], 16, 2, 64),                   # G = 8
+    (306, [0, 12, 0, 600], [0, 4, 0, 2], 8, 4, 128),                  # empty sequences
+    (307, [2049, 513, 512], [1025, 2, 512], 8, 2, 128),               # partition edges
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[str(c[0]) for c in SMALL])
+def test_small_all_elements(pkv_lib, orc, case):
+    index, lens, qlens, H, Hk, D = case
+    wl = W.chunk_workload(index, lens, qlens, H=H, Hk=Hk, D=D)
+    _, got = run(wl)
+    assert_close(got, oracle(orc, wl), what=f"case {index}")
+
+
+def test_repeated_calls_are_identical(pkv_lib):
+    # tickets are left at zero: the second step merges exactly as the first
+    wl = W.chunk_workload(308, [1500, 900], [200, 33], H=32, Hk=8, D=128)
+    dev = DeviceChunk(wl)
+    dev.step()
+    a = dev.out.clone()
+    dev.step()
+    assert torch.equal(a, dev.out)
+
+
+def _sampled_rows(wl, rng, per_seq=3, seqs=12):
+    rows = set()
+    pick = rng.choice(wl.num_seqs, size=min(seqs, wl.num_seqs), replace=False)
+    for i in pick:
+        r0, r1 = int(wl.query_start[i]), int(wl.query_start[i + 1])
+        if r1 > r0:
+            rows.update([r0, r1 - 1])
+            rows.update(int(x) for x in rng.integers(r0, r1, size=per_seq))
+    return sorted(rows)
+
+
+def test_config6_chunked_prefill_sampled(pkv_lib, orc):
+    wl = W.config6_chunked_prefill()
+    _, got = run(wl)
+    rng = np.random.default_rng(16)
+    rows = _sampled_rows(wl, rng, seqs=8)
+    # and spread over the 952-token chunk (sequence 0)
+    rows = sorted(set(rows) | {0, 1, 63, 64, 511, 512, 951} |
+                  set(int(x) for x in rng.integers(0, 952, size=12)))
+    ref = oracle(orc, wl, rows=rows)
+    assert_close(got[rows], ref[rows], what="config 6")
+    assert np.isfinite(got).all()
+
+
+def test_config7_draft_verify_sampled(pkv_lib, orc):
+    wl = W.config7_draft_verify()
+    _, got = run(wl)
+    rows = _sampled_rows(wl, np.random.default_rng(17))
+    ref = oracle(orc, wl, rows=rows)
+    assert_close(got[rows], ref[rows], what="config 7")
+    assert np.isfinite(got).all()
