@@ -20,7 +20,13 @@ per launch / its event-timed duration against the measured HBM copy
 bandwidth.  `cpu_baseline` times the float64 oracle on the host.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config 2|3|4] [--compute auto|simt|mma]
+                  [--config 2|3|4|6|7] [--compute auto|simt|mma] [--kv fp16|fp8]
+
+Configs 6 and 7 time the multi-token step instead: the write of every new
+token's row, then the causal attention of each sequence's new tokens
+(pkv_chunk_attention) -- 6 is one engine step of chunked prefill (a
+952-token prompt chunk beside 63 decodes), 7 is 4-token draft verification
+on 64 sequences.
 """
 
 from __future__ import annotations
@@ -49,6 +55,11 @@ WORKLOAD_NAMES = {
     3: "long context: S=8, L=32768, bs=16, H=32, Hk=8, D=128, 16384 shuffled blocks, decode only",
     4: "shared prefix: S=256, 2000-token shared prefix + tail U[1,300], bs=16, H=64, Hk=8, "
        "D=128, 16384 blocks, 1 new token/seq written",
+    6: "chunked-prefill step: 952-token chunk of a 3000-token prompt (positions 2048..2999) + "
+       "63 decodes L~U[256,4096], bs=16, H=32, Hk=8, D=128, 16384 shuffled blocks, new rows "
+       "written first",
+    7: "draft verification: S=64, 4 new tokens each, L~U[256,4096], bs=16, H=32, Hk=8, D=128, "
+       "16384 shuffled blocks, new rows written first",
 }
 
 DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_131_gb300", "csrc", f)
@@ -63,7 +74,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 6, 7])
     ap.add_argument("--compute", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--schedule", choices=["auto", "grid", "balanced"], default="auto")
     ap.add_argument("--kv", choices=["fp16", "fp8"], default="fp16",
@@ -79,6 +90,14 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def measured_bf16_tflops() -> float:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f).get("bf16_tflops", 1900.0))
+    return 1900.0
 
 
 def measured_peaks():
@@ -242,8 +261,73 @@ class OracleSampler:
         return total_b / total_t / 1e9, total_t, n
 
 
+class ChunkOracleSampler:
+    """Times the float64 chunk oracle on rotating query rows (all heads of a
+    row); bytes = the key+value bytes each row's causal attention reads."""
+
+    def __init__(self, wl):
+        import oracle as orc
+
+        orc.build()
+        self.orc, self.wl = orc, wl
+        NB, bs, Hk, D = wl.k_cache.shape
+        self.k, self.v = wl.k_cache.copy(), wl.v_cache.copy()
+        self.k.reshape(NB * bs, Hk * D)[wl.slot_mapping] = wl.k_new
+        self.v.reshape(NB * bs, Hk * D)[wl.slot_mapping] = wl.v_new
+        qs, L = wl.query_start, wl.seq_lens
+        self.pos_of = {}
+        for i in range(wl.num_seqs):
+            for r in range(int(qs[i]), int(qs[i + 1])):
+                self.pos_of[r] = int(L[i]) - int(qs[i + 1] - qs[i]) + r - int(qs[i])
+        self.rows = sorted(self.pos_of)
+        self.cur = 0
+
+    def step(self, n_rows):
+        rows = [self.rows[(self.cur + j) % len(self.rows)] for j in range(n_rows)]
+        self.cur += n_rows
+        wl = self.wl
+        t0 = time.perf_counter()
+        self.orc.chunk_attention(wl.q, self.k, self.v, wl.block_tables, wl.seq_lens,
+                                 wl.query_start, wl.scale, rows=rows)
+        t = time.perf_counter() - t0
+        nbytes = sum(self.pos_of[r] + 1 for r in rows) * wl.num_kv_heads * wl.head_dim * 4
+        return nbytes, t
+
+    def calibrate(self) -> float:
+        nb, t = self.step(2)
+        return t / 2
+
+    def run(self, n_rows, steps=None, budget_s=None):
+        total_b, total_t, n = 0, 0.0, 0
+        while (steps is not None and n < steps) or (budget_s is not None and total_t < budget_s):
+            b, t = self.step(n_rows)
+            total_b, total_t, n = total_b + b, total_t + t, n + 1
+        return total_b / total_t / 1e9, total_t, n
+
+
 def run_reference(args, wl, rank):
     if rank != 0:
+        return
+    if args.config in (6, 7):
+        sampler = ChunkOracleSampler(wl)
+        t_row = sampler.calibrate()
+        n_rows = max(1, int(90.0 / max(1, args.steps + args.warmup) / t_row))
+        sampler.run(n_rows, steps=args.warmup)
+        gbs, t, n = sampler.run(n_rows, steps=args.steps)
+        sample = (f"{n_rows} query rows (all heads) per step, rotating over all "
+                  f"{len(sampler.rows)}; single-threaded float64")
+        line = {
+            "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
         return
     sampler = OracleSampler(wl)
     t_unit = sampler.calibrate()
@@ -270,6 +354,133 @@ def run_reference(args, wl, rank):
 # --------------------------------------------------------------------------- our arm
 
 
+def main_chunk(args, wl, rank, world, local):
+    """Multi-token step: write every new token's row, then the causal
+    attention of each sequence's new tokens."""
+    import torch
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import paged_kv_cache_131_gb300 as pkv
+    from paged_kv_cache_131_gb300 import _build
+    from paged_kv_cache_131_gb300.harness import DeviceChunk, L2Flush
+
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build()
+    if dist is not None:
+        dist.barrier()
+    dev = DeviceChunk(wl, device=f"cuda:{local}")
+    flush = L2Flush(f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    kv_bytes = wl.kv_bytes()
+    flops = wl.flops()
+    Tq, H, D = wl.q.shape
+    nblk = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
+    # algorithmic bytes of the attention: every sequence's K and V once, q in,
+    # out, block tables, lengths and query offsets
+    attn_bytes = kv_bytes + Tq * H * D * 2 * 2 + nblk * 4 + wl.num_seqs * 8 + 4
+    for _ in range(args.warmup):
+        flush()
+        dev.step()
+    torch.cuda.synchronize()
+    kind, idx = pkv.pkv_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error {pkv.DEVICE_ERRORS.get(kind)} at {idx}")
+    K = args.steps
+
+    def timed_loop(split: bool):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            dev.write()
+            if split:
+                ev[i][1].record(stream)
+            dev.attend()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        step = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+        if not split:
+            return step, None, None
+        return (step, float(np.median([e[0].elapsed_time(e[1]) for e in ev])),
+                float(np.median([e[1].elapsed_time(e[2]) for e in ev])))
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        step_ms, _, _ = timed_loop(split=False)
+        _, write_ms, attn_ms = timed_loop(split=True)
+    if dist is not None:
+        step_ms = max_over_ranks(step_ms, dist, f"cuda:{local}")
+        dist.barrier()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peak_hbm, peak_kind = measured_peaks()
+    peak_tf = measured_bf16_tflops()
+    value = whole_job_gbs(kv_bytes, world, step_ms)
+    gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
+    tfs = flops / (attn_ms * 1e-3) / 1e12
+    hbm_frac, tf_frac = gbs / peak_hbm, tfs / peak_tf
+    if hbm_frac >= tf_frac:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                "frac": round(hbm_frac, 4), "traffic": None,
+                "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)"}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tfs, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(tf_frac, 4), "traffic": None,
+                "peak_source": "measured bf16_tflops (cuBLAS, burst); fp16 mma.sync here"}
+    roof.update({"kernel": "chunk_attention_kernel", "alg_bytes_per_launch": attn_bytes,
+                 "flops_per_launch": flops, "achieved_gbs": round(gbs, 1),
+                 "achieved_tflops": round(tfs, 2), "hbm_frac": round(hbm_frac, 4),
+                 "tensor_frac": round(tf_frac, 4)})
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sampler = ChunkOracleSampler(wl)
+        t_row = sampler.calibrate()
+        n_rows = max(1, int(1.0 / t_row))
+        gbs_cpu, t_cpu, n_cpu = sampler.run(n_rows, budget_s=15.0)
+        cpu = {"value": round(gbs_cpu, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_cpu} x {n_rows} query rows (all heads), rotating, "
+                         f"{t_cpu:.1f} s single-threaded float64"}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16xf16->f32",
+        "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
+        "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": wl.num_seqs * world,
+                   "query_tokens": Tq, "seq_len": int(wl.max_seq_len),
+                   "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (write a 2x L2 buffer, then read another "
+                         "2x L2 buffer: cold, clean L2)",
+                   "kv_cache": "resident in HBM (state), not copied per step"},
+        "query_tokens_per_s": round(world * Tq / (step_ms * 1e-3), 1),
+        "attention_kernel_ms": round(attn_ms, 5),
+        "write_kernel_ms": round(write_ms, 5),
+        "roofline": roof,
+        "e2e": None,
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -278,6 +489,9 @@ def main():
     wl = W.config(args.config)
     if args.impl == "reference":
         run_reference(args, wl, rank)
+        return
+    if args.config in (6, 7):
+        main_chunk(args, wl, rank, world, local)
         return
 
     import torch

@@ -4,6 +4,10 @@
 // verified together).  Sequence i holds L tokens, the last Q of them new;
 // new token j (position L - Q + j) attends to positions 0 .. L - Q + j.
 //
+// Sequences whose new tokens times the group size fit the balanced decode
+// schedule's query columns (8 or 16: MmaColsPolicy) run there -- the same
+// streaming of whole token rows as a decode; the others run here.
+//
 // One CTA per (query tile of 64 rows, KV head, KV partition of 512 tokens,
 // sequence).  A row is (new token j, query head g of the KV head's group):
 // row = j*G + g, so a tile covers 64/G consecutive new tokens.  Four
@@ -63,6 +67,7 @@ struct ChunkParams {
     int max_seq_len;
     int num_tiles;  // grid.x
     int num_query_tokens;
+    int min_rows;   // sequences with fewer rows (new tokens x group) are not ours
     int64_t num_blocks;
     int *counters;    // [S][Hk][num_tiles] tickets, zero between calls
     float2 *part_ml;  // [parts][Tq][H] (m, l)
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;
     }
     const int rows = Q * G;
-    if (tile * kRows >= rows) return;  // no rows in this tile
+    if (rows < p.min_rows || tile * kRows >= rows) return;  // not ours, or no rows here
     const int j_last = (min(rows, (tile + 1) * kRows) - 1) / G;
     const int kv_end = L - Q + j_last + 1;  // keys [0, kv_end) for this tile
     const int nparts = (kv_end + kPartTokens - 1) / kPartTokens;
@@ -436,6 +441,9 @@ ChunkFn select(int D, int G) {
 
 struct Sizes {
     int64_t tiles, parts, counters_bytes, ml_bytes, o_bytes;
+    int col_tiles;          // balanced schedule's column n-tiles (0: not used)
+    dec::BalancedShape bal;  // its shape (workspace first in the scratch)
+    int64_t bal_bytes;
 };
 
 Sizes sizes(int64_t S, int64_t H, int64_t Hk, int64_t D, int64_t Tq, int64_t max_q,
@@ -447,6 +455,12 @@ Sizes sizes(int64_t S, int64_t H, int64_t Hk, int64_t D, int64_t Tq, int64_t max
     z.counters_bytes = dec::align256(S * Hk * z.tiles * 4);
     z.ml_bytes = z.parts > 1 ? dec::align256(z.parts * Tq * H * 8) : 0;
     z.o_bytes = z.parts > 1 ? z.parts * Tq * H * D * 4 : 0;
+    // the balanced schedule takes the chunks of up to 8 (or 16) query rows
+    z.col_tiles = max_q * G <= 8 ? 1 : 2;
+    z.bal = dec::balanced_shape(static_cast<int>(S), static_cast<int>(Hk), static_cast<int>(G),
+                                static_cast<int>(D), sm_count(), false, 8 * z.col_tiles);
+    if (!z.bal.ok) z.col_tiles = 0;
+    z.bal_bytes = z.bal.ok ? dec::align256(z.bal.workspace) : 0;
     return z;
 }
 
@@ -464,7 +478,7 @@ extern "C" size_t pkv_chunk_workspace_bytes(int32_t num_seqs, int32_t num_heads,
         return 0;
     const auto z = pkv::chunk::sizes(num_seqs, num_heads, num_kv_heads, head_dim,
                                      num_query_tokens, max_query_len, max_seq_len);
-    return static_cast<size_t>(z.counters_bytes + z.ml_bytes + z.o_bytes);
+    return static_cast<size_t>(z.bal_bytes + z.counters_bytes + z.ml_bytes + z.o_bytes);
 }
 
 extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache,
@@ -498,19 +512,63 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     const auto z = sizes(num_seqs, num_heads, num_kv_heads, head_dim, num_query_tokens,
                          max_query_len, max_seq_len);
     if (z.tiles > INT32_MAX || num_kv_heads * z.parts > 65535) return PKV_ERR_UNSUPPORTED;
-    const int64_t need = z.counters_bytes + z.ml_bytes + z.o_bytes;
+    const int64_t need = z.bal_bytes + z.counters_bytes + z.ml_bytes + z.o_bytes;
     if (workspace == nullptr || static_cast<int64_t>(workspace_bytes) < need)
         return PKV_ERR_WORKSPACE;
     ChunkFn fn = select(head_dim, G);
     if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    const int row_bytes = num_kv_heads * head_dim * 2;
 
+    // ---- chunks of up to 8 * col_tiles query rows: the balanced schedule
+    int min_rows = 1;
+    // (the balanced schedule indexes the flattened block list in 32 bits)
+    if (z.col_tiles > 0 && static_cast<int64_t>(num_seqs) * max_blocks_per_seq <= INT32_MAX) {
+        dec::BalancedParams b{};
+        b.out = static_cast<__half *>(out);
+        b.q = static_cast<const __half *>(q);
+        b.k_cache = static_cast<const __half *>(k_cache);
+        b.v_cache = static_cast<const __half *>(v_cache);
+        b.block_tables = block_tables;
+        b.seq_lens = seq_lens;
+        b.scale_log2 = scale_log2;
+        b.num_seqs = num_seqs;
+        b.num_heads = num_heads;
+        b.num_kv_heads = num_kv_heads;
+        b.max_blocks_per_seq = max_blocks_per_seq;
+        b.num_stages = z.bal.stages;
+        b.row_bytes = z.bal.row_bytes;
+        b.num_blocks = num_blocks;
+        b.query_start = query_start;
+        b.max_cols = 8 * z.col_tiles;
+        b.num_query_tokens = num_query_tokens;
+        const int64_t c_bytes = dec::align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
+        const int64_t slots = 2 * static_cast<int64_t>(z.bal.grid) * num_kv_heads * b.max_cols;
+        b.counters = reinterpret_cast<int *>(ws);
+        b.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
+        b.part_o = reinterpret_cast<float *>(ws + c_bytes + dec::align256(slots * 8));
+        const int box = row_bytes / dec::chunk_bytes_for_row(row_bytes);
+        int st = dec::make_kv_tensor_map(&b.tm_k, k_cache, num_blocks, row_bytes, box);
+        if (st == PKV_OK) st = dec::make_kv_tensor_map(&b.tm_v, v_cache, num_blocks, row_bytes, box);
+        if (st != PKV_OK) return st;
+        b.err = device_error_record();
+        if (b.err == nullptr) return PKV_ERR_CUDA;
+        st = dec::launch_balanced(b, z.bal, head_dim, G, false, false, s, z.col_tiles);
+        if (st != PKV_OK) return st;
+        min_rows = b.max_cols + 1;
+        if (static_cast<int64_t>(max_query_len) * G < min_rows) return PKV_OK;  // all done
+    }
+
+    // ---- the larger chunks: query tiles of 64 rows
     ChunkParams p{};
     p.out = static_cast<__half *>(out);
     p.q = static_cast<const __half *>(q);
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.query_start = query_start;
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.scale_log2 = scale_log2;
     p.num_heads = num_heads;
     p.num_kv_heads = num_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
@@ -518,14 +576,14 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     p.max_seq_len = max_seq_len;
     p.num_tiles = static_cast<int>(z.tiles);
     p.num_query_tokens = num_query_tokens;
+    p.min_rows = min_rows;
     p.num_blocks = num_blocks;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    p.counters = reinterpret_cast<int *>(ws);
-    p.part_ml = reinterpret_cast<float2 *>(ws + z.counters_bytes);
-    p.part_o = reinterpret_cast<float *>(ws + z.counters_bytes + z.ml_bytes);
+    uint8_t *cws = ws + z.bal_bytes;
+    p.counters = reinterpret_cast<int *>(cws);
+    p.part_ml = reinterpret_cast<float2 *>(cws + z.counters_bytes);
+    p.part_o = reinterpret_cast<float *>(cws + z.counters_bytes + z.ml_bytes);
     {
         // per-head boxes: kv_head's head_dim*2 bytes are whole 128-byte chunks
-        const int row_bytes = num_kv_heads * head_dim * 2;
         const int box = head_dim * 2 / dec::chunk_bytes_for_row(row_bytes);
         int st = dec::make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, row_bytes, box);
         if (st == PKV_OK) st = dec::make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, row_bytes, box);
@@ -543,7 +601,7 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
                        static_cast<unsigned>(num_seqs));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
-    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

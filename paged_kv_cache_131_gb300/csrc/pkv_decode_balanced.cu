@@ -89,102 +89,114 @@ __device__ __forceinline__ int cta_of(int64_t f, int64_t T, int64_t N) {
 // partial outputs are then accumulated U contributors at a time (32 floats
 // in flight per lane), so their loads overlap instead of forming a chain of
 // L2 round trips.
-template <int D, int G>
-__device__ void combine_partials(const BalancedParams &p, int seq, int kvh, int c_a, int c_b,
-                                 int64_t f_s, int64_t T, int64_t N, int lane) {
+// R partial rows per (sequence, kv head); row r is query row
+// (row0 + r / Gq) * H + kvh * Gq + r % Gq, rows >= ncols unused.  Rows are
+// merged eight at a time (bounded registers).
+template <int D, int R>
+__device__ void combine_partials(const BalancedParams &p, int kvh, int c_a, int c_b,
+                                 int64_t f_s, int64_t T, int64_t N, int lane, int64_t row0,
+                                 int ncols, int Gq) {
+    constexpr int G = R < 8 ? R : 8;  // rows per pass
     constexpr int DPL = D / 32;
     constexpr int U = (32 / (G * DPL)) < 1 ? 1 : ((32 / (G * DPL)) > 4 ? 4 : 32 / (G * DPL));
     const int Hk = p.num_kv_heads;
     const int nc = c_b - c_a + 1;
-    // first (head-0) partial row of contributor c_a + j
+    // first partial row of contributor c_a + j
     auto row_of = [&](int j) -> int64_t {
         const int c = c_a + j;
         const int64_t fc = static_cast<int64_t>(c) * T / N;
         const int64_t slot = 2 * static_cast<int64_t>(c) + ((j == 0 && fc < f_s) ? 1 : 0);
-        return (slot * Hk + kvh) * G;
+        return (slot * Hk + kvh) * R;
     };
-    // pass 1: the running maximum of every head over all contributors
-    float M[G];
+    for (int r0 = 0; r0 < R && r0 < ncols; r0 += G) {
+        // pass 1: the running maximum of every row over all contributors
+        float M[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) M[g] = kNegInf;
-    for (int j0 = 0; j0 < nc; j0 += 32) {
-        if (j0 + lane < nc) {
-            const int64_t r = row_of(j0 + lane);
+        for (int g = 0; g < G; ++g) M[g] = kNegInf;
+        for (int j0 = 0; j0 < nc; j0 += 32) {
+            if (j0 + lane < nc) {
+                const int64_t r = row_of(j0 + lane) + r0;
 #pragma unroll
-            for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], __ldcg(p.part_ml + r + g).x);
-        }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
-    // pass 2: per chunk, each lane's contributor weight 2^(m - M) (0 for a
-    // contributor whose blocks were all skipped), the normaliser, and the
-    // weighted partial outputs
-    float den[G], acc[G][DPL];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        den[g] = 0.f;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[g][i] = 0.f;
-    }
-    for (int j0 = 0; j0 < nc; j0 += 32) {
-        float w[G];
-        int64_t r = 0;
-        if (j0 + lane < nc) {
-            r = row_of(j0 + lane);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float2 ml = __ldcg(p.part_ml + r + g);
-                w[g] = ml.x == kNegInf ? 0.f : exp2f(ml.x - M[g]);
-                den[g] = fmaf(ml.y, w[g], den[g]);
+                for (int g = 0; g < G; ++g) M[g] = fmaxf(M[g], __ldcg(p.part_ml + r + g).x);
             }
-        } else {
-#pragma unroll
-            for (int g = 0; g < G; ++g) w[g] = 0.f;
         }
-        const int cnt = min(32, nc - j0);
-        for (int k0 = 0; k0 < cnt; k0 += U) {
-            float o[U][G][DPL];
-            float wk[U][G];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = min(k0 + u, cnt - 1);  // a repeated contributor gets weight 0
-                const int64_t rk = __shfl_sync(0xffffffffu, r, k);
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                M[g] = fmaxf(M[g], __shfl_xor_sync(0xffffffffu, M[g], o));
+        // pass 2: per chunk, each lane's contributor weight 2^(m - M) (0 for
+        // a contributor whose blocks were all skipped or masked), the
+        // normaliser, and the weighted partial outputs
+        float den[G], acc[G][DPL];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            den[g] = 0.f;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[g][i] = 0.f;
+        }
+        for (int j0 = 0; j0 < nc; j0 += 32) {
+            float w[G];
+            int64_t r = 0;
+            if (j0 + lane < nc) {
+                r = row_of(j0 + lane) + r0;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float wg = __shfl_sync(0xffffffffu, w[g], k);
-                    wk[u][g] = k0 + u < cnt ? wg : 0.f;
-                    const float *po = p.part_o + (rk + g) * D + lane * DPL;
-                    if constexpr (DPL == 4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
-                        o[u][g][0] = v.x; o[u][g][1] = v.y; o[u][g][2] = v.z; o[u][g][3] = v.w;
-                    } else {
-                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(po));
-                        o[u][g][0] = v.x; o[u][g][1] = v.y;
+                    const float2 ml = __ldcg(p.part_ml + r + g);
+                    w[g] = ml.x == kNegInf ? 0.f : exp2f(ml.x - M[g]);
+                    den[g] = fmaf(ml.y, w[g], den[g]);
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g) w[g] = 0.f;
+            }
+            const int cnt = min(32, nc - j0);
+            for (int k0 = 0; k0 < cnt; k0 += U) {
+                float o[U][G][DPL];
+                float wk[U][G];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int k = min(k0 + u, cnt - 1);  // a repeated contributor gets weight 0
+                    const int64_t rk = __shfl_sync(0xffffffffu, r, k);
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float wg = __shfl_sync(0xffffffffu, w[g], k);
+                        wk[u][g] = k0 + u < cnt ? wg : 0.f;
+                        const float *po = p.part_o + (rk + g) * D + lane * DPL;
+                        if constexpr (DPL == 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(po));
+                            o[u][g][0] = v.x; o[u][g][1] = v.y; o[u][g][2] = v.z; o[u][g][3] = v.w;
+                        } else {
+                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(po));
+                            o[u][g][0] = v.x; o[u][g][1] = v.y;
+                        }
                     }
                 }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int i = 0; i < DPL; ++i)
+                            acc[g][i] = fmaf(o[u][g][i], wk[u][g], acc[g][i]);
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int i = 0; i < DPL; ++i) acc[g][i] = fmaf(o[u][g][i], wk[u][g], acc[g][i]);
         }
-    }
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den[g] += __shfl_xor_sync(0xffffffffu, den[g], o);
-    __half *out = p.out + (static_cast<int64_t>(seq) * p.num_heads + kvh * G) * D + lane * DPL;
+            for (int o = 16; o >= 1; o >>= 1) den[g] += __shfl_xor_sync(0xffffffffu, den[g], o);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float inv = den[g] > 0.f ? 1.f / den[g] : 0.f;
+        for (int g = 0; g < G; ++g) {
+            const int rr = r0 + g;
+            if (rr >= ncols) break;
+            const float inv = den[g] > 0.f ? 1.f / den[g] : 0.f;
+            __half *out =
+                p.out + ((row0 + rr / Gq) * p.num_heads + kvh * Gq + rr % Gq) * D + lane * DPL;
 #pragma unroll
-        for (int i = 0; i < DPL; i += 2)
-            *reinterpret_cast<__half2 *>(out + g * D + i) =
-                __floats2half2_rn(acc[g][i] * inv, acc[g][i + 1] * inv);
+            for (int i = 0; i < DPL; i += 2)
+                *reinterpret_cast<__half2 *>(out + i) =
+                    __floats2half2_rn(acc[g][i] * inv, acc[g][i + 1] * inv);
+        }
     }
 }
 
@@ -237,8 +249,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             if (blockIdx.x == 0) record_error(p.err, PKV_DEVERR_SEQ_LEN, s);
             L = L < 0 ? 0 : cap;
         }
+        if constexpr (Policy::kColumns) {
+            // -1: not this kernel's (no new token, or more columns than it holds)
+            const int nq = __ldg(p.query_start + s + 1) - __ldg(p.query_start + s);
+            if (nq > L || nq < 0) {
+                if (blockIdx.x == 0) record_error(p.err, PKV_DEVERR_SEQ_LEN, s);
+                L = -1;
+            } else if (nq == 0 || nq * G > p.max_cols) {
+                L = -1;
+            }
+        }
         lens[s] = L;
-        local += (L + kBS - 1) / kBS;
+        local += L > 0 ? (L + kBS - 1) / kBS : 0;
     }
     int incl = local;
 #pragma unroll
@@ -265,7 +287,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         int run = wsum[warp] + incl - local;
         for (int s = s_begin; s < s_end; ++s) {
             cum[s] = run;
-            run += (lens[s] + kBS - 1) / kBS;
+            run += lens[s] > 0 ? (lens[s] + kBS - 1) / kBS : 0;
         }
         if (threadIdx.x == 0) cum[S] = wsum[32];
     }
@@ -308,6 +330,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 const int64_t f = f0 + i;
                 seq = find_seq(cum, S, f);
                 const int blk = static_cast<int>(f - cum[seq]);
+                // (the block's index in its sequence is f - cum[seq])
                 nv = min(kBS, lens[seq] - blk * kBS);
                 // checked when its window becomes current, so the load's latency
                 // hides behind the 32 blocks before it
@@ -355,7 +378,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const bool copy = bid >= 0 && nv > 0;
             const uint32_t stage = ring_s + st * stage_bytes;
             if (lane == 0) {
-                meta[st] = make_int4(seq, nv, bid, 0);
+                // .w: the block's index in its sequence
+                meta[st] = make_int4(seq, nv, bid, static_cast<int>(f0 + i - cum[max(seq, 0)]));
                 mbar_arrive_expect_tx(full_s + st * 8,
                                       copy ? 2u * tile_bytes + (kFp8 ? 2u * scale_bytes : 0u)
                                            : 0u);
@@ -402,16 +426,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     grid_dependency_wait();  // outputs and partials are written below
 
+    QueryRows qr{p.q, p.out, 0, H, kvh, G, 0};  // the current sequence's query rows
     auto finish = [&](int seq) {
         const int64_t f_s = cum[seq], f_e = cum[seq + 1];
         const int64_t qrow = static_cast<int64_t>(seq) * H + kvh * G;
         if (f_s >= f0 && f_e <= f1) {
-            st.write_output(p.out + qrow * D, lane);
+            if constexpr (Policy::kColumns) st.write_output(qr, lane);
+            else st.write_output(p.out + qrow * D, lane);
             return;
         }
         const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (f_s <= f0 ? 0 : 1);
-        const int64_t base = (slot * Hk + kvh) * G;
-        st.write_partial(p.part_ml + base, p.part_o + base * D, lane);
+        const int64_t base = (slot * Hk + kvh) * Policy::kRows;
+        if constexpr (Policy::kColumns)
+            st.write_partial(p.part_ml + base, p.part_o + base * D, qr.ncols, lane);
+        else
+            st.write_partial(p.part_ml + base, p.part_o + base * D, lane);
         __threadfence();
         __syncwarp();
         const int c_a = cta_of(f_s, T, N), c_b = cta_of(f_e - 1, T, N);
@@ -427,7 +456,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             }
         }
         last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) combine_partials<D, G>(p, seq, kvh, c_a, c_b, f_s, T, N, lane);
+        if (last) {
+            if constexpr (Policy::kColumns)
+                combine_partials<D, Policy::kRows>(p, kvh, c_a, c_b, f_s, T, N, lane, qr.row0,
+                                                   qr.ncols, G);
+            else
+                combine_partials<D, G>(p, kvh, c_a, c_b, f_s, T, N, lane, seq, G, G);
+        }
     };
 
     // FP8 scales of this lane's tokens in a staged block
@@ -455,7 +490,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         if (mt.x != cur) {
             if (cur >= 0) finish(cur);
             cur = mt.x;
-            st.init(p.q + (static_cast<int64_t>(cur) * H + kvh * G) * D, p.scale_log2, lane);
+            if constexpr (Policy::kColumns) {
+                const int qs0 = __ldg(p.query_start + cur), qs1 = __ldg(p.query_start + cur + 1);
+                qr.row0 = qs0;
+                qr.ncols = (qs1 - qs0) * G;
+                qr.lim0 = lens[cur] - (qs1 - qs0);
+                st.init(qr, lane);
+            } else {
+                st.init(p.q + (static_cast<int64_t>(cur) * H + kvh * G) * D, p.scale_log2, lane);
+            }
         }
         int used = 1;
         int s2 = 0;
@@ -503,7 +546,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 const uint32_t head = kvh * D * 2;
                 if (Policy::kZeroTailRows && mt.y < kBS)
                     zero_tail_rows<D>(vb, tile, head, mt.y, lane);
-                st.block(kb, vb, tile, head, mt.y, p.scale_log2, lane, pbuf);
+                if constexpr (Policy::kColumns)
+                    st.block(kb, vb, tile, head, mt.y, mt.w * kBS, p.scale_log2, lane);
+                else
+                    st.block(kb, vb, tile, head, mt.y, p.scale_log2, lane, pbuf);
             }
         }
         __syncwarp();
@@ -523,15 +569,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 using BalancedFn = void (*)(const BalancedParams);
 
 template <int D, int G>
-BalancedFn pick(bool simt, bool fp8) {
+BalancedFn pick(bool simt, bool fp8, int col_tiles) {
+    if (col_tiles == 1) return decode_balanced_kernel<D, G, MmaColsPolicy<D, G, 1>, false>;
+    if (col_tiles == 2) return decode_balanced_kernel<D, G, MmaColsPolicy<D, G, 2>, false>;
     if (fp8) return decode_balanced_kernel<D, G, MmaFp8Policy<D, G>, true>;
     if (simt) return decode_balanced_kernel<D, G, SimtPolicy<D, G>, false>;
     return decode_balanced_kernel<D, G, MmaPolicy<D, G>, false>;
 }
 
-BalancedFn select(int D, int G, bool simt, bool fp8) {
+BalancedFn select(int D, int G, bool simt, bool fp8, int col_tiles) {
 #define PKV_CASE(d, g) \
-    if (D == d && G == g) return pick<d, g>(simt, fp8);
+    if (D == d && G == g) return pick<d, g>(simt, fp8, col_tiles);
     PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
     PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
 #undef PKV_CASE
@@ -541,7 +589,8 @@ BalancedFn select(int D, int G, bool simt, bool fp8) {
 }  // namespace
 
 BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms,
-                             bool fp8) {
+                             bool fp8, int rows) {
+    if (rows <= 0) rows = G;
     BalancedShape r{};
     r.ok = num_kv_heads >= 1 && num_kv_heads <= kMaxBalancedKvHeads && num_seqs >= 1 &&
            (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
@@ -562,15 +611,15 @@ BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int n
     const int threads = (num_kv_heads + 1) * 32;
     r.ctas_per_sm = std::max(1, std::min({(228 * 1024) / (r.smem + 1024), 2048 / threads, 32}));
     r.grid = std::max(1, num_sms) * r.ctas_per_sm;
-    const int64_t slots = 2 * static_cast<int64_t>(r.grid) * num_kv_heads * G;
+    const int64_t slots = 2 * static_cast<int64_t>(r.grid) * num_kv_heads * rows;
     r.workspace = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4) +
                   align256(slots * 8) + slots * D * 4;
     return r;
 }
 
 int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
-                    bool fp8, cudaStream_t stream) {
-    BalancedFn fn = select(D, G, simt, fp8);
+                    bool fp8, cudaStream_t stream, int col_tiles) {
+    BalancedFn fn = select(D, G, simt, fp8, col_tiles);
     if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
     const int threads = (p.num_kv_heads + 1) * 32;
     int per_sm = 0;

@@ -62,6 +62,8 @@ struct SwizzledTile {
 
 template <int D, int G>
 struct MmaPolicy {
+    static constexpr bool kColumns = false;  // columns = the G heads of one new token
+    static constexpr int kRows = G;          // partial-state rows per (sequence, kv head)
     static constexpr int KS = D / 16;  // k-steps of S^T (16 head dims each)
     static constexpr int MT = D / 16;  // m-tiles (16 head dims each) of O^T
     static constexpr bool kZeroTailRows = true;  // reads all 16 value rows
@@ -229,6 +231,205 @@ struct MmaPolicy {
 };
 
 // ---------------------------------------------------------------------------
+// MMA policy for several new tokens per sequence (chunked prefill, draft
+// verification: "vLLM 技术内幕" §3.2, §7.4) on the same transposed products
+// as MmaPolicy.  The 8*NT columns of S^T = K Q^T and O^T = V^T P^T are
+// (new token j, query head g of the group) pairs, column c = j*G + g, each
+// with its own causal limit: token j of a sequence with L tokens, the last Q
+// of them new, sees the keys 0 .. L - Q + j.  One new token (Q = 1) is a
+// decode with G columns.
+
+// The query rows one (sequence, kv head) contributes.
+struct QueryRows {
+    const __half *q;  // q [rows, H, D]
+    __half *out;      // out [rows, H, D]
+    int64_t row0;     // query row of the sequence's first new token
+    int H;            // query heads
+    int kvh;          // kv head
+    int ncols;        // valid columns: Q * G
+    int lim0;         // last key position token 0 sees: L - Q
+};
+
+template <int D, int G, int NT>
+struct MmaColsPolicy {
+    static constexpr bool kColumns = true;
+    static constexpr int kRows = 8 * NT;  // partial-state rows (columns) per (sequence, kv head)
+    static constexpr bool kZeroTailRows = true;
+    static constexpr int KS = D / 16;
+    static constexpr int MT = D / 16;
+    uint32_t qb[NT][KS][2];  // B operand of S^T: query dims of column 8c + l/4
+    // O^T, n-tile c, m-tile mt: c0 / c2 = dims 16mt + g / + g + 8 of column
+    // 8c + 2t, c1 / c3 the same of column 8c + 2t + 1
+    float o[NT][MT][4];
+    float m[NT][2], l[NT][2];  // softmax state of columns 8c + 2t + h
+    int lim[NT][2];            // last key position of those columns (-1: no column)
+
+    __device__ __forceinline__ void init(const QueryRows &qr, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int c = 0; c < NT; ++c) {
+            const int col = 8 * c + g;
+            const __half *qrow = nullptr;
+            if (col < qr.ncols)
+                qrow = qr.q + ((qr.row0 + col / G) * qr.H + qr.kvh * G + col % G) * D;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                if (qrow) {
+                    const uint32_t *r = reinterpret_cast<const uint32_t *>(qrow + kk * 16);
+                    qb[c][kk][0] = __ldg(r + t);
+                    qb[c][kk][1] = __ldg(r + 4 + t);
+                } else {
+                    qb[c][kk][0] = qb[c][kk][1] = 0u;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int cc = 8 * c + 2 * t + h;
+                lim[c][h] = cc < qr.ncols ? qr.lim0 + cc / G : -1;
+                m[c][h] = kNegInf;
+                l[c][h] = 0.f;
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+                o[c][mt][0] = o[c][mt][1] = o[c][mt][2] = o[c][mt][3] = 0.f;
+        }
+    }
+
+    // One staged block whose first key is at position kp: key tile at kb,
+    // value tile at vb, this head's bytes from `head`; nv valid tokens.
+    __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, SwizzledTile tile,
+                                          uint32_t head, int nv, int kp, float scale_log2,
+                                          int lane) {
+        const int g = lane >> 2;
+        const int rt = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const uint32_t kcol = head + (lane >> 4) * 16;
+        float sa[NT][4], sb[NT][4];
+#pragma unroll
+        for (int c = 0; c < NT; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sa[c][e] = sb[c][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; kk += 2) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(a0, a1, a2, a3, kb + tile.at(rt, kcol + kk * 32));
+#pragma unroll
+            for (int c = 0; c < NT; ++c) mma_16816(sa[c], a0, a1, a2, a3, qb[c][kk][0], qb[c][kk][1]);
+            if (kk + 1 < KS) {
+                ldsm_x4(a0, a1, a2, a3, kb + tile.at(rt, kcol + kk * 32 + 32));
+#pragma unroll
+                for (int c = 0; c < NT; ++c)
+                    mma_16816(sb[c], a0, a1, a2, a3, qb[c][kk + 1][0], qb[c][kk + 1][1]);
+            }
+        }
+        // element e: token g + 8*(e>>1), column 8c + 2t + (e&1)
+        float x[NT][4];
+        float mx[NT][2];
+#pragma unroll
+        for (int c = 0; c < NT; ++c) {
+            mx[c][0] = mx[c][1] = kNegInf;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = g + 8 * (e >> 1);
+                const bool vis = tok < nv && kp + tok <= lim[c][e & 1];
+                x[c][e] = vis ? (sa[c][e] + sb[c][e]) * scale_log2 : kNegInf;
+                mx[c][e & 1] = fmaxf(mx[c][e & 1], x[c][e]);
+            }
+        }
+        float alpha[NT][2], msafe[NT][2];
+#pragma unroll
+        for (int c = 0; c < NT; ++c)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v = mx[c][h];
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                const float mnew = fmaxf(m[c][h], v);
+                // a column with no visible key yet keeps m = -inf, l = 0, o = 0
+                msafe[c][h] = mnew == kNegInf ? 0.f : mnew;
+                alpha[c][h] = exp2f(m[c][h] - msafe[c][h]);
+                m[c][h] = mnew;
+            }
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int c = 0; c < NT; ++c) {
+            const uint32_t p0 = pack_half2(exp2f(x[c][0] - msafe[c][0]), exp2f(x[c][1] - msafe[c][1]));
+            const uint32_t p1 = pack_half2(exp2f(x[c][2] - msafe[c][0]), exp2f(x[c][3] - msafe[c][1]));
+            // the normaliser sums the same fp16-rounded weights the MMA applies
+            const float2 u0 = unpack_half2(p0), u1 = unpack_half2(p1);
+            l[c][0] = l[c][0] * alpha[c][0] + (u0.x + u1.x);
+            l[c][1] = l[c][1] * alpha[c][1] + (u0.y + u1.y);
+            pb[c][0] = movmatrix_trans(p0);
+            pb[c][1] = movmatrix_trans(p1);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                o[c][mt][0] *= alpha[c][0];
+                o[c][mt][1] *= alpha[c][1];
+                o[c][mt][2] *= alpha[c][0];
+                o[c][mt][3] *= alpha[c][1];
+            }
+        }
+        const int vt = (lane >> 4) * 8 + (lane & 7);
+        const uint32_t vcol = head + ((lane >> 3) & 1) * 16;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(a0, a1, a2, a3, vb + tile.at(vt, vcol + mt * 32));
+#pragma unroll
+            for (int c = 0; c < NT; ++c) mma_16816(o[c][mt], a0, a1, a2, a3, pb[c][0], pb[c][1]);
+        }
+    }
+
+    __device__ __forceinline__ float l_total(int c, int h) const {
+        float ls = l[c][h];
+        ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+        ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+        return ls;
+    }
+
+    // Final fp16 output o / l of every valid column.
+    __device__ __forceinline__ void write_output(const QueryRows &qr, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int c = 0; c < NT; ++c)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float ls = l_total(c, h);
+                const int col = 8 * c + 2 * t + h;
+                if (col >= qr.ncols) continue;
+                const float inv = ls > 0.f ? 1.f / ls : 0.f;
+                __half *dst = qr.out + ((qr.row0 + col / G) * qr.H + qr.kvh * G + col % G) * D;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    dst[16 * mt + g] = __float2half_rn(o[c][mt][h] * inv);
+                    dst[16 * mt + g + 8] = __float2half_rn(o[c][mt][2 + h] * inv);
+                }
+            }
+    }
+
+    // Partial state to global memory, one row per column: ml[col] = (m, l),
+    // o[col*D + d] (columns >= ncols are not written).
+    __device__ __forceinline__ void write_partial(float2 *ml, float *og, int ncols, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int c = 0; c < NT; ++c)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float ls = l_total(c, h);
+                const int col = 8 * c + 2 * t + h;
+                if (col >= ncols) continue;
+                if (g == 0) ml[col] = make_float2(m[c][h], ls);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    og[col * D + 16 * mt + g] = o[c][mt][h];
+                    og[col * D + 16 * mt + g + 8] = o[c][mt][2 + h];
+                }
+            }
+    }
+};
+
+// ---------------------------------------------------------------------------
 // MMA policy over FP8 (E4M3) staged tiles, fed to the fp16 MMA without a
 // shared-memory round trip.  Tokens are tiled 0-7 / 8-15 as in MmaPolicy.
 //
@@ -274,6 +475,8 @@ __device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t sel) {
 
 template <int D, int G>
 struct MmaFp8Policy {
+    static constexpr bool kColumns = false;
+    static constexpr int kRows = G;
     static constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
     static constexpr int MT = D / 16;  // m-tiles (16 head dims each) of O^T
     static constexpr int kLaneTokens = 2;  // tokens whose scales a lane needs per block
@@ -486,6 +689,8 @@ struct ReduceScatter<1, H> {
 
 template <int D, int G>
 struct SimtPolicy {
+    static constexpr bool kColumns = false;
+    static constexpr int kRows = G;
     static constexpr int DPL = D / 32;                        // dims per lane: 4 or 2
     static constexpr int TC = (32 / G) < kBS ? 32 / G : kBS;  // tokens per chunk
     static constexpr int NCH = kBS / TC;                      // chunks per block

@@ -85,6 +85,13 @@ struct BalancedParams {
     int row_bytes;   // staged row: all KV heads of one token, Hk*D*elem bytes
     const float *k_scale;  // FP8 caches: [NB, 16, Hk] per-row scales (else null)
     const float *v_scale;
+    // several new tokens per sequence (MmaColsPolicy): sequence i's query
+    // rows are query_start[i] .. query_start[i+1]-1; sequences whose
+    // (new tokens x group) exceeds max_cols are left to the chunk kernel.
+    // Null for decode (one new token per sequence, query row = sequence).
+    const int32_t *query_start;
+    int max_cols;
+    int num_query_tokens;
     int64_t num_blocks;
     int *counters;    // [S * Hk] tickets, zero between calls
     float2 *part_ml;  // [2 * grid][Hk][G]
@@ -102,11 +109,13 @@ struct BalancedShape {
     int64_t workspace;  // bytes of scratch it needs
 };
 
-// Shape of the balanced launch for fp16 or FP8 caches.
+// Shape of the balanced launch for fp16 or FP8 caches; rows = partial-state
+// rows per (sequence, kv head): G for decode, 8 * col_tiles for chunks.
 BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms,
-                             bool fp8);
+                             bool fp8, int rows = 0);
+// col_tiles: 0 for decode, else the column n-tiles (1 or 2) of MmaColsPolicy.
 int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
-                    bool fp8, cudaStream_t stream);
+                    bool fp8, cudaStream_t stream, int col_tiles = 0);
 
 inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
