@@ -8,16 +8,20 @@
 // schedule's query columns (8 or 16: MmaColsPolicy) run there -- the same
 // streaming of whole token rows as a decode; the others run here.
 //
-// One CTA per (query tile of 64 rows, KV head, KV partition of 512 tokens,
-// sequence).  A row is (new token j, query head g of the KV head's group):
-// row = j*G + g, so a tile covers 64/G consecutive new tokens.  Four
+// The work is a list of items (query tile of 64 rows, KV head, KV
+// partition of 2048 tokens, sequence), built on the device by a one-CTA plan
+// kernel for the sequences this kernel takes (partitions past a tile's
+// causal range are not items).  Persistent CTAs (two per SM) pull items in
+// list order from an atomic counter, so tiles with more keys and tiles with
+// fewer balance out.  A row is (new token j, query head g of the KV head's
+// group): row = j*G + g, so a tile covers 64/G consecutive new tokens.  Four
 // consumer warps own 16 rows each; a producer warp stages the partition's
 // blocks -- two per stage, each block one tensor copy (TMA) of the head's
-// 16 key rows and one of its 16 value rows -- into a 4-deep ring.  Per block
-// a warp computes S = Q K^T (m16n8k16: rows = query rows, columns = tokens),
-// masks the keys past each row's position, folds the block into each row's
-// online softmax (log2 domain) and accumulates O += P V, the weights taken
-// straight from the score fragments.  A tile whose causal range fits one
+// 16 key rows and one of its 16 value rows -- into a 4-deep ring.  Per stage
+// (32 keys) a warp computes S = Q K^T (m16n8k16: rows = query rows, columns
+// = tokens), masks the keys past each row's position, folds the 32 keys into
+// each row's online softmax (log2 domain) and accumulates O += P V, the
+// weights taken straight from the score fragments.  A tile whose causal range fits one
 // partition writes fp16 out; otherwise every partition leaves fp32 partial
 // states and the last CTA of the tile to take a ticket merges them with a
 // log-sum-exp rescale.  No CTA waits for another.
@@ -29,7 +33,7 @@
 #include <cmath>
 #include <cstdint>
 
-#include "../../include/pagedkv.h"
+#include "/root/repo/include/pagedkv.h"
 #include "pkv_decode_common.cuh"
 #include "pkv_decode_host.h"
 #include "pkv_device.cuh"
@@ -48,7 +52,7 @@ constexpr int kWarps = 4;                 // consumer warps, 16 rows each
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kStages = 4;
 constexpr int kBlocksPerStage = 2;
-constexpr int kPartTokens = 512;          // KV partition
+constexpr int kPartTokens = 2048;         // KV partition
 constexpr int kPartBlocks = kPartTokens / kBS;
 
 struct ChunkParams {
@@ -68,6 +72,14 @@ struct ChunkParams {
     int num_tiles;  // grid.x
     int num_query_tokens;
     int min_rows;   // sequences with fewer rows (new tokens x group) are not ours
+    int num_seqs;
+    // work list: the sequences taken here (big_seq[k]) and the exclusive
+    // prefix of their item counts (big_cum[k], big_cum[n_big] = total items);
+    // *work is the next item to hand out
+    int *big_seq;
+    int *big_cum;
+    int *n_big;
+    int *work;
     int64_t num_blocks;
     int *counters;    // [S][Hk][num_tiles] tickets, zero between calls
     float2 *part_ml;  // [parts][Tq][H] (m, l)
@@ -82,14 +94,127 @@ struct Geo {
     static constexpr int kRing = kStages * kStage;
 };
 
+constexpr int kMisc = 8;  // ints of CTA-wide scratch
+
 int smem_bytes(int D) {
     const int tile = kBS * D * 2;
     return dec::kTileAlign + kStages * 2 * kBlocksPerStage * tile + 2 * kStages * 8 +
-           kPartBlocks * 4 + 16;
+           kPartBlocks * 4 + kMisc * 4;
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Geometry of sequence s for this kernel; false if the sequence is not
+// ours (too few rows) or invalid (recorded when `report`).
+struct SeqGeo {
+    int L, Q, q0, rows, tiles, parts;
+};
+
+__device__ __forceinline__ bool seq_geo(const ChunkParams &p, int s, int G, bool report,
+                                        SeqGeo &sg) {
+    const int L = __ldg(p.seq_lens + s);
+    const int q0 = __ldg(p.query_start + s), q1 = __ldg(p.query_start + s + 1);
+    const int Q = q1 - q0;
+    if (L < 0 || L > p.max_blocks_per_seq * kBS || L > p.max_seq_len || Q < 0 || Q > L ||
+        Q > p.max_query_len || q0 < 0 || q1 > p.num_query_tokens) {
+        if (report) record_error(p.err, PKV_DEVERR_SEQ_LEN, s);
+        return false;
+    }
+    sg.L = L;
+    sg.Q = Q;
+    sg.q0 = q0;
+    sg.rows = Q * G;
+    if (sg.rows < p.min_rows || sg.rows == 0) return false;
+    sg.tiles = (sg.rows + kRows - 1) / kRows;
+    sg.parts = (L + kPartTokens - 1) / kPartTokens;
+    return true;
+}
+
+// First query tile that needs KV partition `part` (its last token reaches
+// the partition): tile t's last token j_last(t) = (min(rows, 64(t+1)) - 1)/G
+// sees keys up to L - Q + j_last(t).
+__device__ __forceinline__ int first_tile(const SeqGeo &sg, int part, int G) {
+    const int x = part * kPartTokens - (sg.L - sg.Q);  // j_last must reach x
+    if (x <= 0) return 0;
+    const int t = (x * G + 1 + kRows - 1) / kRows - 1;
+    return min(sg.tiles - 1, max(0, t));
+}
+
+__device__ __forceinline__ int seq_items(const SeqGeo &sg, int G, int Hk) {
+    int n = 0;
+    for (int pt = 0; pt < sg.parts; ++pt) n += sg.tiles - first_tile(sg, pt, G);
+    return n * Hk;
+}
+
+// One CTA: the list of the sequences this kernel takes and their item counts.
+__global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant__ ChunkParams p,
+                                                          int G) {
+    __shared__ int wsum[32];
+    __shared__ int run[2];  // sequences listed, items listed
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) run[0] = run[1] = 0;
+    __syncthreads();
+    for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
+        const int s = s0 + threadIdx.x;
+        SeqGeo sg;
+        const bool mine = s < p.num_seqs && seq_geo(p, s, G, true, sg);
+        const int cnt = mine ? seq_items(sg, G, p.num_kv_heads) : 0;
+        // two exclusive scans at once: (is listed, items) packed in one int2
+        int a = mine ? 1 : 0, c = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, a, o);
+            const int yc = __shfl_up_sync(0xffffffffu, c, o);
+            if (lane >= o) {
+                a += ya;
+                c += yc;
+            }
+        }
+        __shared__ int wa[32];
+        if (lane == 31) {
+            wa[warp] = a;
+            wsum[warp] = c;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int nw = blockDim.x >> 5;
+            int va = lane < nw ? wa[lane] : 0, vc = lane < nw ? wsum[lane] : 0;
+            int ia = va, ic = vc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int ya = __shfl_up_sync(0xffffffffu, ia, o);
+                const int yc = __shfl_up_sync(0xffffffffu, ic, o);
+                if (lane >= o) {
+                    ia += ya;
+                    ic += yc;
+                }
+            }
+            if (lane < nw) {
+                wa[lane] = ia - va;
+                wsum[lane] = ic - vc;
+            }
+        }
+        __syncthreads();
+        const int ea = run[0] + wa[warp] + a - (mine ? 1 : 0);
+        const int ec = run[1] + wsum[warp] + c - cnt;
+        if (mine) {
+            p.big_seq[ea] = s;
+            p.big_cum[ea] = ec;
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) {
+            run[0] = ea + (mine ? 1 : 0);
+            run[1] = ec + cnt;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        p.big_cum[run[0]] = run[1];
+        *p.n_big = run[0];
+        *p.work = 0;
+    }
 }
 
 template <int D, int G>
@@ -104,327 +229,398 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Gm::kRing);
     uint64_t *empty = full + kStages;
     int *bt_s = reinterpret_cast<int *>(empty + kStages);
+    // misc: [0] last-contributor flag, [1] failure flag, [2..7] current item
+    // (sequence, partition, kv head, tile, valid)
     int *misc = bt_s + kPartBlocks;
 
     const int Hk = p.num_kv_heads, H = p.num_heads;
-    const int tile = blockIdx.x, kvh = blockIdx.y % Hk, part = blockIdx.y / Hk,
-              seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // ---- the sequence's geometry (not written by the cache write: read
-    // before the dependency wait)
-    const int L = __ldg(p.seq_lens + seq);
-    const int q0 = __ldg(p.query_start + seq), q1 = __ldg(p.query_start + seq + 1);
-    const int Q = q1 - q0;
-    if (L < 0 || L > p.max_blocks_per_seq * kBS || L > p.max_seq_len || Q < 0 || Q > L ||
-        Q > p.max_query_len || q0 < 0 || q1 > p.num_query_tokens) {
-        if (threadIdx.x == 0 && tile == 0 && blockIdx.y == 0)
-            record_error(p.err, PKV_DEVERR_SEQ_LEN, seq);
-        return;
-    }
-    const int rows = Q * G;
-    if (rows < p.min_rows || tile * kRows >= rows) return;  // not ours, or no rows here
-    const int j_last = (min(rows, (tile + 1) * kRows) - 1) / G;
-    const int kv_end = L - Q + j_last + 1;  // keys [0, kv_end) for this tile
-    const int nparts = (kv_end + kPartTokens - 1) / kPartTokens;
-    if (part >= nparts) return;
-    const int k0 = part * kPartTokens;
-    const int k1 = min(kv_end, k0 + kPartTokens);
-    const int blo = k0 / kBS;
-    const int nblk = (k1 + kBS - 1) / kBS - blo;  // >= 1
-    const int nsteps = (nblk + kBlocksPerStage - 1) / kBlocksPerStage;
-
-    // ---- the partition's block ids, checked
-    for (int b = threadIdx.x; b < nblk; b += kThreads) {
-        int id = __ldg(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blo + b);
-        if (id < 0 || static_cast<int64_t>(id) >= p.num_blocks) {
-            if (tile == 0 && kvh == 0)
-                record_error(p.err, PKV_DEVERR_BLOCK_ID,
-                             static_cast<int64_t>(seq) * p.max_blocks_per_seq + blo + b);
-            id = -1;
-        }
-        bt_s[b] = id;
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), kWarps);
         }
         fence_mbarrier_init();
+        misc[1] = 0;
     }
+    // the work list, the caches and the outputs are all written by earlier
+    // kernels of the stream
+    grid_dependency_wait();
     __syncthreads();
-
+    const int n_big = __ldcg(p.n_big);
+    const int total = __ldcg(p.big_cum + n_big);
     const uint32_t ring_s = smem_u32(smem);
     const uint32_t full_s = smem_u32(full), empty_s = smem_u32(empty);
-    const int head_chunk = kvh * (D * 2 / 128);
+    const SwizzledTile tl{7u};
+    int gstep = 0;  // ring steps run by this CTA so far (stage and phase of the next)
 
-    if (warp == kWarps) {
-        // ================================ producer ================================
-        grid_dependency_wait();  // the caches may have just been written
-        int issued = 0;
-        bool ok = true;
-        for (int i = 0; i < nsteps; ++i) {
-            const int st = i % kStages;
-            if (i >= kStages) {
-                const bool free_ = mbar_wait_bounded(empty_s + st * 8, ((i / kStages) - 1) & 1);
-                if (!__all_sync(0xffffffffu, free_)) {
+    for (;;) {
+        if (threadIdx.x == 0) {
+            const int item = atomicAdd(p.work, 1);
+            int valid = item < total && !misc[1];
+            if (valid) {
+                // the listed sequence holding the item, then its (partition,
+                // kv head, tile): partition-major, then kv head, then tile
+                int lo = 0, hi = n_big - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (__ldcg(p.big_cum + mid) <= item) lo = mid;
+                    else hi = mid - 1;
+                }
+                const int s = __ldcg(p.big_seq + lo);
+                int local = item - __ldcg(p.big_cum + lo);
+                SeqGeo sg;
+                valid = seq_geo(p, s, G, false, sg);
+                int part = 0, kv = 0, tile = 0;
+                for (int pt = 0; valid && pt < sg.parts; ++pt) {
+                    const int t0 = first_tile(sg, pt, G);
+                    const int nt = sg.tiles - t0;
+                    if (local < nt * Hk) {
+                        part = pt;
+                        kv = local / nt;
+                        tile = t0 + local % nt;
+                        break;
+                    }
+                    local -= nt * Hk;
+                }
+                misc[2] = s;
+                misc[3] = part;
+                misc[4] = kv;
+                misc[5] = tile;
+            }
+            misc[6] = valid;
+        }
+        __syncthreads();
+        if (!misc[6]) break;
+        const int seq = misc[2], part = misc[3], kvh = misc[4], tile = misc[5];
+        SeqGeo sg;
+        seq_geo(p, seq, G, false, sg);
+        const int L = sg.L, Q = sg.Q, q0 = sg.q0, rows = sg.rows;
+        const int j_last = (min(rows, (tile + 1) * kRows) - 1) / G;
+        const int kv_end = L - Q + j_last + 1;  // keys [0, kv_end) for this tile
+        const int nparts = (kv_end + kPartTokens - 1) / kPartTokens;
+        const int k0 = part * kPartTokens;
+        const int k1 = min(kv_end, k0 + kPartTokens);
+        const int blo = k0 / kBS;
+        const int nblk = (k1 + kBS - 1) / kBS - blo;  // >= 1
+        const int nsteps = (nblk + kBlocksPerStage - 1) / kBlocksPerStage;
+        const int head_chunk = kvh * (D * 2 / 128);
+
+        // the partition's block ids, checked
+        for (int b = threadIdx.x; b < nblk; b += kThreads) {
+            int id = __ldg(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blo + b);
+            if (id < 0 || static_cast<int64_t>(id) >= p.num_blocks) {
+                record_error(p.err, PKV_DEVERR_BLOCK_ID,
+                             static_cast<int64_t>(seq) * p.max_blocks_per_seq + blo + b);
+                id = -1;
+            }
+            bt_s[b] = id;
+        }
+        __syncthreads();
+
+        if (warp == kWarps) {
+            // ============================== producer ==============================
+            for (int i = 0; i < nsteps; ++i) {
+                const int gi = gstep + i;
+                const int st = gi % kStages;
+                if (gi >= kStages) {
+                    const bool free_ =
+                        mbar_wait_bounded(empty_s + st * 8, ((gi / kStages) - 1) & 1);
+                    if (!__all_sync(0xffffffffu, free_)) {
+                        if (lane == 0) {
+                            record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+                            atomicOr(&misc[1], 1);
+                        }
+                        break;
+                    }
+                }
+                const int nb = min(kBlocksPerStage, nblk - i * kBlocksPerStage);
+                int ncopy = 0;
+                for (int k = 0; k < nb; ++k) ncopy += bt_s[i * kBlocksPerStage + k] >= 0 ? 1 : 0;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full_s + st * 8,
+                                          static_cast<uint32_t>(ncopy) * 2u * Gm::kTile);
+                __syncwarp();
+                // lanes 0, 1: key tiles of the stage's blocks; lanes 2, 3: value tiles
+                const int k = lane % kBlocksPerStage;
+                const bool value = lane >= kBlocksPerStage;
+                if (lane < 2 * kBlocksPerStage && k < nb) {
+                    const int id = bt_s[i * kBlocksPerStage + k];
+                    if (id >= 0)
+                        tensor_g2s_3d(ring_s + st * Gm::kStage +
+                                          (value ? kBlocksPerStage + k : k) * Gm::kTile,
+                                      value ? &p.tm_v : &p.tm_k, 0, id * kBS, head_chunk,
+                                      full_s + st * 8);
+                }
+            }
+        } else {
+            // ============================== consumers ==============================
+            const int g = lane >> 2, t = lane & 3;
+            int lim[2];
+            int64_t orow[2];  // (query row * H + head) of each of the lane's two rows, or -1
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int rr = tile * kRows + warp * 16 + g + 8 * r;
+                if (rr < rows) {
+                    const int j = rr / G;
+                    lim[r] = L - Q + j;  // last key position it sees
+                    orow[r] = static_cast<int64_t>(q0 + j) * H + kvh * G + rr % G;
+                } else {
+                    lim[r] = -1;
+                    orow[r] = -1;
+                }
+            }
+            int wlim = max(lim[0], lim[1]);  // the largest key position this warp sees
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                wlim = max(wlim, __shfl_xor_sync(0xffffffffu, wlim, o));
+            uint32_t qa[KS][4];
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (orow[r] >= 0) {
+                        const uint32_t *src =
+                            reinterpret_cast<const uint32_t *>(p.q + orow[r] * D + kk * 16);
+                        qa[kk][r] = __ldg(src + t);
+                        qa[kk][2 + r] = __ldg(src + 4 + t);
+                    } else {
+                        qa[kk][r] = qa[kk][2 + r] = 0u;
+                    }
+                }
+            }
+            float o[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+            float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+            const int ktok = (lane & 7) + (lane >> 4) * 8;
+            const uint32_t kcol = ((lane >> 3) & 1) * 16;
+            const int vtok = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const uint32_t vcol = (lane >> 4) * 16;
+
+            bool ok = true;
+            for (int i = 0; i < nsteps; ++i) {
+                const int gi = gstep + i;
+                const int st = gi % kStages;
+                const bool landed = mbar_wait_bounded(full_s + st * 8, (gi / kStages) & 1);
+                if (!__all_sync(0xffffffffu, landed)) {
                     ok = false;
                     break;
                 }
-            }
-            const int nb = min(kBlocksPerStage, nblk - i * kBlocksPerStage);
-            int ncopy = 0;
-            for (int k = 0; k < nb; ++k) ncopy += bt_s[i * kBlocksPerStage + k] >= 0 ? 1 : 0;
-            if (lane == 0)
-                mbar_arrive_expect_tx(full_s + st * 8, static_cast<uint32_t>(ncopy) * 2u * Gm::kTile);
-            __syncwarp();
-            // lanes 0..nb-1: key tiles, lanes kBlocksPerStage..+nb-1: value tiles
-            const int k = lane % kBlocksPerStage;
-            const bool value = lane >= kBlocksPerStage;
-            if (lane < 2 * kBlocksPerStage && k < nb) {
-                const int id = bt_s[i * kBlocksPerStage + k];
-                if (id >= 0)
-                    tensor_g2s_3d(ring_s + st * Gm::kStage + (value ? kBlocksPerStage + k : k) *
-                                                                 Gm::kTile,
-                                  value ? &p.tm_v : &p.tm_k, 0, id * kBS, head_chunk,
-                                  full_s + st * 8);
-            }
-            issued = i + 1;
-        }
-        if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
-        // every copy issued must land before the CTA may exit
-        for (int st = 0; st < kStages && st < issued; ++st) {
-            const int uses = (issued - 1 - st) / kStages + 1;
-            mbar_wait_bounded(full_s + st * 8, (uses - 1) & 1);
-        }
-        return;
-    }
-
-    // ================================ consumers ================================
-    const int g = lane >> 2, t = lane & 3;
-    // this lane's two rows (MMA rows g and g+8 of the warp's 16)
-    int row[2], lim[2];
-    int64_t orow[2];  // (query row * H + head) of each row, or -1
+                const int nb = min(kBlocksPerStage, nblk - i * kBlocksPerStage);
+                // the stage's blocks in one softmax step (2 x 16 keys): which
+                // of them this warp needs (warp-uniform), and where they start
+                bool use[kBlocksPerStage];
+                int kps[kBlocksPerStage];
+                bool any = false;
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int rr = tile * kRows + warp * 16 + g + 8 * r;
-        row[r] = rr;
-        if (rr < rows) {
-            const int j = rr / G;
-            lim[r] = L - Q + j;  // last key position it sees
-            orow[r] = static_cast<int64_t>(q0 + j) * H + kvh * G + rr % G;
-        } else {
-            lim[r] = -1;
-            orow[r] = -1;
-        }
-    }
-    // the largest key position any row of this warp sees
-    int wlim = max(lim[0], lim[1]);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) wlim = max(wlim, __shfl_xor_sync(0xffffffffu, wlim, o));
-
-    // query fragments (A operand): qa[kk] = {row g: dims 2t.., row g+8: 2t..,
-    // row g: 8+2t.., row g+8: 8+2t..} of k-step kk
-    uint32_t qa[KS][4];
-#pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            if (orow[r] >= 0) {
-                const uint32_t *src =
-                    reinterpret_cast<const uint32_t *>(p.q + orow[r] * D + kk * 16);
-                qa[kk][r] = __ldg(src + t);
-                qa[kk][2 + r] = __ldg(src + 4 + t);
-            } else {
-                qa[kk][r] = qa[kk][2 + r] = 0u;
-            }
-        }
-    }
-    float o[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
-
-    const SwizzledTile tl{7u};
-    const int ktok = (lane & 7) + (lane >> 4) * 8;       // key ldmatrix: matrix row token
-    const uint32_t kcol = ((lane >> 3) & 1) * 16;
-    const int vtok = (lane & 7) + ((lane >> 3) & 1) * 8;  // value ldmatrix (transposed)
-    const uint32_t vcol = (lane >> 4) * 16;
-
-    grid_dependency_wait();  // outputs and partials are written below
-    bool ok = true;
-    for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages;
-        const bool landed = mbar_wait_bounded(full_s + st * 8, (i / kStages) & 1);
-        if (!__all_sync(0xffffffffu, landed)) {
-            ok = false;
-            break;
-        }
-        const int nb = min(kBlocksPerStage, nblk - i * kBlocksPerStage);
-        for (int k = 0; k < nb; ++k) {
-            const int kp = (blo + i * kBlocksPerStage + k) * kBS;  // first key position
-            if (bt_s[i * kBlocksPerStage + k] < 0 || kp > wlim) continue;  // warp-uniform
-            const uint32_t kb = ring_s + st * Gm::kStage + k * Gm::kTile;
-            const uint32_t vb = ring_s + st * Gm::kStage + (kBlocksPerStage + k) * Gm::kTile;
-            // value rows past the sequence end hold anything (their weights
-            // are 0, but 0 * NaN is not): every warp zeroes them before use
-            // (the same zeros, so the warps' writes agree)
-            if (kp + kBS > L) dec::zero_tail_rows<D>(vb, tl, 0u, L - kp, lane);
-            // S = Q K^T: n-tile 0 = tokens 0-7, n-tile 1 = tokens 8-15
-            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(b0, b1, b2, b3, kb + tl.at(ktok, kcol + kk * 32));
-                mma_16816(s0, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                mma_16816(s1, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-            }
-            // element e of n-tile n: row g (e < 2) or g+8, token 8n + 2t + (e & 1)
-            float x[2][4];
-            float mx[2] = {kNegInf, kNegInf};
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = e >> 1;
-                    const int pos = kp + 8 * n + 2 * t + (e & 1);
-                    const float s = n ? s1[e] : s0[e];
-                    x[n][e] = pos <= lim[r] ? s * p.scale_log2 : kNegInf;
-                    mx[r] = fmaxf(mx[r], x[n][e]);
+                for (int k = 0; k < kBlocksPerStage; ++k) {
+                    kps[k] = (blo + i * kBlocksPerStage + k) * kBS;
+                    use[k] = k < nb && bt_s[i * kBlocksPerStage + k] >= 0 && kps[k] <= wlim;
+                    any = any || use[k];
                 }
-            float alpha[2], msafe[2];
+                if (any) {
+                    const uint32_t stage = ring_s + st * Gm::kStage;
+                    // S = Q K^T for both blocks: n-tiles (block k, tokens 0-7 / 8-15)
+                    float sc[kBlocksPerStage][2][4];
+#pragma unroll
+                    for (int k = 0; k < kBlocksPerStage; ++k)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) sc[k][n][e] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < kBlocksPerStage; ++k) {
+                        if (!use[k]) continue;
+                        const uint32_t kb = stage + k * Gm::kTile;
+#pragma unroll
+                        for (int kk = 0; kk < KS; ++kk) {
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(b0, b1, b2, b3, kb + tl.at(ktok, kcol + kk * 32));
+                            mma_16816(sc[k][0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                            mma_16816(sc[k][1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                        }
+                    }
+                    // element e of n-tile n of block k: row g (e < 2) or g+8,
+                    // key position kps[k] + 8n + 2t + (e & 1)
+                    float mx[2] = {kNegInf, kNegInf};
+#pragma unroll
+                    for (int k = 0; k < kBlocksPerStage; ++k)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int r = e >> 1;
+                                const int pos = kps[k] + 8 * n + 2 * t + (e & 1);
+                                sc[k][n][e] = use[k] && pos <= lim[r] ? sc[k][n][e] * p.scale_log2
+                                                                      : kNegInf;
+                                mx[r] = fmaxf(mx[r], sc[k][n][e]);
+                            }
+                    float alpha[2], msafe[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                        const float mnew = fmaxf(m[r], mx[r]);
+                        // a row with no visible key yet keeps m = -inf, l = 0, o = 0
+                        msafe[r] = mnew == kNegInf ? 0.f : mnew;
+                        alpha[r] = exp2f(m[r] - msafe[r]);
+                        m[r] = mnew;
+                    }
+                    // weights, rounded to fp16 as the MMA applies them: the A
+                    // fragments of P V, one k-step per block
+                    uint32_t pa[kBlocksPerStage][4];
+                    float lsum[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < kBlocksPerStage; ++k)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n)
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                const uint32_t h2 =
+                                    pack_half2(exp2f(sc[k][n][2 * r] - msafe[r]),
+                                               exp2f(sc[k][n][2 * r + 1] - msafe[r]));
+                                pa[k][2 * n + r] = h2;
+                                const float2 u = unpack_half2(h2);
+                                lsum[r] += u.x + u.y;
+                            }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + lsum[r];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        o[nt][0] *= alpha[0];
+                        o[nt][1] *= alpha[0];
+                        o[nt][2] *= alpha[1];
+                        o[nt][3] *= alpha[1];
+                    }
+#pragma unroll
+                    for (int k = 0; k < kBlocksPerStage; ++k) {
+                        if (!use[k]) continue;
+                        const uint32_t vb = stage + (kBlocksPerStage + k) * Gm::kTile;
+                        // value rows past the sequence end hold anything (their
+                        // weights are 0, but 0 * NaN is not): every warp zeroes
+                        // them before use (the same zeros, so the writes agree)
+                        if (kps[k] + kBS > L) dec::zero_tail_rows<D>(vb, tl, 0u, L - kps[k], lane);
+                        // O += P V; per transposed ldmatrix: tokens 0-7 / 8-15
+                        // of dims 0-7, then of dims 8-15
+#pragma unroll
+                        for (int nd = 0; nd < D / 16; ++nd) {
+                            uint32_t v0, v1, v2, v3;
+                            ldsm_x4_trans(v0, v1, v2, v3, vb + tl.at(vtok, vcol + nd * 32));
+                            mma_16816(o[2 * nd], pa[k][0], pa[k][1], pa[k][2], pa[k][3], v0, v1);
+                            mma_16816(o[2 * nd + 1], pa[k][0], pa[k][1], pa[k][2], pa[k][3], v2,
+                                      v3);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_s + st * 8);
+            }
+            if (!ok && lane == 0) {
+                record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+                atomicOr(&misc[1], 1);
+            }
+
+            // normaliser of each row (its four lanes hold parts of it)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float mnew = fmaxf(m[r], mx[r]);
-                // a row with no visible key yet keeps m = -inf, l = 0, o = 0
-                msafe[r] = mnew == kNegInf ? 0.f : mnew;
-                alpha[r] = exp2f(m[r] - msafe[r]);
-                m[r] = mnew;
+                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
             }
-            // weights, rounded to fp16 as the MMA applies them; A fragments of P V
-            uint32_t pa[4];
-            float lsum[2] = {0.f, 0.f};
+            if (nparts == 1) {
+                if (ok) {
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
+                    for (int r = 0; r < 2; ++r) {
+                        if (orow[r] < 0) continue;
+                        const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
+                        __half *dst = p.out + orow[r] * D + 2 * t;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            *reinterpret_cast<__half2 *>(dst + 8 * nt) =
+                                __floats2half2_rn(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
+                    }
+                }
+            } else {
+                // partial state of this partition, then the ticket
+                const int64_t Tq = p.num_query_tokens;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const uint32_t h2 = pack_half2(exp2f(x[n][2 * r] - msafe[r]),
-                                                   exp2f(x[n][2 * r + 1] - msafe[r]));
-                    pa[2 * n + r] = h2;
-                    const float2 u = unpack_half2(h2);
-                    lsum[r] += u.x + u.y;
+                    if (orow[r] < 0) continue;
+                    const int64_t idx = static_cast<int64_t>(part) * Tq * H + orow[r];
+                    if (t == 0) p.part_ml[idx] = make_float2(m[r], l[r]);
+                    float *dst = p.part_o + idx * D + 2 * t;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        *reinterpret_cast<float2 *>(dst + 8 * nt) =
+                            make_float2(o[nt][2 * r], o[nt][2 * r + 1]);
                 }
+                __threadfence();
+                named_barrier(1, kWarps * 32);
+                if (threadIdx.x == 0) {
+                    int *ticket =
+                        p.counters + (static_cast<int64_t>(seq) * Hk + kvh) * p.num_tiles + tile;
+                    __threadfence();
+                    const int prev = atomicAdd(ticket, 1);
+                    const int last = prev == nparts - 1;
+                    if (last) {
+                        atomicExch(ticket, 0);  // leave the workspace zeroed
+                        __threadfence();
+                    }
+                    misc[0] = last;
+                }
+                named_barrier(1, kWarps * 32);
+                if (misc[0]) {
+                    // last partition of the tile: merge every partition's
+                    // partial rows (this warp's 16 rows; lanes over head dims)
+                    constexpr int DPL = D / 32;
+                    for (int rr = 0; rr < 16; ++rr) {
+                        const int rw = tile * kRows + warp * 16 + rr;
+                        if (rw >= rows) break;
+                        const int64_t orw = static_cast<int64_t>(q0 + rw / G) * H + kvh * G + rw % G;
+                        float M = kNegInf;
+                        for (int pp = 0; pp < nparts; ++pp)
+                            M = fmaxf(M, __ldcg(p.part_ml + static_cast<int64_t>(pp) * Tq * H + orw).x);
+                        float den = 0.f, acc[DPL];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + lsum[r];
+                        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+                        for (int pp = 0; pp < nparts; ++pp) {
+                            const int64_t idx = static_cast<int64_t>(pp) * Tq * H + orw;
+                            const float2 ml = __ldcg(p.part_ml + idx);
+                            const float w = ml.x == kNegInf ? 0.f : exp2f(ml.x - M);
+                            den = fmaf(ml.y, w, den);
+                            const float *src = p.part_o + idx * D + lane * DPL;
+                            if constexpr (DPL == 4) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                                acc[0] = fmaf(v.x, w, acc[0]);
+                                acc[1] = fmaf(v.y, w, acc[1]);
+                                acc[2] = fmaf(v.z, w, acc[2]);
+                                acc[3] = fmaf(v.w, w, acc[3]);
+                            } else {
+                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                                acc[0] = fmaf(v.x, w, acc[0]);
+                                acc[1] = fmaf(v.y, w, acc[1]);
+                            }
+                        }
+                        const float inv = den > 0.f ? 1.f / den : 0.f;
+                        __half *dst = p.out + orw * D + lane * DPL;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                o[nt][0] *= alpha[0];
-                o[nt][1] *= alpha[0];
-                o[nt][2] *= alpha[1];
-                o[nt][3] *= alpha[1];
-            }
-            // O += P V: B fragments from the value tile, transposed; per
-            // ldmatrix: tokens 0-7 / 8-15 of dims 0-7, then of dims 8-15
-#pragma unroll
-            for (int nd = 0; nd < D / 16; ++nd) {
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_trans(v0, v1, v2, v3, vb + tl.at(vtok, vcol + nd * 32));
-                mma_16816(o[2 * nd], pa[0], pa[1], pa[2], pa[3], v0, v1);
-                mma_16816(o[2 * nd + 1], pa[0], pa[1], pa[2], pa[3], v2, v3);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_s + st * 8);
-    }
-    if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
-
-    // ---- normaliser of each row (its four lanes hold parts of it)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-        l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-    }
-    if (nparts == 1) {
-        if (!ok) return;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            if (orow[r] < 0) continue;
-            const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
-            __half *dst = p.out + orow[r] * D + 2 * t;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<__half2 *>(dst + 8 * nt) =
-                    __floats2half2_rn(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
-        }
-        return;
-    }
-
-    // ---- partial state of this partition, then the ticket
-    const int64_t Tq = p.num_query_tokens;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        if (orow[r] < 0) continue;
-        const int64_t idx = static_cast<int64_t>(part) * Tq * H + orow[r];
-        if (t == 0) p.part_ml[idx] = make_float2(m[r], l[r]);
-        float *dst = p.part_o + idx * D + 2 * t;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-            *reinterpret_cast<float2 *>(dst + 8 * nt) = make_float2(o[nt][2 * r], o[nt][2 * r + 1]);
-    }
-    __threadfence();
-    named_barrier(1, kWarps * 32);
-    if (threadIdx.x == 0) {
-        int *ticket = p.counters + (static_cast<int64_t>(seq) * Hk + kvh) * p.num_tiles + tile;
-        __threadfence();
-        const int prev = atomicAdd(ticket, 1);
-        const int last = prev == nparts - 1;
-        if (last) {
-            atomicExch(ticket, 0);  // leave the workspace zeroed
-            __threadfence();
-        }
-        misc[0] = last;
-    }
-    named_barrier(1, kWarps * 32);
-    if (!misc[0]) return;
-
-    // ---- last partition of the tile: merge every partition's partial rows
-    // (this warp's 16 rows; lanes over head dims)
-    constexpr int DPL = D / 32;
-    for (int rr = 0; rr < 16; ++rr) {
-        const int rw = tile * kRows + warp * 16 + rr;
-        if (rw >= rows) break;
-        const int64_t orw = static_cast<int64_t>(q0 + rw / G) * H + kvh * G + rw % G;
-        float M = kNegInf;
-        for (int pp = 0; pp < nparts; ++pp)
-            M = fmaxf(M, __ldcg(p.part_ml + static_cast<int64_t>(pp) * Tq * H + orw).x);
-        float den = 0.f, acc[DPL];
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-        for (int pp = 0; pp < nparts; ++pp) {
-            const int64_t idx = static_cast<int64_t>(pp) * Tq * H + orw;
-            const float2 ml = __ldcg(p.part_ml + idx);
-            const float w = ml.x == kNegInf ? 0.f : exp2f(ml.x - M);
-            den = fmaf(ml.y, w, den);
-            const float *src = p.part_o + idx * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                acc[0] = fmaf(v.x, w, acc[0]);
-                acc[1] = fmaf(v.y, w, acc[1]);
-                acc[2] = fmaf(v.z, w, acc[2]);
-                acc[3] = fmaf(v.w, w, acc[3]);
-            } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                acc[0] = fmaf(v.x, w, acc[0]);
-                acc[1] = fmaf(v.y, w, acc[1]);
+                        for (int i = 0; i < DPL; i += 2)
+                            *reinterpret_cast<__half2 *>(dst + i) =
+                                __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+                    }
+                }
             }
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        __half *dst = p.out + orw * D + lane * DPL;
-#pragma unroll
-        for (int i = 0; i < DPL; i += 2)
-            *reinterpret_cast<__half2 *>(dst + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+        gstep += nsteps;
+        __syncthreads();  // the item is done: bt_s and misc are free again
+    }
+    // (every issued copy was waited for by the consumers, unless a wait gave
+    // up; then let the copies of the last ring turn land before exiting)
+    if (warp == kWarps && misc[1]) {
+        for (int st = 0; st < kStages && st < gstep; ++st) {
+            const int last_use = gstep - 1 - ((gstep - 1 - st) % kStages);
+            mbar_wait_bounded(full_s + st * 8, (last_use / kStages) & 1);
+        }
     }
 }
 
@@ -440,7 +636,7 @@ ChunkFn select(int D, int G) {
 }
 
 struct Sizes {
-    int64_t tiles, parts, counters_bytes, ml_bytes, o_bytes;
+    int64_t tiles, parts, counters_bytes, ml_bytes, o_bytes, list_bytes;
     int col_tiles;          // balanced schedule's column n-tiles (0: not used)
     dec::BalancedShape bal;  // its shape (workspace first in the scratch)
     int64_t bal_bytes;
@@ -453,10 +649,13 @@ Sizes sizes(int64_t S, int64_t H, int64_t Hk, int64_t D, int64_t Tq, int64_t max
     z.tiles = std::max<int64_t>(1, (max_q * G + kRows - 1) / kRows);
     z.parts = std::max<int64_t>(1, (max_len + kPartTokens - 1) / kPartTokens);
     z.counters_bytes = dec::align256(S * Hk * z.tiles * 4);
+    z.list_bytes = dec::align256((2 * S + 3) * 4);  // big_seq, big_cum, n_big, work
     z.ml_bytes = z.parts > 1 ? dec::align256(z.parts * Tq * H * 8) : 0;
     z.o_bytes = z.parts > 1 ? z.parts * Tq * H * D * 4 : 0;
-    // the balanced schedule takes the chunks of up to 8 (or 16) query rows
-    z.col_tiles = max_q * G <= 8 ? 1 : 2;
+    // the balanced schedule takes the chunks of up to 8 query rows, or of up
+    // to 16 when no chunk needs the tile kernel (one column tile is the
+    // cheaper policy, so it is used whenever the tile kernel runs anyway)
+    z.col_tiles = (max_q * G <= 8 || max_q * G > 16) ? 1 : 2;
     z.bal = dec::balanced_shape(static_cast<int>(S), static_cast<int>(Hk), static_cast<int>(G),
                                 static_cast<int>(D), sm_count(), false, 8 * z.col_tiles);
     if (!z.bal.ok) z.col_tiles = 0;
@@ -478,7 +677,8 @@ extern "C" size_t pkv_chunk_workspace_bytes(int32_t num_seqs, int32_t num_heads,
         return 0;
     const auto z = pkv::chunk::sizes(num_seqs, num_heads, num_kv_heads, head_dim,
                                      num_query_tokens, max_query_len, max_seq_len);
-    return static_cast<size_t>(z.bal_bytes + z.counters_bytes + z.ml_bytes + z.o_bytes);
+    return static_cast<size_t>(z.bal_bytes + z.list_bytes + z.counters_bytes + z.ml_bytes +
+                               z.o_bytes);
 }
 
 extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache,
@@ -511,8 +711,13 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
         return PKV_ERR_ALIGNMENT;
     const auto z = sizes(num_seqs, num_heads, num_kv_heads, head_dim, num_query_tokens,
                          max_query_len, max_seq_len);
-    if (z.tiles > INT32_MAX || num_kv_heads * z.parts > 65535) return PKV_ERR_UNSUPPORTED;
-    const int64_t need = z.bal_bytes + z.counters_bytes + z.ml_bytes + z.o_bytes;
+    // work items (and their prefix sums) are 32-bit: at most
+    // (sum of tiles <= Tq*G/64 + S) * partitions * Hk of them
+    const int64_t tiles_sum = (static_cast<int64_t>(num_query_tokens) * G + kRows - 1) / kRows +
+                              num_seqs;
+    if (tiles_sum * z.parts * num_kv_heads > INT32_MAX || z.tiles > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    const int64_t need = z.bal_bytes + z.list_bytes + z.counters_bytes + z.ml_bytes + z.o_bytes;
     if (workspace == nullptr || static_cast<int64_t>(workspace_bytes) < need)
         return PKV_ERR_WORKSPACE;
     ChunkFn fn = select(head_dim, G);
@@ -579,6 +784,12 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     p.min_rows = min_rows;
     p.num_blocks = num_blocks;
     uint8_t *cws = ws + z.bal_bytes;
+    p.num_seqs = num_seqs;
+    p.big_seq = reinterpret_cast<int *>(cws);
+    p.big_cum = p.big_seq + num_seqs;
+    p.n_big = p.big_cum + num_seqs + 1;
+    p.work = p.n_big + 1;
+    cws += z.list_bytes;
     p.counters = reinterpret_cast<int *>(cws);
     p.part_ml = reinterpret_cast<float2 *>(cws + z.counters_bytes);
     p.part_o = reinterpret_cast<float *>(cws + z.counters_bytes + z.ml_bytes);
@@ -592,13 +803,16 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     p.err = device_error_record();
     if (p.err == nullptr) return PKV_ERR_CUDA;
 
+    // the work list (one CTA), then persistent CTAs that pull from it
+    chunk_plan_kernel<<<1, 1024, 0, s>>>(p, G);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_failure(e, "chunk plan launch");
     const int smem = smem_bytes(head_dim);
-    const int st = prepare_kernel(reinterpret_cast<const void *>(fn), kThreads, smem, nullptr);
+    int per_sm = 0;
+    const int st = prepare_kernel(reinterpret_cast<const void *>(fn), kThreads, smem, &per_sm);
     if (st != PKV_OK) return st;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(z.tiles),
-                       static_cast<unsigned>(num_kv_heads * z.parts),
-                       static_cast<unsigned>(num_seqs));
+    cfg.gridDim = dim3(static_cast<unsigned>(std::max(1, sm_count() * std::max(1, per_sm))));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -607,7 +821,7 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
+    e = cudaLaunchKernelEx(&cfg, fn, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_failure(e, "chunk attention launch");
 }
