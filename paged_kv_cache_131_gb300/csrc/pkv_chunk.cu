@@ -6,25 +6,37 @@
 //
 // Sequences whose new tokens times the group size fit the balanced decode
 // schedule's query columns (8 or 16: MmaColsPolicy) run there -- the same
-// streaming of whole token rows as a decode; the others run here.
+// streaming of whole token rows as a decode; the others run here, on the
+// fifth-generation tensor cores (tcgen05) with accumulators in tensor memory.
 //
-// The work is a list of items (query tile of 64 rows, KV head, KV
+// The work is a list of items (query tile of 128 rows, KV head, KV
 // partition of 2048 tokens, sequence), built on the device by a one-CTA plan
 // kernel for the sequences this kernel takes (partitions past a tile's
-// causal range are not items).  Persistent CTAs (two per SM) pull items in
+// causal range are not items).  Persistent CTAs (one per SM) pull items in
 // list order from an atomic counter, so tiles with more keys and tiles with
 // fewer balance out.  A row is (new token j, query head g of the KV head's
-// group): row = j*G + g, so a tile covers 64/G consecutive new tokens.  Four
-// consumer warps own 16 rows each; a producer warp stages the partition's
-// blocks -- two per stage, each block one tensor copy (TMA) of the head's
-// 16 key rows and one of its 16 value rows -- into a 4-deep ring.  Per stage
-// (32 keys) a warp computes S = Q K^T (m16n8k16: rows = query rows, columns
-// = tokens), masks the keys past each row's position, folds the 32 keys into
-// each row's online softmax (log2 domain) and accumulates O += P V, the
-// weights taken straight from the score fragments.  A tile whose causal range fits one
-// partition writes fp16 out; otherwise every partition leaves fp32 partial
-// states and the last CTA of the tile to take a ticket merges them with a
-// log-sum-exp rescale.  No CTA waits for another.
+// group): row = j*G + g, so a tile covers 128/G consecutive new tokens.
+//
+// Per CTA, warp-specialised, all hand-offs through mbarriers:
+//  * warp 0 takes the items, stages the tile's query rows (two tiles in
+//    flight) and the partition's keys, 8 blocks (128 keys) per step, one
+//    tensor copy per block and 64-dimension chunk, into a 3-step ring laid
+//    out [chunk][key][128 B] so the 128 keys form one MMA operand;
+//  * warp 1 stages the values, one tensor copy per block, into a 2-step ring;
+//  * warp 2 issues the MMAs (one thread): S = Q K^T (M = 128 rows, N = 128
+//    keys) into one of two 128-column score buffers in tensor memory, and
+//    O += P V (N = head_dim, 16 keys per MMA) with P read from tensor memory;
+//  * warps 3-6 run the softmax, one thread per query row: they read the
+//    row's scores, mask keys past the row's position (and past the sequence
+//    or in a bad block), keep the row's running maximum m and sum l in the
+//    log2 domain and write the fp16 weights P = 2^(s - m) back to tensor
+//    memory.  The reference m moves only when the maximum grows by more
+//    than 2^8 (the weights stay <= 256): then O is rescaled in tensor memory
+//    first.  The result O / l does not depend on which reference was used.
+// A tile whose causal range fits one partition writes fp16 out; otherwise
+// every partition leaves fp32 partial states (m, l, O) and the last CTA of
+// the tile to take a ticket merges them with a log-sum-exp rescale.  No CTA
+// waits for another.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -33,11 +45,12 @@
 #include <cmath>
 #include <cstdint>
 
-#include "/root/repo/include/pagedkv.h"
+#include "../../include/pagedkv.h"
 #include "pkv_decode_common.cuh"
 #include "pkv_decode_host.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_tcgen05.cuh"
 
 namespace pkv {
 namespace chunk {
@@ -45,19 +58,28 @@ namespace {
 
 using dec::kBS;
 using dec::kNegInf;
-using dec::SwizzledTile;
 
-constexpr int kRows = 64;                 // query rows per CTA
-constexpr int kWarps = 4;                 // consumer warps, 16 rows each
-constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kStages = 4;
-constexpr int kBlocksPerStage = 2;
-constexpr int kPartTokens = 2048;         // KV partition
+constexpr int kRows = 128;                     // query rows per tile: the MMA's M
+constexpr int kStepBlocks = 8;                 // blocks per step
+constexpr int kStepKeys = kStepBlocks * kBS;   // 128 keys: the score MMA's N
+constexpr int kKStages = 3;                    // key ring depth (steps)
+constexpr int kVStages = 2;                    // value ring depth (steps)
+constexpr int kPartTokens = 2048;              // KV partition
 constexpr int kPartBlocks = kPartTokens / kBS;
+constexpr int kSoftmaxWarps = 4;               // one thread per query row
+constexpr int kThreads = (3 + kSoftmaxWarps) * 32;
+// tensor memory: O in columns [0, head_dim), scores in two buffers of 128
+// columns, weights (fp16 pairs) in 64 columns
+constexpr int kTmemCols = 512;
+constexpr int kTmemO = 0;
+constexpr int kTmemS = 128;
+constexpr int kTmemP = 384;
+constexpr float kRescaleLog2 = 8.f;            // move the reference past 2^8
 
 struct ChunkParams {
-    CUtensorMap tm_k;  // per-head boxes of the key / value caches
-    CUtensorMap tm_v;
+    CUtensorMap tm_k;  // keys: one 128-byte chunk of 16 rows per copy
+    CUtensorMap tm_v;  // values: a head's chunks of 16 rows per copy
+    CUtensorMap tm_q;  // query rows: 128 bytes of each row of a 128-row tile
     __half *out;
     const __half *q;
     const int32_t *block_tables;
@@ -69,7 +91,7 @@ struct ChunkParams {
     int max_blocks_per_seq;
     int max_query_len;
     int max_seq_len;
-    int num_tiles;  // grid.x
+    int num_tiles;  // tiles per (sequence, kv head) the tickets are sized for
     int num_query_tokens;
     int min_rows;   // sequences with fewer rows (new tokens x group) are not ours
     int num_seqs;
@@ -87,23 +109,66 @@ struct ChunkParams {
     ErrorRecord *err;
 };
 
-template <int D>
-struct Geo {
-    static constexpr int kTile = kBS * D * 2;  // one block's K (or V) slice of one head
-    static constexpr int kStage = 2 * kBlocksPerStage * kTile;
-    static constexpr int kRing = kStages * kStage;
+// An item as the producer hands it to the other warps (64 bytes).
+struct ItemInfo {
+    int seq, part, kvh, tile;
+    int nsteps, nblk, L, Q;
+    int q0, nparts, done, pad;
+    uint32_t valid[kPartBlocks / 32];  // one bit per block of the partition: id in range
 };
 
-constexpr int kMisc = 8;  // ints of CTA-wide scratch
+// Shared memory (from a 1024-aligned base): two query tiles, the key ring,
+// the value ring, the mbarriers, two item records and a few words.
+template <int D>
+struct Geo {
+    static constexpr int kChunks = D / 64;                   // 128-byte chunks of a head row
+    static constexpr int kQ = kChunks * kRows * 128;         // [chunk][row][128 B]
+    static constexpr int kK = kChunks * kStepKeys * 128;     // [chunk][key][128 B]
+    static constexpr int kVBlock = kChunks * kBS * 128;      // [chunk][token][128 B]
+    static constexpr int kV = kStepBlocks * kVBlock;
+    static constexpr int kOffK = 2 * kQ;
+    static constexpr int kOffV = kOffK + kKStages * kK;
+    static constexpr int kOffBar = kOffV + kVStages * kV;
+    static constexpr int kBars = 2 + 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 3;
+    static constexpr int kOffInfo = kOffBar + kBars * 8;
+    static constexpr int kOffMisc = kOffInfo + 2 * static_cast<int>(sizeof(ItemInfo));
+    static constexpr int kBytes = kOffMisc + 16;
+};
 
 int smem_bytes(int D) {
-    const int tile = kBS * D * 2;
-    return dec::kTileAlign + kStages * 2 * kBlocksPerStage * tile + 2 * kStages * 8 +
-           kPartBlocks * 4 + kMisc * 4;
+    return dec::kTileAlign + (D == 128 ? Geo<128>::kBytes : Geo<64>::kBytes);
 }
 
-__device__ __forceinline__ void named_barrier(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+// mbarrier addresses (shared-space) by role
+struct Bars {
+    uint32_t b;
+    __device__ uint32_t q_full(int s) const { return b + 8 * s; }
+    __device__ uint32_t q_empty(int s) const { return b + 8 * (2 + s); }
+    __device__ uint32_t k_full(int s) const { return b + 8 * (4 + s); }
+    __device__ uint32_t k_empty(int s) const { return b + 8 * (4 + kKStages + s); }
+    __device__ uint32_t v_full(int s) const { return b + 8 * (4 + 2 * kKStages + s); }
+    __device__ uint32_t v_empty(int s) const { return b + 8 * (4 + 2 * kKStages + kVStages + s); }
+    __device__ uint32_t s_full(int s) const { return b + 8 * (4 + 2 * kKStages + 2 * kVStages + s); }
+    __device__ uint32_t s_free(int s) const {
+        return b + 8 * (6 + 2 * kKStages + 2 * kVStages + s);
+    }
+    __device__ uint32_t p_full() const { return b + 8 * (8 + 2 * kKStages + 2 * kVStages); }
+    __device__ uint32_t pv_done() const { return b + 8 * (9 + 2 * kKStages + 2 * kVStages); }
+    __device__ uint32_t o_free() const { return b + 8 * (10 + 2 * kKStages + 2 * kVStages); }
+};
+
+// arrivals that complete a phase of each barrier
+constexpr int kQEmptyArrivals = 2 + kSoftmaxWarps;  // MMA commit, value producer, softmax warps
+
+// Every lane waits (bounded); false if any lane gave up.
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Geometry of sequence s for this kernel; false if the sequence is not
@@ -133,7 +198,7 @@ __device__ __forceinline__ bool seq_geo(const ChunkParams &p, int s, int G, bool
 }
 
 // First query tile that needs KV partition `part` (its last token reaches
-// the partition): tile t's last token j_last(t) = (min(rows, 64(t+1)) - 1)/G
+// the partition): tile t's last token j_last(t) = (min(rows, 128(t+1)) - 1)/G
 // sees keys up to L - Q + j_last(t).
 __device__ __forceinline__ int first_tile(const SeqGeo &sg, int part, int G) {
     const int x = part * kPartTokens - (sg.L - sg.Q);  // j_last must reach x
@@ -217,421 +282,550 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
     }
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+// Block ids of an item's partition: lane l holds blocks l, 32 + l, 64 + l and
+// 96 + l of it; -1 past the item or out of range (recorded when `report`).
+__device__ __forceinline__ void load_ids(const ChunkParams &p, int seq, int blo, int nblk,
+                                         int lane, bool report, int (&ids)[kPartBlocks / 32]) {
+#pragma unroll
+    for (int w = 0; w < kPartBlocks / 32; ++w) {
+        const int b = w * 32 + lane;
+        int id = -1;
+        if (b < nblk) {
+            const int64_t at = static_cast<int64_t>(seq) * p.max_blocks_per_seq + blo + b;
+            id = __ldg(p.block_tables + at);
+            if (id < 0 || static_cast<int64_t>(id) >= p.num_blocks) {
+                if (report) record_error(p.err, PKV_DEVERR_BLOCK_ID, at);
+                id = -1;
+            }
+        }
+        ids[w] = id;
+    }
+}
+
+// Block b's id (every lane calls).
+__device__ __forceinline__ int id_of(const int (&ids)[kPartBlocks / 32], int b) {
+    int v = -1;
+#pragma unroll
+    for (int w = 0; w < kPartBlocks / 32; ++w) {
+        const int x = __shfl_sync(0xffffffffu, ids[w], b & 31);
+        if ((b >> 5) == w) v = x;
+    }
+    return v;
+}
+
+// The (partition, kv head, tile) of item `local` of a sequence: partition-
+// major, then kv head, then tile (consecutive items share their keys).
+__device__ __forceinline__ int3 decode_item(const SeqGeo &sg, int local, int G, int Hk) {
+    for (int pt = 0; pt < sg.parts; ++pt) {
+        const int t0 = first_tile(sg, pt, G);
+        const int nt = sg.tiles - t0;
+        if (local < nt * Hk) return make_int3(pt, local / nt, t0 + local % nt);
+        local -= nt * Hk;
+    }
+    return make_int3(-1, -1, -1);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
     chunk_attention_kernel(const __grid_constant__ ChunkParams p) {
     using Gm = Geo<D>;
-    constexpr int KS = D / 16;  // k-steps of S = Q K^T
-    constexpr int NT = D / 8;   // n-tiles of O
+    constexpr int CH = Gm::kChunks;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((dec::kTileAlign - (smem_u32(smem_raw) & (dec::kTileAlign - 1))) &
                                 (dec::kTileAlign - 1));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Gm::kRing);
-    uint64_t *empty = full + kStages;
-    int *bt_s = reinterpret_cast<int *>(empty + kStages);
-    // misc: [0] last-contributor flag, [1] failure flag, [2..7] current item
-    // (sequence, partition, kv head, tile, valid)
-    int *misc = bt_s + kPartBlocks;
+    const uint32_t sb = smem_u32(smem);
+    const Bars br{sb + Gm::kOffBar};
+    ItemInfo *info = reinterpret_cast<ItemInfo *>(smem + Gm::kOffInfo);
+    // misc: [0] tensor-memory base
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + Gm::kOffMisc);
 
     const int Hk = p.num_kv_heads, H = p.num_heads;
+    const int G = H / Hk, logG = __ffs(G) - 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), kWarps);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(br.q_full(s), 1);
+            mbar_init(br.q_empty(s), kQEmptyArrivals);
+            mbar_init(br.s_full(s), 1);
+            mbar_init(br.s_free(s), kSoftmaxWarps);
         }
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(br.k_full(s), 1);
+            mbar_init(br.k_empty(s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(br.v_full(s), 1);
+            mbar_init(br.v_empty(s), 1);
+        }
+        mbar_init(br.p_full(), kSoftmaxWarps);
+        mbar_init(br.pv_done(), 1);
+        mbar_init(br.o_free(), kSoftmaxWarps);
         fence_mbarrier_init();
-        misc[1] = 0;
     }
-    // the work list, the caches and the outputs are all written by earlier
+    if (warp == 2) {
+        tc::tmem_alloc(sb + Gm::kOffMisc, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // the work list, the caches and the outputs are written by earlier
     // kernels of the stream
     grid_dependency_wait();
+    tc::fence_before_sync();
     __syncthreads();
-    const int n_big = __ldcg(p.n_big);
-    const int total = __ldcg(p.big_cum + n_big);
-    const uint32_t ring_s = smem_u32(smem);
-    const uint32_t full_s = smem_u32(full), empty_s = smem_u32(empty);
-    const SwizzledTile tl{7u};
-    int gstep = 0;  // ring steps run by this CTA so far (stage and phase of the next)
+    tc::fence_after_sync();
+    const uint32_t tmem = static_cast<uint32_t>(misc[0]);
 
-    for (;;) {
-        if (threadIdx.x == 0) {
-            const int item = atomicAdd(p.work, 1);
-            int valid = item < total && !misc[1];
-            if (valid) {
-                // the listed sequence holding the item, then its (partition,
-                // kv head, tile): partition-major, then kv head, then tile
-                int lo = 0, hi = n_big - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (__ldcg(p.big_cum + mid) <= item) lo = mid;
-                    else hi = mid - 1;
-                }
-                const int s = __ldcg(p.big_seq + lo);
-                int local = item - __ldcg(p.big_cum + lo);
-                SeqGeo sg;
-                valid = seq_geo(p, s, G, false, sg);
-                int part = 0, kv = 0, tile = 0;
-                for (int pt = 0; valid && pt < sg.parts; ++pt) {
-                    const int t0 = first_tile(sg, pt, G);
-                    const int nt = sg.tiles - t0;
-                    if (local < nt * Hk) {
-                        part = pt;
-                        kv = local / nt;
-                        tile = t0 + local % nt;
-                        break;
-                    }
-                    local -= nt * Hk;
-                }
-                misc[2] = s;
-                misc[3] = part;
-                misc[4] = kv;
-                misc[5] = tile;
+    if (warp == 0) {
+        // ===================== items, query tiles and keys =====================
+        const int n_big = __ldcg(p.n_big);
+        const int total = __ldcg(p.big_cum + n_big);
+        int gs = 0;  // steps staged
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(p.work, 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            const int slot = it & 1;
+            if (it >= 2 && !wait_all(br.q_empty(slot), ((it >> 1) - 1) & 1)) {
+                ok = false;
+                break;
             }
-            misc[6] = valid;
-        }
-        __syncthreads();
-        if (!misc[6]) break;
-        const int seq = misc[2], part = misc[3], kvh = misc[4], tile = misc[5];
-        SeqGeo sg;
-        seq_geo(p, seq, G, false, sg);
-        const int L = sg.L, Q = sg.Q, q0 = sg.q0, rows = sg.rows;
-        const int j_last = (min(rows, (tile + 1) * kRows) - 1) / G;
-        const int kv_end = L - Q + j_last + 1;  // keys [0, kv_end) for this tile
-        const int nparts = (kv_end + kPartTokens - 1) / kPartTokens;
-        const int k0 = part * kPartTokens;
-        const int k1 = min(kv_end, k0 + kPartTokens);
-        const int blo = k0 / kBS;
-        const int nblk = (k1 + kBS - 1) / kBS - blo;  // >= 1
-        const int nsteps = (nblk + kBlocksPerStage - 1) / kBlocksPerStage;
-        const int head_chunk = kvh * (D * 2 / 128);
-
-        // the partition's block ids, checked
-        for (int b = threadIdx.x; b < nblk; b += kThreads) {
-            int id = __ldg(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blo + b);
-            if (id < 0 || static_cast<int64_t>(id) >= p.num_blocks) {
-                record_error(p.err, PKV_DEVERR_BLOCK_ID,
-                             static_cast<int64_t>(seq) * p.max_blocks_per_seq + blo + b);
-                id = -1;
-            }
-            bt_s[b] = id;
-        }
-        __syncthreads();
-
-        if (warp == kWarps) {
-            // ============================== producer ==============================
-            for (int i = 0; i < nsteps; ++i) {
-                const int gi = gstep + i;
-                const int st = gi % kStages;
-                if (gi >= kStages) {
-                    const bool free_ =
-                        mbar_wait_bounded(empty_s + st * 8, ((gi / kStages) - 1) & 1);
-                    if (!__all_sync(0xffffffffu, free_)) {
-                        if (lane == 0) {
-                            record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
-                            atomicOr(&misc[1], 1);
-                        }
-                        break;
-                    }
+            if (item >= total) {
+                if (lane == 0) {
+                    info[slot].done = 1;
+                    mbar_arrive(br.q_full(slot));
                 }
-                const int nb = min(kBlocksPerStage, nblk - i * kBlocksPerStage);
-                int ncopy = 0;
-                for (int k = 0; k < nb; ++k) ncopy += bt_s[i * kBlocksPerStage + k] >= 0 ? 1 : 0;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(full_s + st * 8,
-                                          static_cast<uint32_t>(ncopy) * 2u * Gm::kTile);
-                __syncwarp();
-                // lanes 0, 1: key tiles of the stage's blocks; lanes 2, 3: value tiles
-                const int k = lane % kBlocksPerStage;
-                const bool value = lane >= kBlocksPerStage;
-                if (lane < 2 * kBlocksPerStage && k < nb) {
-                    const int id = bt_s[i * kBlocksPerStage + k];
-                    if (id >= 0)
-                        tensor_g2s_3d(ring_s + st * Gm::kStage +
-                                          (value ? kBlocksPerStage + k : k) * Gm::kTile,
-                                      value ? &p.tm_v : &p.tm_k, 0, id * kBS, head_chunk,
-                                      full_s + st * 8);
-                }
+                break;
             }
-        } else {
-            // ============================== consumers ==============================
-            const int g = lane >> 2, t = lane & 3;
-            int lim[2];
-            int64_t orow[2];  // (query row * H + head) of each of the lane's two rows, or -1
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int rr = tile * kRows + warp * 16 + g + 8 * r;
-                if (rr < rows) {
-                    const int j = rr / G;
-                    lim[r] = L - Q + j;  // last key position it sees
-                    orow[r] = static_cast<int64_t>(q0 + j) * H + kvh * G + rr % G;
-                } else {
-                    lim[r] = -1;
-                    orow[r] = -1;
-                }
+            // the listed sequence holding the item (every lane searches alike)
+            int lo = 0, hi = n_big - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldcg(p.big_cum + mid) <= item) lo = mid;
+                else hi = mid - 1;
             }
-            int wlim = max(lim[0], lim[1]);  // the largest key position this warp sees
+            const int seq = __ldcg(p.big_seq + lo);
+            SeqGeo sg;
+            seq_geo(p, seq, G, false, sg);  // (the plan listed it: valid)
+            const int3 d = decode_item(sg, item - __ldcg(p.big_cum + lo), G, Hk);
+            const int part = d.x, kvh = d.y, tile = d.z;
+            const int j_last = (min(sg.rows, (tile + 1) * kRows) - 1) >> logG;
+            const int kv_end = sg.L - sg.Q + j_last + 1;  // keys [0, kv_end) for the tile
+            const int k1 = min(kv_end, (part + 1) * kPartTokens);
+            const int blo = part * kPartBlocks;
+            const int nblk = (k1 + kBS - 1) / kBS - blo;  // >= 1
+            const int nsteps = (nblk + kStepBlocks - 1) / kStepBlocks;
+            int ids[kPartBlocks / 32];
+            load_ids(p, seq, blo, nblk, lane, true, ids);
+            uint32_t valid[kPartBlocks / 32];
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1)
-                wlim = max(wlim, __shfl_xor_sync(0xffffffffu, wlim, o));
-            uint32_t qa[KS][4];
+            for (int w = 0; w < kPartBlocks / 32; ++w) valid[w] = __ballot_sync(0xffffffffu, ids[w] >= 0);
+            if (lane == 0) {
+                ItemInfo &in = info[slot];
+                in.seq = seq;
+                in.part = part;
+                in.kvh = kvh;
+                in.tile = tile;
+                in.nsteps = nsteps;
+                in.nblk = nblk;
+                in.L = sg.L;
+                in.Q = sg.Q;
+                in.q0 = sg.q0;
+                in.nparts = (kv_end + kPartTokens - 1) / kPartTokens;
+                in.done = 0;
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if (orow[r] >= 0) {
-                        const uint32_t *src =
-                            reinterpret_cast<const uint32_t *>(p.q + orow[r] * D + kk * 16);
-                        qa[kk][r] = __ldg(src + t);
-                        qa[kk][2 + r] = __ldg(src + 4 + t);
-                    } else {
-                        qa[kk][r] = qa[kk][2 + r] = 0u;
-                    }
-                }
+                for (int w = 0; w < kPartBlocks / 32; ++w) in.valid[w] = valid[w];
+                mbar_arrive_expect_tx(br.q_full(slot), Gm::kQ);
             }
-            float o[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-            float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
-            const int ktok = (lane & 7) + (lane >> 4) * 8;
-            const uint32_t kcol = ((lane >> 3) & 1) * 16;
-            const int vtok = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const uint32_t vcol = (lane >> 4) * 16;
-
-            bool ok = true;
-            for (int i = 0; i < nsteps; ++i) {
-                const int gi = gstep + i;
-                const int st = gi % kStages;
-                const bool landed = mbar_wait_bounded(full_s + st * 8, (gi / kStages) & 1);
-                if (!__all_sync(0xffffffffu, landed)) {
+            __syncwarp();
+            if (lane < CH)
+                tensor_g2s_3d(sb + slot * Gm::kQ + lane * (kRows * 128), &p.tm_q, 128 * lane,
+                              kvh * G, sg.q0 + tile * (kRows >> logG), br.q_full(slot));
+            for (int n = 0; n < nsteps; ++n, ++gs) {
+                const int ks = gs % kKStages;
+                if (gs >= kKStages && !wait_all(br.k_empty(ks), ((gs / kKStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                const int nb = min(kBlocksPerStage, nblk - i * kBlocksPerStage);
-                // the stage's blocks in one softmax step (2 x 16 keys): which
-                // of them this warp needs (warp-uniform), and where they start
-                bool use[kBlocksPerStage];
-                int kps[kBlocksPerStage];
-                bool any = false;
-#pragma unroll
-                for (int k = 0; k < kBlocksPerStage; ++k) {
-                    kps[k] = (blo + i * kBlocksPerStage + k) * kBS;
-                    use[k] = k < nb && bt_s[i * kBlocksPerStage + k] >= 0 && kps[k] <= wlim;
-                    any = any || use[k];
-                }
-                if (any) {
-                    const uint32_t stage = ring_s + st * Gm::kStage;
-                    // S = Q K^T for both blocks: n-tiles (block k, tokens 0-7 / 8-15)
-                    float sc[kBlocksPerStage][2][4];
-#pragma unroll
-                    for (int k = 0; k < kBlocksPerStage; ++k)
-#pragma unroll
-                        for (int n = 0; n < 2; ++n)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) sc[k][n][e] = 0.f;
-#pragma unroll
-                    for (int k = 0; k < kBlocksPerStage; ++k) {
-                        if (!use[k]) continue;
-                        const uint32_t kb = stage + k * Gm::kTile;
-#pragma unroll
-                        for (int kk = 0; kk < KS; ++kk) {
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4(b0, b1, b2, b3, kb + tl.at(ktok, kcol + kk * 32));
-                            mma_16816(sc[k][0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                            mma_16816(sc[k][1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-                        }
-                    }
-                    // element e of n-tile n of block k: row g (e < 2) or g+8,
-                    // key position kps[k] + 8n + 2t + (e & 1)
-                    float mx[2] = {kNegInf, kNegInf};
-#pragma unroll
-                    for (int k = 0; k < kBlocksPerStage; ++k)
-#pragma unroll
-                        for (int n = 0; n < 2; ++n)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int r = e >> 1;
-                                const int pos = kps[k] + 8 * n + 2 * t + (e & 1);
-                                sc[k][n][e] = use[k] && pos <= lim[r] ? sc[k][n][e] * p.scale_log2
-                                                                      : kNegInf;
-                                mx[r] = fmaxf(mx[r], sc[k][n][e]);
-                            }
-                    float alpha[2], msafe[2];
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                        const float mnew = fmaxf(m[r], mx[r]);
-                        // a row with no visible key yet keeps m = -inf, l = 0, o = 0
-                        msafe[r] = mnew == kNegInf ? 0.f : mnew;
-                        alpha[r] = exp2f(m[r] - msafe[r]);
-                        m[r] = mnew;
-                    }
-                    // weights, rounded to fp16 as the MMA applies them: the A
-                    // fragments of P V, one k-step per block
-                    uint32_t pa[kBlocksPerStage][4];
-                    float lsum[2] = {0.f, 0.f};
-#pragma unroll
-                    for (int k = 0; k < kBlocksPerStage; ++k)
-#pragma unroll
-                        for (int n = 0; n < 2; ++n)
-#pragma unroll
-                            for (int r = 0; r < 2; ++r) {
-                                const uint32_t h2 =
-                                    pack_half2(exp2f(sc[k][n][2 * r] - msafe[r]),
-                                               exp2f(sc[k][n][2 * r + 1] - msafe[r]));
-                                pa[k][2 * n + r] = h2;
-                                const float2 u = unpack_half2(h2);
-                                lsum[r] += u.x + u.y;
-                            }
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) l[r] = l[r] * alpha[r] + lsum[r];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        o[nt][0] *= alpha[0];
-                        o[nt][1] *= alpha[0];
-                        o[nt][2] *= alpha[1];
-                        o[nt][3] *= alpha[1];
-                    }
-#pragma unroll
-                    for (int k = 0; k < kBlocksPerStage; ++k) {
-                        if (!use[k]) continue;
-                        const uint32_t vb = stage + (kBlocksPerStage + k) * Gm::kTile;
-                        // value rows past the sequence end hold anything (their
-                        // weights are 0, but 0 * NaN is not): every warp zeroes
-                        // them before use (the same zeros, so the writes agree)
-                        if (kps[k] + kBS > L) dec::zero_tail_rows<D>(vb, tl, 0u, L - kps[k], lane);
-                        // O += P V; per transposed ldmatrix: tokens 0-7 / 8-15
-                        // of dims 0-7, then of dims 8-15
-#pragma unroll
-                        for (int nd = 0; nd < D / 16; ++nd) {
-                            uint32_t v0, v1, v2, v3;
-                            ldsm_x4_trans(v0, v1, v2, v3, vb + tl.at(vtok, vcol + nd * 32));
-                            mma_16816(o[2 * nd], pa[k][0], pa[k][1], pa[k][2], pa[k][3], v0, v1);
-                            mma_16816(o[2 * nd + 1], pa[k][0], pa[k][1], pa[k][2], pa[k][3], v2,
-                                      v3);
-                        }
-                    }
-                }
+                const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
+                if (lane == 0) mbar_arrive_expect_tx(br.k_full(ks), nb * CH * kBS * 128);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_s + st * 8);
+                // lane l: block l / CH of the step, chunk l % CH (a bad block
+                // reads rows before the cache: zeros)
+                const int b = min(lane / CH, kStepBlocks - 1), c = lane % CH;
+                const int id = id_of(ids, n * kStepBlocks + b);
+                if (lane < nb * CH)
+                    tensor_g2s_3d(sb + Gm::kOffK + ks * Gm::kK + c * (kStepKeys * 128) +
+                                      b * (kBS * 128),
+                                  &p.tm_k, 0, id >= 0 ? id * kBS : -kBS, kvh * CH + c,
+                                  br.k_full(ks));
             }
-            if (!ok && lane == 0) {
-                record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
-                atomicOr(&misc[1], 1);
+        }
+        if (!ok) {
+            if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+            // let the last copies land before the CTA can exit
+            for (int s = 0; s < kKStages && s < gs; ++s) {
+                const int last = gs - 1 - ((gs - 1 - s) % kKStages);
+                mbar_wait_bounded(br.k_full(s), (last / kKStages) & 1);
             }
-
-            // normaliser of each row (its four lanes hold parts of it)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+        }
+    } else if (warp == 1) {
+        // ================================ values ================================
+        int gs = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            const int slot = it & 1;
+            if (!wait_all(br.q_full(slot), (it >> 1) & 1)) {
+                ok = false;
+                break;
             }
-            if (nparts == 1) {
-                if (ok) {
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        if (orow[r] < 0) continue;
-                        const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
-                        __half *dst = p.out + orow[r] * D + 2 * t;
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            *reinterpret_cast<__half2 *>(dst + 8 * nt) =
-                                __floats2half2_rn(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
-                    }
+            const ItemInfo &in = info[slot];
+            const int done = in.done, seq = in.seq, part = in.part, kvh = in.kvh;
+            const int nsteps = in.nsteps, nblk = in.nblk;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(br.q_empty(slot));
+            if (done) break;
+            int ids[kPartBlocks / 32];
+            load_ids(p, seq, part * kPartBlocks, nblk, lane, false, ids);
+            for (int n = 0; n < nsteps; ++n, ++gs) {
+                const int vs = gs % kVStages;
+                if (gs >= kVStages && !wait_all(br.v_empty(vs), ((gs / kVStages) - 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-            } else {
-                // partial state of this partition, then the ticket
-                const int64_t Tq = p.num_query_tokens;
+                const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
+                if (lane == 0) mbar_arrive_expect_tx(br.v_full(vs), nb * Gm::kVBlock);
+                __syncwarp();
+                const int id = id_of(ids, n * kStepBlocks + min(lane, kStepBlocks - 1));
+                if (lane < nb)
+                    tensor_g2s_3d(sb + Gm::kOffV + vs * Gm::kV + lane * Gm::kVBlock, &p.tm_v, 0,
+                                  id >= 0 ? id * kBS : -kBS, kvh * CH, br.v_full(vs));
+            }
+        }
+        if (!ok) {
+            if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+            for (int s = 0; s < kVStages && s < gs; ++s) {
+                const int last = gs - 1 - ((gs - 1 - s) % kVStages);
+                mbar_wait_bounded(br.v_full(s), (last / kVStages) & 1);
+            }
+        }
+    } else if (warp == 2) {
+        // ================================= MMAs =================================
+        constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kRows, D, false, true);
+        int gs = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            const int slot = it & 1;
+            if (!wait_all(br.q_full(slot), (it >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const ItemInfo &in = info[slot];
+            const int done = in.done, nsteps = in.nsteps, nblk = in.nblk, L = in.L;
+            const int blo = in.part * kPartBlocks;
+            if (done) break;
+            const uint32_t q_s = sb + slot * Gm::kQ;
+            // step n: scores of step n, then the values of step n - 1 (the
+            // softmax of step n - 1 overlaps the score MMAs of step n)
+            for (int n = 0; n <= nsteps && ok; ++n) {
+                if (n < nsteps) {
+                    const int g = gs + n, ks = g % kKStages, buf = g & 1;
+                    ok = wait_all(br.k_full(ks), (g / kKStages) & 1);
+                    if (ok && g >= 2) ok = wait_all(br.s_free(buf), ((g - 2) >> 1) & 1);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    if (lane == 0) {
+                        const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
+                        const uint32_t idesc = tc::idesc_f16_f32(kRows, nb * kBS, false, false);
+                        const uint32_t k_s = sb + Gm::kOffK + ks * Gm::kK;
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if (orow[r] < 0) continue;
-                    const int64_t idx = static_cast<int64_t>(part) * Tq * H + orow[r];
-                    if (t == 0) p.part_ml[idx] = make_float2(m[r], l[r]);
-                    float *dst = p.part_o + idx * D + 2 * t;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        *reinterpret_cast<float2 *>(dst + 8 * nt) =
-                            make_float2(o[nt][2 * r], o[nt][2 * r + 1]);
-                }
-                __threadfence();
-                named_barrier(1, kWarps * 32);
-                if (threadIdx.x == 0) {
-                    int *ticket =
-                        p.counters + (static_cast<int64_t>(seq) * Hk + kvh) * p.num_tiles + tile;
-                    __threadfence();
-                    const int prev = atomicAdd(ticket, 1);
-                    const int last = prev == nparts - 1;
-                    if (last) {
-                        atomicExch(ticket, 0);  // leave the workspace zeroed
-                        __threadfence();
-                    }
-                    misc[0] = last;
-                }
-                named_barrier(1, kWarps * 32);
-                if (misc[0]) {
-                    // last partition of the tile: merge every partition's
-                    // partial rows (this warp's 16 rows; lanes over head dims)
-                    constexpr int DPL = D / 32;
-                    for (int rr = 0; rr < 16; ++rr) {
-                        const int rw = tile * kRows + warp * 16 + rr;
-                        if (rw >= rows) break;
-                        const int64_t orw = static_cast<int64_t>(q0 + rw / G) * H + kvh * G + rw % G;
-                        float M = kNegInf;
-                        for (int pp = 0; pp < nparts; ++pp)
-                            M = fmaxf(M, __ldcg(p.part_ml + static_cast<int64_t>(pp) * Tq * H + orw).x);
-                        float den = 0.f, acc[DPL];
-#pragma unroll
-                        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-                        for (int pp = 0; pp < nparts; ++pp) {
-                            const int64_t idx = static_cast<int64_t>(pp) * Tq * H + orw;
-                            const float2 ml = __ldcg(p.part_ml + idx);
-                            const float w = ml.x == kNegInf ? 0.f : exp2f(ml.x - M);
-                            den = fmaf(ml.y, w, den);
-                            const float *src = p.part_o + idx * D + lane * DPL;
-                            if constexpr (DPL == 4) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                                acc[0] = fmaf(v.x, w, acc[0]);
-                                acc[1] = fmaf(v.y, w, acc[1]);
-                                acc[2] = fmaf(v.z, w, acc[2]);
-                                acc[3] = fmaf(v.w, w, acc[3]);
-                            } else {
-                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                                acc[0] = fmaf(v.x, w, acc[0]);
-                                acc[1] = fmaf(v.y, w, acc[1]);
-                            }
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t c = kk >> 2, off = (kk & 3) * 32;
+                            tc::mma_ss(tmem + kTmemS + buf * 128,
+                                       tc::smem_desc(q_s + c * (kRows * 128) + off, 16, 1024,
+                                                     tc::kSwizzle128B),
+                                       tc::smem_desc(k_s + c * (kStepKeys * 128) + off, 16, 1024,
+                                                     tc::kSwizzle128B),
+                                       idesc, kk > 0);
                         }
-                        const float inv = den > 0.f ? 1.f / den : 0.f;
-                        __half *dst = p.out + orw * D + lane * DPL;
-#pragma unroll
-                        for (int i = 0; i < DPL; i += 2)
-                            *reinterpret_cast<__half2 *>(dst + i) =
-                                __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+                        tc::commit(br.s_full(buf));
+                        tc::commit(br.k_empty(ks));
+                        if (n == nsteps - 1) tc::commit(br.q_empty(slot));
                     }
+                    __syncwarp();
+                }
+                if (n > 0) {
+                    const int m = n - 1, g = gs + m, vs = g % kVStages;
+                    const int nb = min(kStepBlocks, nblk - m * kStepBlocks);
+                    ok = wait_all(br.v_full(vs), (g / kVStages) & 1);
+                    if (!ok) break;
+                    const uint32_t v_s = sb + Gm::kOffV + vs * Gm::kV;
+                    if (m == nsteps - 1) {
+                        // value rows at and past the sequence end hold anything
+                        // (their weights are 0, but 0 * NaN is not): zero them
+                        const int t0 = L - (blo + m * kStepBlocks + nb - 1) * kBS;
+                        if (t0 < kBS) {
+                            const int units = (kBS - t0) * 8;  // 16-byte units per chunk
+                            uint8_t *vb = smem + Gm::kOffV + vs * Gm::kV + (nb - 1) * Gm::kVBlock;
+                            for (int i = lane; i < units * CH; i += 32) {
+                                const int c = i / units, r = i % units;
+                                *reinterpret_cast<uint4 *>(vb + c * (kBS * 128) +
+                                                           (t0 + (r >> 3)) * 128 + (r & 7) * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                    }
+                    ok = wait_all(br.p_full(), g & 1);
+                    if (ok && m == 0 && it > 0) ok = wait_all(br.o_free(), (it - 1) & 1);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    if (lane == 0) {
+                        for (int b = 0; b < nb; ++b)
+                            tc::mma_ts(tmem + kTmemO, tmem + kTmemP + 8 * b,
+                                       tc::smem_desc(v_s + b * Gm::kVBlock, kBS * 128, 1024,
+                                                     tc::kSwizzle128B),
+                                       kIdescPV, (m > 0 || b > 0) ? 1u : 0u);
+                        tc::commit(br.pv_done());
+                        tc::commit(br.v_empty(vs));
+                    }
+                    __syncwarp();
                 }
             }
+            gs += nsteps;
         }
-        gstep += nsteps;
-        __syncthreads();  // the item is done: bt_s and misc are free again
+        if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+    } else {
+        // =============================== softmax ===============================
+        // one thread per query row; a warp reaches tensor-memory lanes
+        // 32 * (warp % 4) ...
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int64_t Tq = p.num_query_tokens;
+        const float sl2 = p.scale_log2;
+        int gs = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            const int slot = it & 1;
+            if (!wait_all(br.q_full(slot), (it >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const ItemInfo &in = info[slot];
+            const int done = in.done, seq = in.seq, part = in.part, kvh = in.kvh, tile = in.tile;
+            const int nsteps = in.nsteps, nblk = in.nblk, L = in.L, Q = in.Q, q0 = in.q0;
+            const int nparts = in.nparts;
+            uint32_t valid[kPartBlocks / 32];
+#pragma unroll
+            for (int w = 0; w < kPartBlocks / 32; ++w) valid[w] = in.valid[w];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(br.q_empty(slot));
+            if (done) break;
+            const int rows = Q * G;
+            const int rr = tile * kRows + r;
+            const bool row_ok = rr < rows;
+            const int j = rr >> logG;
+            const int lim = row_ok ? L - Q + j : -1;  // last key position this row sees
+            const int64_t orow = static_cast<int64_t>(q0 + j) * H + kvh * G + (rr & (G - 1));
+            float m_used = kNegInf, l = 0.f;
+
+            for (int n = 0; n < nsteps; ++n) {
+                const int g = gs + n, buf = g & 1;
+                if (!wait_all(br.s_full(buf), (g >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                float t[kStepKeys];
+                {
+                    uint32_t x[32];
+#pragma unroll
+                    for (int c = 0; c < kStepKeys / 32; ++c) {
+                        tc::ld32(tl + kTmemS + buf * 128 + 32 * c, x);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) t[32 * c + e] = __uint_as_float(x[e]);
+                    }
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(br.s_free(buf));
+                const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
+                const int kbase = part * kPartTokens + n * kStepKeys;
+                const int b0 = n * kStepBlocks;
+                const uint32_t vmask = (valid[b0 >> 5] >> (b0 & 31)) & 0xFFu;
+                float mx = kNegInf;
+                if (nb == kStepBlocks && vmask == 0xFFu && kbase + kStepKeys - 1 <= lim) {
+#pragma unroll
+                    for (int e = 0; e < kStepKeys; ++e) {
+                        t[e] *= sl2;
+                        mx = fmaxf(mx, t[e]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kStepKeys; ++e) {
+                        const bool vis = e < nb * kBS && ((vmask >> (e >> 4)) & 1u) && kbase + e <= lim;
+                        t[e] = vis ? t[e] * sl2 : kNegInf;
+                        mx = fmaxf(mx, t[e]);
+                    }
+                }
+                const float m_new = fmaxf(m_used, mx);
+                const bool raise = m_new > m_used + kRescaleLog2;
+                // O holds this item's earlier steps (relative to m_used):
+                // rescale it before the reference moves
+                const bool resc = raise && n > 0 && m_used != kNegInf;
+                if (g > 0) {
+                    // the previous P V must be done: before O is touched and
+                    // before its weights are overwritten
+                    if (!wait_all(br.pv_done(), (g - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                }
+                if (__any_sync(0xffffffffu, resc)) {
+                    const float alpha = resc ? ex2(m_used - m_new) : 1.f;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t x[32];
+                        tc::ld32(tl + kTmemO + 32 * c, x);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
+                        tc::st32(tl + kTmemO + 32 * c, x);
+                    }
+                    tc::wait_st();
+                    l *= alpha;
+                }
+                if (raise) m_used = m_new;
+                const float ms = m_used == kNegInf ? 0.f : m_used;
+                // weights, fp16 pairs: column i holds keys 2i, 2i+1
+#pragma unroll
+                for (int c = 0; c < kStepKeys / 64; ++c) {
+                    uint32_t x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = ex2(t[64 * c + 2 * e] - ms);
+                        const float p1 = ex2(t[64 * c + 2 * e + 1] - ms);
+                        l += p0 + p1;
+                        x[e] = pack_half2(p0, p1);
+                    }
+                    tc::st32(tl + kTmemP + 32 * c, x);
+                }
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(br.p_full());
+            }
+            if (!ok) break;
+            gs += nsteps;
+
+            // ---- the item's output: O / l, or the partial state (m, l, O)
+            if (!wait_all(br.pv_done(), (gs - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            float o[D];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t x[32];
+                tc::ld32(tl + kTmemO + 32 * c, x);
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[32 * c + e] = __uint_as_float(x[e]);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(br.o_free());
+            if (nparts == 1) {
+                if (row_ok) {
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c)
+                        dst[c] = make_uint4(pack_half2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                            pack_half2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                            pack_half2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                            pack_half2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+                }
+                continue;
+            }
+            if (row_ok) {
+                const int64_t idx = static_cast<int64_t>(part) * Tq * H + orow;
+                p.part_ml[idx] = make_float2(m_used, l);
+                float4 *dst = reinterpret_cast<float4 *>(p.part_o + idx * D);
+#pragma unroll
+                for (int c = 0; c < D / 4; ++c)
+                    dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            }
+            // a ticket per (sequence, kv head, tile, warp): the warp that
+            // brings the last partition of its 32 rows merges them
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                int *ticket = p.counters +
+                              ((static_cast<int64_t>(seq) * Hk + kvh) * p.num_tiles + tile) * 4 +
+                              quarter;
+                last = atomicAdd(ticket, 1) == nparts - 1;
+                if (last) {
+                    atomicExch(ticket, 0);  // leave the workspace zeroed
+                    __threadfence();
+                }
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last || !row_ok) continue;
+            // the tile's last partition: merge every partition's partial row
+            float M = kNegInf;
+            for (int pp = 0; pp < nparts; ++pp)
+                M = fmaxf(M, __ldcg(p.part_ml + static_cast<int64_t>(pp) * Tq * H + orow).x);
+            float den = 0.f;
+#pragma unroll
+            for (int e = 0; e < D; ++e) o[e] = 0.f;
+            for (int pp = 0; pp < nparts; ++pp) {
+                const int64_t idx = static_cast<int64_t>(pp) * Tq * H + orow;
+                const float2 ml = __ldcg(p.part_ml + idx);
+                const float w = ml.x == kNegInf ? 0.f : ex2(ml.x - M);
+                den = fmaf(ml.y, w, den);
+                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + idx * D);
+#pragma unroll
+                for (int c = 0; c < D / 4; ++c) {
+                    const float4 v = __ldcg(src + c);
+                    o[4 * c] = fmaf(v.x, w, o[4 * c]);
+                    o[4 * c + 1] = fmaf(v.y, w, o[4 * c + 1]);
+                    o[4 * c + 2] = fmaf(v.z, w, o[4 * c + 2]);
+                    o[4 * c + 3] = fmaf(v.w, w, o[4 * c + 3]);
+                }
+            }
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c)
+                dst[c] = make_uint4(pack_half2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                    pack_half2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                    pack_half2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                    pack_half2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+        }
+        if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
     }
-    // (every issued copy was waited for by the consumers, unless a wait gave
-    // up; then let the copies of the last ring turn land before exiting)
-    if (warp == kWarps && misc[1]) {
-        for (int st = 0; st < kStages && st < gstep; ++st) {
-            const int last_use = gstep - 1 - ((gstep - 1 - st) % kStages);
-            mbar_wait_bounded(full_s + st * 8, (last_use / kStages) & 1);
-        }
+
+    // every role is done: hand the tensor memory back
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 using ChunkFn = void (*)(const ChunkParams);
 
-ChunkFn select(int D, int G) {
-#define PKV_CASE(d, g) \
-    if (D == d && G == g) return chunk_attention_kernel<d, g>;
-    PKV_CASE(128, 1) PKV_CASE(128, 2) PKV_CASE(128, 4) PKV_CASE(128, 8)
-    PKV_CASE(64, 1) PKV_CASE(64, 2) PKV_CASE(64, 4) PKV_CASE(64, 8)
-#undef PKV_CASE
+ChunkFn select(int D) {
+    if (D == 128) return chunk_attention_kernel<128>;
+    if (D == 64) return chunk_attention_kernel<64>;
     return nullptr;
 }
 
@@ -648,7 +842,7 @@ Sizes sizes(int64_t S, int64_t H, int64_t Hk, int64_t D, int64_t Tq, int64_t max
     const int64_t G = H / Hk;
     z.tiles = std::max<int64_t>(1, (max_q * G + kRows - 1) / kRows);
     z.parts = std::max<int64_t>(1, (max_len + kPartTokens - 1) / kPartTokens);
-    z.counters_bytes = dec::align256(S * Hk * z.tiles * 4);
+    z.counters_bytes = dec::align256(S * Hk * z.tiles * 4 * 4);  // a ticket per softmax warp
     z.list_bytes = dec::align256((2 * S + 3) * 4);  // big_seq, big_cum, n_big, work
     z.ml_bytes = z.parts > 1 ? dec::align256(z.parts * Tq * H * 8) : 0;
     z.o_bytes = z.parts > 1 ? z.parts * Tq * H * D * 4 : 0;
@@ -720,7 +914,7 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     const int64_t need = z.bal_bytes + z.list_bytes + z.counters_bytes + z.ml_bytes + z.o_bytes;
     if (workspace == nullptr || static_cast<int64_t>(workspace_bytes) < need)
         return PKV_ERR_WORKSPACE;
-    ChunkFn fn = select(head_dim, G);
+    ChunkFn fn = select(head_dim);
     if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -794,10 +988,14 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     p.part_ml = reinterpret_cast<float2 *>(cws + z.counters_bytes);
     p.part_o = reinterpret_cast<float *>(cws + z.counters_bytes + z.ml_bytes);
     {
-        // per-head boxes: kv_head's head_dim*2 bytes are whole 128-byte chunks
-        const int box = head_dim * 2 / dec::chunk_bytes_for_row(row_bytes);
-        int st = dec::make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, row_bytes, box);
-        if (st == PKV_OK) st = dec::make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, row_bytes, box);
+        // keys: one 128-byte chunk per copy; values: the head's chunks (a
+        // head's head_dim * 2 bytes are whole 128-byte chunks); query rows
+        const int chunks = head_dim * 2 / 128;
+        int st = dec::make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, row_bytes, 1);
+        if (st == PKV_OK)
+            st = dec::make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, row_bytes, chunks);
+        if (st == PKV_OK)
+            st = dec::make_q_tensor_map(&p.tm_q, q, num_query_tokens, num_heads, head_dim, G);
         if (st != PKV_OK) return st;
     }
     p.err = device_error_record();

@@ -36,6 +36,14 @@ __host__ __device__ constexpr int chunk_bytes_for_row(int row_bytes) {
 int make_kv_tensor_map(CUtensorMap *map, const void *cache, int64_t num_blocks, int row_bytes,
                        int box_chunks);
 
+// Tensor map over query rows fp16 [num_tokens][num_heads][head_dim] viewed
+// as {head_dim * 2 bytes, heads, tokens}, with a box of {128 bytes, group
+// heads, 128 / group tokens} and the 128-byte swizzle: a box at (128 c,
+// kv_head * group, token t) lands as 128 rows (token-major, head-minor) of
+// the bytes 128 c .. 128 c + 127 of each head.  Returns a PKV status.
+int make_q_tensor_map(CUtensorMap *map, const void *q, int64_t num_tokens, int num_heads,
+                      int head_dim, int group);
+
 // Grid schedule.
 struct GridParams {
     CUtensorMap tm_k;  // per-head boxes of the key / value caches
