@@ -69,7 +69,7 @@ constexpr int kPartBlocks = kPartTokens / kBS;
 constexpr int kSoftmaxWarps = 4;               // one thread per query row
 constexpr int kThreads = (3 + kSoftmaxWarps) * 32;
 // tensor memory: O in columns [0, head_dim), scores in two buffers of 128
-// columns, weights (fp16 pairs) in 64 columns
+// columns, weights (fp16 pairs) in two buffers of 64 columns
 constexpr int kTmemCols = 512;
 constexpr int kTmemO = 0;
 constexpr int kTmemS = 128;
@@ -104,8 +104,10 @@ struct ChunkParams {
     int *work;
     int64_t num_blocks;
     int *counters;    // [S][Hk][num_tiles] tickets, zero between calls
-    float2 *part_ml;  // [parts][Tq][H] (m, l)
-    float *part_o;    // [parts][Tq][H][D]
+    // partial states, row index R = kv_head * Tq * G + query_start * G + tile
+    // row (the rows of a warp are consecutive): ml [parts][R], O [parts][D][R]
+    float2 *part_ml;
+    float *part_o;
     ErrorRecord *err;
 };
 
@@ -129,7 +131,7 @@ struct Geo {
     static constexpr int kOffK = 2 * kQ;
     static constexpr int kOffV = kOffK + kKStages * kK;
     static constexpr int kOffBar = kOffV + kVStages * kV;
-    static constexpr int kBars = 2 + 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 3;
+    static constexpr int kBars = 2 + 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 1;
     static constexpr int kOffInfo = kOffBar + kBars * 8;
     static constexpr int kOffMisc = kOffInfo + 2 * static_cast<int>(sizeof(ItemInfo));
     static constexpr int kBytes = kOffMisc + 16;
@@ -152,9 +154,11 @@ struct Bars {
     __device__ uint32_t s_free(int s) const {
         return b + 8 * (6 + 2 * kKStages + 2 * kVStages + s);
     }
-    __device__ uint32_t p_full() const { return b + 8 * (8 + 2 * kKStages + 2 * kVStages); }
-    __device__ uint32_t pv_done() const { return b + 8 * (9 + 2 * kKStages + 2 * kVStages); }
-    __device__ uint32_t o_free() const { return b + 8 * (10 + 2 * kKStages + 2 * kVStages); }
+    __device__ uint32_t p_full(int s) const { return b + 8 * (8 + 2 * kKStages + 2 * kVStages + s); }
+    __device__ uint32_t pv_done(int s) const {
+        return b + 8 * (10 + 2 * kKStages + 2 * kVStages + s);
+    }
+    __device__ uint32_t o_free() const { return b + 8 * (12 + 2 * kKStages + 2 * kVStages); }
 };
 
 // arrivals that complete a phase of each barrier
@@ -325,6 +329,51 @@ __device__ __forceinline__ int3 decode_item(const SeqGeo &sg, int local, int G, 
     return make_int3(-1, -1, -1);
 }
 
+// An item as the key producer takes it from the list (every lane holds the
+// scalars; block ids are spread over the lanes).
+struct Fetched {
+    int done, seq, part, kvh, tile, nsteps, nblk, L, Q, q0, nparts;
+    int ids[kPartBlocks / 32];
+    uint32_t valid[kPartBlocks / 32];
+};
+
+__device__ __forceinline__ void fetch_item(const ChunkParams &p, int n_big, int total, int G,
+                                           int logG, int lane, Fetched &f) {
+    int item = 0;
+    if (lane == 0) item = atomicAdd(p.work, 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    f.done = item >= total;
+    if (f.done) return;
+    // the listed sequence holding the item (every lane searches alike)
+    int lo = 0, hi = n_big - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldcg(p.big_cum + mid) <= item) lo = mid;
+        else hi = mid - 1;
+    }
+    const int seq = __ldcg(p.big_seq + lo);
+    SeqGeo sg;
+    seq_geo(p, seq, G, false, sg);  // (the plan listed it: valid)
+    const int3 d = decode_item(sg, item - __ldcg(p.big_cum + lo), G, p.num_kv_heads);
+    const int j_last = (min(sg.rows, (d.z + 1) * kRows) - 1) >> logG;
+    const int kv_end = sg.L - sg.Q + j_last + 1;  // keys [0, kv_end) for the tile
+    const int k1 = min(kv_end, (d.x + 1) * kPartTokens);
+    const int blo = d.x * kPartBlocks;
+    f.seq = seq;
+    f.part = d.x;
+    f.kvh = d.y;
+    f.tile = d.z;
+    f.nblk = (k1 + kBS - 1) / kBS - blo;  // >= 1
+    f.nsteps = (f.nblk + kStepBlocks - 1) / kStepBlocks;
+    f.L = sg.L;
+    f.Q = sg.Q;
+    f.q0 = sg.q0;
+    f.nparts = (kv_end + kPartTokens - 1) / kPartTokens;
+    load_ids(p, seq, blo, f.nblk, lane, true, f.ids);
+#pragma unroll
+    for (int w = 0; w < kPartBlocks / 32; ++w) f.valid[w] = __ballot_sync(0xffffffffu, f.ids[w] >= 0);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_attention_kernel(const __grid_constant__ ChunkParams p) {
@@ -348,6 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(br.q_empty(s), kQEmptyArrivals);
             mbar_init(br.s_full(s), 1);
             mbar_init(br.s_free(s), kSoftmaxWarps);
+            mbar_init(br.p_full(s), kSoftmaxWarps);
+            mbar_init(br.pv_done(s), 1);
         }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(br.k_full(s), 1);
@@ -357,8 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(br.v_full(s), 1);
             mbar_init(br.v_empty(s), 1);
         }
-        mbar_init(br.p_full(), kSoftmaxWarps);
-        mbar_init(br.pv_done(), 1);
         mbar_init(br.o_free(), kSoftmaxWarps);
         fence_mbarrier_init();
     }
@@ -380,85 +429,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int total = __ldcg(p.big_cum + n_big);
         int gs = 0;  // steps staged
         bool ok = true;
+        Fetched cur;
+        fetch_item(p, n_big, total, G, logG, lane, cur);
         for (int it = 0; ok; ++it) {
-            int item = 0;
-            if (lane == 0) item = atomicAdd(p.work, 1);
-            item = __shfl_sync(0xffffffffu, item, 0);
             const int slot = it & 1;
             if (it >= 2 && !wait_all(br.q_empty(slot), ((it >> 1) - 1) & 1)) {
                 ok = false;
                 break;
             }
-            if (item >= total) {
+            if (cur.done) {
                 if (lane == 0) {
                     info[slot].done = 1;
                     mbar_arrive(br.q_full(slot));
                 }
                 break;
             }
-            // the listed sequence holding the item (every lane searches alike)
-            int lo = 0, hi = n_big - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldcg(p.big_cum + mid) <= item) lo = mid;
-                else hi = mid - 1;
-            }
-            const int seq = __ldcg(p.big_seq + lo);
-            SeqGeo sg;
-            seq_geo(p, seq, G, false, sg);  // (the plan listed it: valid)
-            const int3 d = decode_item(sg, item - __ldcg(p.big_cum + lo), G, Hk);
-            const int part = d.x, kvh = d.y, tile = d.z;
-            const int j_last = (min(sg.rows, (tile + 1) * kRows) - 1) >> logG;
-            const int kv_end = sg.L - sg.Q + j_last + 1;  // keys [0, kv_end) for the tile
-            const int k1 = min(kv_end, (part + 1) * kPartTokens);
-            const int blo = part * kPartBlocks;
-            const int nblk = (k1 + kBS - 1) / kBS - blo;  // >= 1
-            const int nsteps = (nblk + kStepBlocks - 1) / kStepBlocks;
-            int ids[kPartBlocks / 32];
-            load_ids(p, seq, blo, nblk, lane, true, ids);
-            uint32_t valid[kPartBlocks / 32];
-#pragma unroll
-            for (int w = 0; w < kPartBlocks / 32; ++w) valid[w] = __ballot_sync(0xffffffffu, ids[w] >= 0);
             if (lane == 0) {
                 ItemInfo &in = info[slot];
-                in.seq = seq;
-                in.part = part;
-                in.kvh = kvh;
-                in.tile = tile;
-                in.nsteps = nsteps;
-                in.nblk = nblk;
-                in.L = sg.L;
-                in.Q = sg.Q;
-                in.q0 = sg.q0;
-                in.nparts = (kv_end + kPartTokens - 1) / kPartTokens;
+                in.seq = cur.seq;
+                in.part = cur.part;
+                in.kvh = cur.kvh;
+                in.tile = cur.tile;
+                in.nsteps = cur.nsteps;
+                in.nblk = cur.nblk;
+                in.L = cur.L;
+                in.Q = cur.Q;
+                in.q0 = cur.q0;
+                in.nparts = cur.nparts;
                 in.done = 0;
 #pragma unroll
-                for (int w = 0; w < kPartBlocks / 32; ++w) in.valid[w] = valid[w];
+                for (int w = 0; w < kPartBlocks / 32; ++w) in.valid[w] = cur.valid[w];
                 mbar_arrive_expect_tx(br.q_full(slot), Gm::kQ);
             }
             __syncwarp();
             if (lane < CH)
                 tensor_g2s_3d(sb + slot * Gm::kQ + lane * (kRows * 128), &p.tm_q, 128 * lane,
-                              kvh * G, sg.q0 + tile * (kRows >> logG), br.q_full(slot));
-            for (int n = 0; n < nsteps; ++n, ++gs) {
+                              cur.kvh * G, cur.q0 + cur.tile * (kRows >> logG), br.q_full(slot));
+            // the next item is taken once this one's first steps are staged
+            // (its lookups then overlap this item's work)
+            Fetched nxt;
+            nxt.done = 1;
+            const int fetch_at = min(cur.nsteps, kKStages) - 1;
+            for (int n = 0; n < cur.nsteps; ++n, ++gs) {
                 const int ks = gs % kKStages;
                 if (gs >= kKStages && !wait_all(br.k_empty(ks), ((gs / kKStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
+                const int nb = min(kStepBlocks, cur.nblk - n * kStepBlocks);
                 if (lane == 0) mbar_arrive_expect_tx(br.k_full(ks), nb * CH * kBS * 128);
                 __syncwarp();
                 // lane l: block l / CH of the step, chunk l % CH (a bad block
                 // reads rows before the cache: zeros)
                 const int b = min(lane / CH, kStepBlocks - 1), c = lane % CH;
-                const int id = id_of(ids, n * kStepBlocks + b);
+                const int id = id_of(cur.ids, n * kStepBlocks + b);
                 if (lane < nb * CH)
                     tensor_g2s_3d(sb + Gm::kOffK + ks * Gm::kK + c * (kStepKeys * 128) +
                                       b * (kBS * 128),
-                                  &p.tm_k, 0, id >= 0 ? id * kBS : -kBS, kvh * CH + c,
+                                  &p.tm_k, 0, id >= 0 ? id * kBS : -kBS, cur.kvh * CH + c,
                                   br.k_full(ks));
+                if (n == fetch_at) fetch_item(p, n_big, total, G, logG, lane, nxt);
             }
+            cur = nxt;
         }
         if (!ok) {
             if (lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
@@ -534,18 +566,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc::fence_after_sync();
                     if (lane == 0) {
+                        // two accumulators of up to 64 keys each, their k steps
+                        // interleaved (one chain of dependent MMAs would wait
+                        // on each other's results)
                         const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
-                        const uint32_t idesc = tc::idesc_f16_f32(kRows, nb * kBS, false, false);
+                        const int nlo = min(nb, kStepBlocks / 2), nhi = nb - nlo;
+                        const uint32_t id_lo = tc::idesc_f16_f32(kRows, nlo * kBS, false, false);
+                        const uint32_t id_hi =
+                            tc::idesc_f16_f32(kRows, (nhi > 0 ? nhi : 1) * kBS, false, false);
                         const uint32_t k_s = sb + Gm::kOffK + ks * Gm::kK;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-                            tc::mma_ss(tmem + kTmemS + buf * 128,
-                                       tc::smem_desc(q_s + c * (kRows * 128) + off, 16, 1024,
-                                                     tc::kSwizzle128B),
-                                       tc::smem_desc(k_s + c * (kStepKeys * 128) + off, 16, 1024,
-                                                     tc::kSwizzle128B),
-                                       idesc, kk > 0);
+                            const uint64_t a = tc::smem_desc(q_s + c * (kRows * 128) + off, 16,
+                                                             1024, tc::kSwizzle128B);
+                            const uint32_t kc = k_s + c * (kStepKeys * 128) + off;
+                            tc::mma_ss(tmem + kTmemS + buf * 128, a,
+                                       tc::smem_desc(kc, 16, 1024, tc::kSwizzle128B), id_lo,
+                                       kk > 0);
+                            if (nhi > 0)
+                                tc::mma_ss(tmem + kTmemS + buf * 128 + kStepKeys / 2, a,
+                                           tc::smem_desc(kc + (kStepKeys / 2) * 128, 16, 1024,
+                                                         tc::kSwizzle128B),
+                                           id_hi, kk > 0);
                         }
                         tc::commit(br.s_full(buf));
                         tc::commit(br.k_empty(ks));
@@ -576,17 +619,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __syncwarp();
                         }
                     }
-                    ok = wait_all(br.p_full(), g & 1);
+                    ok = wait_all(br.p_full(g & 1), (g >> 1) & 1);
                     if (ok && m == 0 && it > 0) ok = wait_all(br.o_free(), (it - 1) & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
                     if (lane == 0) {
                         for (int b = 0; b < nb; ++b)
-                            tc::mma_ts(tmem + kTmemO, tmem + kTmemP + 8 * b,
+                            tc::mma_ts(tmem + kTmemO, tmem + kTmemP + 64 * (g & 1) + 8 * b,
                                        tc::smem_desc(v_s + b * Gm::kVBlock, kBS * 128, 1024,
                                                      tc::kSwizzle128B),
                                        kIdescPV, (m > 0 || b > 0) ? 1u : 0u);
-                        tc::commit(br.pv_done());
+                        tc::commit(br.pv_done(g & 1));
                         tc::commit(br.v_empty(vs));
                     }
                     __syncwarp();
@@ -637,17 +680,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc::fence_after_sync();
-                float t[kStepKeys];
-                {
-                    uint32_t x[32];
+                uint32_t sx[kStepKeys];  // this row's scores (fp32 bits)
 #pragma unroll
-                    for (int c = 0; c < kStepKeys / 32; ++c) {
-                        tc::ld32(tl + kTmemS + buf * 128 + 32 * c, x);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) t[32 * c + e] = __uint_as_float(x[e]);
-                    }
-                }
+                for (int c = 0; c < kStepKeys / 32; ++c)
+                    tc::ld32(tl + kTmemS + buf * 128 + 32 * c,
+                             *reinterpret_cast<uint32_t(*)[32]>(sx + 32 * c));
+                tc::wait_ld();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(br.s_free(buf));
@@ -655,36 +693,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kbase = part * kPartTokens + n * kStepKeys;
                 const int b0 = n * kStepBlocks;
                 const uint32_t vmask = (valid[b0 >> 5] >> (b0 & 31)) & 0xFFu;
-                float mx = kNegInf;
-                if (nb == kStepBlocks && vmask == 0xFFu && kbase + kStepKeys - 1 <= lim) {
+                // every key visible (and a non-negative scale): the maximum of
+                // the raw scores, scaled once; else scale and mask each score
+                const bool fast = nb == kStepBlocks && vmask == 0xFFu &&
+                                  kbase + kStepKeys - 1 <= lim && sl2 >= 0.f;
+                float mr[8];
 #pragma unroll
-                    for (int e = 0; e < kStepKeys; ++e) {
-                        t[e] *= sl2;
-                        mx = fmaxf(mx, t[e]);
-                    }
+                for (int i = 0; i < 8; ++i) mr[i] = kNegInf;
+                if (fast) {
+#pragma unroll
+                    for (int e = 0; e < kStepKeys; ++e) mr[e & 7] = fmaxf(mr[e & 7], __uint_as_float(sx[e]));
                 } else {
 #pragma unroll
                     for (int e = 0; e < kStepKeys; ++e) {
-                        const bool vis = e < nb * kBS && ((vmask >> (e >> 4)) & 1u) && kbase + e <= lim;
-                        t[e] = vis ? t[e] * sl2 : kNegInf;
-                        mx = fmaxf(mx, t[e]);
+                        const bool vis =
+                            e < nb * kBS && ((vmask >> (e >> 4)) & 1u) && kbase + e <= lim;
+                        const float t = vis ? __uint_as_float(sx[e]) * sl2 : kNegInf;
+                        sx[e] = __float_as_uint(t);
+                        mr[e & 7] = fmaxf(mr[e & 7], t);
                     }
                 }
+                float mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])),
+                                 fmaxf(fmaxf(mr[4], mr[5]), fmaxf(mr[6], mr[7])));
+                if (fast) mx *= sl2;
                 const float m_new = fmaxf(m_used, mx);
                 const bool raise = m_new > m_used + kRescaleLog2;
-                // O holds this item's earlier steps (relative to m_used):
-                // rescale it before the reference moves
+                // O holds this item's earlier steps relative to m_used: rescale
+                // it before the reference moves (the previous P V done first)
                 const bool resc = raise && n > 0 && m_used != kNegInf;
-                if (g > 0) {
-                    // the previous P V must be done: before O is touched and
-                    // before its weights are overwritten
-                    if (!wait_all(br.pv_done(), (g - 1) & 1)) {
+                if (__any_sync(0xffffffffu, resc)) {
+                    if (!wait_all(br.pv_done((g - 1) & 1), ((g - 1) >> 1) & 1)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                }
-                if (__any_sync(0xffffffffu, resc)) {
                     const float alpha = resc ? ex2(m_used - m_new) : 1.f;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -701,41 +743,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (raise) m_used = m_new;
                 const float ms = m_used == kNegInf ? 0.f : m_used;
-                // weights, fp16 pairs: column i holds keys 2i, 2i+1
+                // weights 2^(s * scale - m) (2^(t - m) for the masked scores),
+                // fp16 pairs: column i of the buffer holds keys 2i, 2i+1; the
+                // P V of two steps back must be done with this buffer
+                const float a = fast ? sl2 : 1.f;
+                const int pb = g & 1;
+                if (g >= 2) {
+                    if (!wait_all(br.pv_done(pb), ((g - 2) >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                }
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < kStepKeys / 64; ++c) {
                     uint32_t x[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = ex2(t[64 * c + 2 * e] - ms);
-                        const float p1 = ex2(t[64 * c + 2 * e + 1] - ms);
-                        l += p0 + p1;
+                        const float p0 = ex2(fmaf(__uint_as_float(sx[64 * c + 2 * e]), a, -ms));
+                        const float p1 = ex2(fmaf(__uint_as_float(sx[64 * c + 2 * e + 1]), a, -ms));
+                        l4[e & 3] += p0 + p1;
                         x[e] = pack_half2(p0, p1);
                     }
-                    tc::st32(tl + kTmemP + 32 * c, x);
+                    tc::st32(tl + kTmemP + 64 * pb + 32 * c, x);
                 }
+                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(br.p_full());
+                if (lane == 0) mbar_arrive(br.p_full(pb));
             }
             if (!ok) break;
             gs += nsteps;
 
             // ---- the item's output: O / l, or the partial state (m, l, O)
-            if (!wait_all(br.pv_done(), (gs - 1) & 1)) {
+            if (!wait_all(br.pv_done((gs - 1) & 1), ((gs - 1) >> 1) & 1)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             float o[D];
+            {
+                uint32_t ob[D];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t x[32];
-                tc::ld32(tl + kTmemO + 32 * c, x);
+                for (int c = 0; c < D / 32; ++c)
+                    tc::ld32(tl + kTmemO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(ob + 32 * c));
                 tc::wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[32 * c + e] = __uint_as_float(x[e]);
+                for (int d = 0; d < D; ++d) o[d] = __uint_as_float(ob[d]);
             }
             tc::fence_before_sync();
             __syncwarp();
@@ -753,13 +809,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
+            // partial state, dimension-major so a warp's 32 rows are
+            // consecutive words (coalesced)
+            const int64_t NR = Tq * H;
+            const int64_t R = static_cast<int64_t>(kvh) * Tq * G + static_cast<int64_t>(q0) * G + rr;
             if (row_ok) {
-                const int64_t idx = static_cast<int64_t>(part) * Tq * H + orow;
-                p.part_ml[idx] = make_float2(m_used, l);
-                float4 *dst = reinterpret_cast<float4 *>(p.part_o + idx * D);
+                p.part_ml[part * NR + R] = make_float2(m_used, l);
+                float *dst = p.part_o + static_cast<int64_t>(part) * D * NR + R;
 #pragma unroll
-                for (int c = 0; c < D / 4; ++c)
-                    dst[c] = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                for (int d = 0; d < D; ++d) dst[d * NR] = o[d];
             }
             // a ticket per (sequence, kv head, tile, warp): the warp that
             // brings the last partition of its 32 rows merges them
@@ -780,25 +838,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!last || !row_ok) continue;
             // the tile's last partition: merge every partition's partial row
             float M = kNegInf;
-            for (int pp = 0; pp < nparts; ++pp)
-                M = fmaxf(M, __ldcg(p.part_ml + static_cast<int64_t>(pp) * Tq * H + orow).x);
+            for (int pp = 0; pp < nparts; ++pp) M = fmaxf(M, __ldcg(p.part_ml + pp * NR + R).x);
             float den = 0.f;
 #pragma unroll
-            for (int e = 0; e < D; ++e) o[e] = 0.f;
+            for (int d = 0; d < D; ++d) o[d] = 0.f;
             for (int pp = 0; pp < nparts; ++pp) {
-                const int64_t idx = static_cast<int64_t>(pp) * Tq * H + orow;
-                const float2 ml = __ldcg(p.part_ml + idx);
+                const float2 ml = __ldcg(p.part_ml + pp * NR + R);
                 const float w = ml.x == kNegInf ? 0.f : ex2(ml.x - M);
                 den = fmaf(ml.y, w, den);
-                const float4 *src = reinterpret_cast<const float4 *>(p.part_o + idx * D);
+                const float *src = p.part_o + static_cast<int64_t>(pp) * D * NR + R;
 #pragma unroll
-                for (int c = 0; c < D / 4; ++c) {
-                    const float4 v = __ldcg(src + c);
-                    o[4 * c] = fmaf(v.x, w, o[4 * c]);
-                    o[4 * c + 1] = fmaf(v.y, w, o[4 * c + 1]);
-                    o[4 * c + 2] = fmaf(v.z, w, o[4 * c + 2]);
-                    o[4 * c + 3] = fmaf(v.w, w, o[4 * c + 3]);
-                }
+                for (int d = 0; d < D; ++d) o[d] = fmaf(__ldcg(src + d * NR), w, o[d]);
             }
             const float inv = den > 0.f ? 1.f / den : 0.f;
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
