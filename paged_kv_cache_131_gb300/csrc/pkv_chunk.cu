@@ -18,25 +18,31 @@
 // group): row = j*G + g, so a tile covers 128/G consecutive new tokens.
 //
 // Per CTA, warp-specialised, all hand-offs through mbarriers:
-//  * warp 0 takes the items, stages the tile's query rows (two tiles in
-//    flight) and the partition's keys, 8 blocks (128 keys) per step, one
-//    tensor copy per block and 64-dimension chunk, into a 3-step ring laid
-//    out [chunk][key][128 B] so the 128 keys form one MMA operand;
+//  * warp 0 takes the items (the next one while the current one is staged),
+//    stages the tile's query rows into shared memory and the partition's
+//    keys, 8 blocks (128 keys) per step, one tensor copy per block and
+//    64-dimension chunk, into a 3-step ring laid out [chunk][key][128 B] so
+//    the 128 keys form one MMA operand;
 //  * warp 1 stages the values, one tensor copy per block, into a 2-step ring;
-//  * warp 2 issues the MMAs (one thread): S = Q K^T (M = 128 rows, N = 128
-//    keys) into one of two 128-column score buffers in tensor memory, and
-//    O += P V (N = head_dim, 16 keys per MMA) with P read from tensor memory;
-//  * warps 3-6 run the softmax, one thread per query row: they read the
-//    row's scores, mask keys past the row's position (and past the sequence
-//    or in a bad block), keep the row's running maximum m and sum l in the
-//    log2 domain and write the fp16 weights P = 2^(s - m) back to tensor
-//    memory.  The reference m moves only when the maximum grows by more
-//    than 2^8 (the weights stay <= 256): then O is rescaled in tensor memory
-//    first.  The result O / l does not depend on which reference was used.
+//  * warp 2 issues the tensor-core work (one thread): it copies the query
+//    tile into tensor memory (two tiles in flight), then per step S = Q K^T
+//    (M = 128 rows, N = 128 keys, A read from tensor memory) into a
+//    128-column score buffer, and O += P V (N = head_dim, 16 keys per MMA)
+//    with the weights P read from tensor memory (two buffers);
+//  * warps 3-10 run the softmax, one thread per query row and half of each
+//    step's keys per group of four warps: they read the row's scores, mask
+//    keys past the row's position (and past the sequence or in a bad
+//    block), exchange the half-row maxima with the other group's thread of
+//    the row, keep the row's running maximum m and the sums l in the log2
+//    domain and write the fp16 weights P = 2^(s - m) back to tensor memory.
+//    The reference m moves only when the maximum grows by more than 2^8
+//    (the weights stay <= 256): then each group rescales its half of O in
+//    tensor memory first.  The result O / l does not depend on which
+//    reference was used.
 // A tile whose causal range fits one partition writes fp16 out; otherwise
-// every partition leaves fp32 partial states (m, l, O) and the last CTA of
-// the tile to take a ticket merges them with a log-sum-exp rescale.  No CTA
-// waits for another.
+// every partition leaves fp32 partial states (m, l, O) and, per softmax warp,
+// the last CTA of the tile to take a ticket merges them with a log-sum-exp
+// rescale.  No CTA waits for another.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -66,14 +72,19 @@ constexpr int kKStages = 3;                    // key ring depth (steps)
 constexpr int kVStages = 2;                    // value ring depth (steps)
 constexpr int kPartTokens = 2048;              // KV partition
 constexpr int kPartBlocks = kPartTokens / kBS;
-constexpr int kSoftmaxWarps = 4;               // one thread per query row
+// softmax: two groups of four warps; warp (3 + 4 grp + q) takes row quarter
+// q (tensor-memory lanes 32 q ..) and keys 64 grp .. 64 grp + 63 of a step
+constexpr int kSoftmaxWarps = 8;
+constexpr int kGroupKeys = kStepKeys / 2;
 constexpr int kThreads = (3 + kSoftmaxWarps) * 32;
-// tensor memory: O in columns [0, head_dim), scores in two buffers of 128
-// columns, weights (fp16 pairs) in two buffers of 64 columns
+// tensor memory: O in columns [0, head_dim), the scores in [128, 256), the
+// weights (fp16 pairs) in two buffers of 64 columns, the query tile (fp16
+// pairs, copied from shared memory) in two buffers of 64 columns
 constexpr int kTmemCols = 512;
 constexpr int kTmemO = 0;
 constexpr int kTmemS = 128;
-constexpr int kTmemP = 384;
+constexpr int kTmemP = 256;
+constexpr int kTmemQ = 384;
 constexpr float kRescaleLog2 = 8.f;            // move the reference past 2^8
 
 struct ChunkParams {
@@ -92,6 +103,7 @@ struct ChunkParams {
     int max_query_len;
     int max_seq_len;
     int num_tiles;  // tiles per (sequence, kv head) the tickets are sized for
+    int num_parts;  // KV partitions the partial states are sized for
     int num_query_tokens;
     int min_rows;   // sequences with fewer rows (new tokens x group) are not ours
     int num_seqs;
@@ -103,9 +115,10 @@ struct ChunkParams {
     int *n_big;
     int *work;
     int64_t num_blocks;
-    int *counters;    // [S][Hk][num_tiles] tickets, zero between calls
+    int *counters;    // [S][Hk][num_tiles][8] tickets (one per softmax warp), zero between calls
     // partial states, row index R = kv_head * Tq * G + query_start * G + tile
-    // row (the rows of a warp are consecutive): ml [parts][R], O [parts][D][R]
+    // row (the rows of a warp are consecutive): (m, l) [2 groups][parts][R]
+    // (each softmax group keeps a copy), O [parts][D][R]
     float2 *part_ml;
     float *part_o;
     ErrorRecord *err;
@@ -119,8 +132,9 @@ struct ItemInfo {
     uint32_t valid[kPartBlocks / 32];  // one bit per block of the partition: id in range
 };
 
-// Shared memory (from a 1024-aligned base): two query tiles, the key ring,
-// the value ring, the mbarriers, two item records and a few words.
+// Shared memory (from a 1024-aligned base): the query tile being staged,
+// the key ring, the value ring, the mbarriers, two item records, the row
+// maxima the two softmax groups exchange, and a few words.
 template <int D>
 struct Geo {
     static constexpr int kChunks = D / 64;                   // 128-byte chunks of a head row
@@ -128,12 +142,13 @@ struct Geo {
     static constexpr int kK = kChunks * kStepKeys * 128;     // [chunk][key][128 B]
     static constexpr int kVBlock = kChunks * kBS * 128;      // [chunk][token][128 B]
     static constexpr int kV = kStepBlocks * kVBlock;
-    static constexpr int kOffK = 2 * kQ;
+    static constexpr int kOffK = kQ;
     static constexpr int kOffV = kOffK + kKStages * kK;
     static constexpr int kOffBar = kOffV + kVStages * kV;
-    static constexpr int kBars = 2 + 2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 1;
+    static constexpr int kBars = 2 + 2 + 1 + 1 + 2 * kKStages + 2 * kVStages + 1 + 1 + 2 + 2 + 1 + 4;
     static constexpr int kOffInfo = kOffBar + kBars * 8;
-    static constexpr int kOffMisc = kOffInfo + 2 * static_cast<int>(sizeof(ItemInfo));
+    static constexpr int kOffX = kOffInfo + 2 * static_cast<int>(sizeof(ItemInfo));
+    static constexpr int kOffMisc = kOffX + 2 * 2 * kRows * 4;  // float [2 phases][2 groups][rows]
     static constexpr int kBytes = kOffMisc + 16;
 };
 
@@ -141,28 +156,32 @@ int smem_bytes(int D) {
     return dec::kTileAlign + (D == 128 ? Geo<128>::kBytes : Geo<64>::kBytes);
 }
 
-// mbarrier addresses (shared-space) by role
+// mbarrier addresses (shared space) by role
 struct Bars {
     uint32_t b;
+    // item records: published / read by every role
     __device__ uint32_t q_full(int s) const { return b + 8 * s; }
     __device__ uint32_t q_empty(int s) const { return b + 8 * (2 + s); }
-    __device__ uint32_t k_full(int s) const { return b + 8 * (4 + s); }
-    __device__ uint32_t k_empty(int s) const { return b + 8 * (4 + kKStages + s); }
-    __device__ uint32_t v_full(int s) const { return b + 8 * (4 + 2 * kKStages + s); }
-    __device__ uint32_t v_empty(int s) const { return b + 8 * (4 + 2 * kKStages + kVStages + s); }
-    __device__ uint32_t s_full(int s) const { return b + 8 * (4 + 2 * kKStages + 2 * kVStages + s); }
-    __device__ uint32_t s_free(int s) const {
-        return b + 8 * (6 + 2 * kKStages + 2 * kVStages + s);
-    }
-    __device__ uint32_t p_full(int s) const { return b + 8 * (8 + 2 * kKStages + 2 * kVStages + s); }
-    __device__ uint32_t pv_done(int s) const {
-        return b + 8 * (10 + 2 * kKStages + 2 * kVStages + s);
-    }
-    __device__ uint32_t o_free() const { return b + 8 * (12 + 2 * kKStages + 2 * kVStages); }
+    // the query tile in shared memory: landed / copied to tensor memory
+    __device__ uint32_t qs_full() const { return b + 8 * 4; }
+    __device__ uint32_t qs_empty() const { return b + 8 * 5; }
+    __device__ uint32_t k_full(int s) const { return b + 8 * (6 + s); }
+    __device__ uint32_t k_empty(int s) const { return b + 8 * (6 + kKStages + s); }
+    __device__ uint32_t v_full(int s) const { return b + 8 * (6 + 2 * kKStages + s); }
+    __device__ uint32_t v_empty(int s) const { return b + 8 * (6 + 2 * kKStages + kVStages + s); }
+    static constexpr int kS = 6 + 2 * kKStages + 2 * kVStages;
+    __device__ uint32_t s_full() const { return b + 8 * kS; }
+    __device__ uint32_t s_free() const { return b + 8 * (kS + 1); }
+    __device__ uint32_t p_full(int s) const { return b + 8 * (kS + 2 + s); }
+    __device__ uint32_t pv_done(int s) const { return b + 8 * (kS + 4 + s); }
+    __device__ uint32_t o_free() const { return b + 8 * (kS + 6); }
+    // row-maximum exchange between the two softmax warps of a row quarter
+    __device__ uint32_t xbar(int q) const { return b + 8 * (kS + 7 + q); }
 };
 
-// arrivals that complete a phase of each barrier
-constexpr int kQEmptyArrivals = 2 + kSoftmaxWarps;  // MMA commit, value producer, softmax warps
+// arrivals that free an item record: the value producer, the MMA warp and
+// every softmax warp, once each has read it
+constexpr int kQEmptyArrivals = 2 + kSoftmaxWarps;
 
 // Every lane waits (bounded); false if any lane gave up.
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
@@ -379,12 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     chunk_attention_kernel(const __grid_constant__ ChunkParams p) {
     using Gm = Geo<D>;
     constexpr int CH = Gm::kChunks;
+    constexpr int DH = D / 2;  // the head dimensions (of O) each softmax group owns
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((dec::kTileAlign - (smem_u32(smem_raw) & (dec::kTileAlign - 1))) &
                                 (dec::kTileAlign - 1));
     const uint32_t sb = smem_u32(smem);
     const Bars br{sb + Gm::kOffBar};
     ItemInfo *info = reinterpret_cast<ItemInfo *>(smem + Gm::kOffInfo);
+    volatile float *xrow = reinterpret_cast<volatile float *>(smem + Gm::kOffX);
     // misc: [0] tensor-memory base
     volatile int *misc = reinterpret_cast<volatile int *>(smem + Gm::kOffMisc);
 
@@ -395,11 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(br.q_full(s), 1);
             mbar_init(br.q_empty(s), kQEmptyArrivals);
-            mbar_init(br.s_full(s), 1);
-            mbar_init(br.s_free(s), kSoftmaxWarps);
             mbar_init(br.p_full(s), kSoftmaxWarps);
             mbar_init(br.pv_done(s), 1);
         }
+        mbar_init(br.qs_full(), 1);
+        mbar_init(br.qs_empty(), 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(br.k_full(s), 1);
             mbar_init(br.k_empty(s), 1);
@@ -408,7 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(br.v_full(s), 1);
             mbar_init(br.v_empty(s), 1);
         }
+        mbar_init(br.s_full(), 1);
+        mbar_init(br.s_free(), kSoftmaxWarps);
         mbar_init(br.o_free(), kSoftmaxWarps);
+        for (int q = 0; q < 4; ++q) mbar_init(br.xbar(q), 2);
         fence_mbarrier_init();
     }
     if (warp == 2) {
@@ -437,34 +461,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            if (cur.done) {
-                if (lane == 0) {
-                    info[slot].done = 1;
-                    mbar_arrive(br.q_full(slot));
-                }
-                break;
-            }
             if (lane == 0) {
                 ItemInfo &in = info[slot];
-                in.seq = cur.seq;
-                in.part = cur.part;
-                in.kvh = cur.kvh;
-                in.tile = cur.tile;
-                in.nsteps = cur.nsteps;
-                in.nblk = cur.nblk;
-                in.L = cur.L;
-                in.Q = cur.Q;
-                in.q0 = cur.q0;
-                in.nparts = cur.nparts;
-                in.done = 0;
+                in.done = cur.done;
+                if (!cur.done) {
+                    in.seq = cur.seq;
+                    in.part = cur.part;
+                    in.kvh = cur.kvh;
+                    in.tile = cur.tile;
+                    in.nsteps = cur.nsteps;
+                    in.nblk = cur.nblk;
+                    in.L = cur.L;
+                    in.Q = cur.Q;
+                    in.q0 = cur.q0;
+                    in.nparts = cur.nparts;
 #pragma unroll
-                for (int w = 0; w < kPartBlocks / 32; ++w) in.valid[w] = cur.valid[w];
-                mbar_arrive_expect_tx(br.q_full(slot), Gm::kQ);
+                    for (int w = 0; w < kPartBlocks / 32; ++w) in.valid[w] = cur.valid[w];
+                }
+                mbar_arrive(br.q_full(slot));
             }
+            if (cur.done) break;
+            // the query tile, into the staging buffer once the previous tile
+            // has been copied to tensor memory
+            if (it >= 1 && !wait_all(br.qs_empty(), (it - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(br.qs_full(), Gm::kQ);
             __syncwarp();
             if (lane < CH)
-                tensor_g2s_3d(sb + slot * Gm::kQ + lane * (kRows * 128), &p.tm_q, 128 * lane,
-                              cur.kvh * G, cur.q0 + cur.tile * (kRows >> logG), br.q_full(slot));
+                tensor_g2s_3d(sb + lane * (kRows * 128), &p.tm_q, 128 * lane, cur.kvh * G,
+                              cur.q0 + cur.tile * (kRows >> logG), br.qs_full());
             // the next item is taken once this one's first steps are staged
             // (its lookups then overlap this item's work)
             Fetched nxt;
@@ -554,45 +581,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             const ItemInfo &in = info[slot];
             const int done = in.done, nsteps = in.nsteps, nblk = in.nblk, L = in.L;
             const int blo = in.part * kPartBlocks;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(br.q_empty(slot));
             if (done) break;
-            const uint32_t q_s = sb + slot * Gm::kQ;
+            // the query tile into tensor memory (the MMAs read A from there);
+            // copies and MMAs of this thread run in issue order
+            const uint32_t q_t = tmem + kTmemQ + 64 * slot;
+            ok = wait_all(br.qs_full(), it & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc::cp_128x256b(q_t + 8 * kk,
+                                    tc::smem_desc(sb + (kk >> 2) * (kRows * 128) + (kk & 3) * 32,
+                                                  16, 1024, tc::kSwizzle128B));
+                tc::commit(br.qs_empty());
+            }
+            __syncwarp();
             // step n: scores of step n, then the values of step n - 1 (the
             // softmax of step n - 1 overlaps the score MMAs of step n)
             for (int n = 0; n <= nsteps && ok; ++n) {
                 if (n < nsteps) {
-                    const int g = gs + n, ks = g % kKStages, buf = g & 1;
+                    const int g = gs + n, ks = g % kKStages;
                     ok = wait_all(br.k_full(ks), (g / kKStages) & 1);
-                    if (ok && g >= 2) ok = wait_all(br.s_free(buf), ((g - 2) >> 1) & 1);
+                    // the softmax has read the previous step's scores
+                    if (ok && g >= 1) ok = wait_all(br.s_free(), (g - 1) & 1);
                     if (!ok) break;
                     tc::fence_after_sync();
                     if (lane == 0) {
-                        // two accumulators of up to 64 keys each, their k steps
-                        // interleaved (one chain of dependent MMAs would wait
-                        // on each other's results)
+                        // one MMA per k step over the step's keys (each MMA
+                        // instruction costs the issuing thread about the same
+                        // whatever its N, so fewer and wider ones are faster)
                         const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
-                        const int nlo = min(nb, kStepBlocks / 2), nhi = nb - nlo;
-                        const uint32_t id_lo = tc::idesc_f16_f32(kRows, nlo * kBS, false, false);
-                        const uint32_t id_hi =
-                            tc::idesc_f16_f32(kRows, (nhi > 0 ? nhi : 1) * kBS, false, false);
+                        const uint32_t idesc = tc::idesc_f16_f32(kRows, nb * kBS, false, false);
                         const uint32_t k_s = sb + Gm::kOffK + ks * Gm::kK;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-                            const uint64_t a = tc::smem_desc(q_s + c * (kRows * 128) + off, 16,
-                                                             1024, tc::kSwizzle128B);
-                            const uint32_t kc = k_s + c * (kStepKeys * 128) + off;
-                            tc::mma_ss(tmem + kTmemS + buf * 128, a,
-                                       tc::smem_desc(kc, 16, 1024, tc::kSwizzle128B), id_lo,
-                                       kk > 0);
-                            if (nhi > 0)
-                                tc::mma_ss(tmem + kTmemS + buf * 128 + kStepKeys / 2, a,
-                                           tc::smem_desc(kc + (kStepKeys / 2) * 128, 16, 1024,
-                                                         tc::kSwizzle128B),
-                                           id_hi, kk > 0);
-                        }
-                        tc::commit(br.s_full(buf));
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            tc::mma_ts(tmem + kTmemS, q_t + 8 * kk,
+                                       tc::smem_desc(k_s + (kk >> 2) * (kStepKeys * 128) + (kk & 3) * 32,
+                                                     16, 1024, tc::kSwizzle128B),
+                                       idesc, kk > 0);
+                        tc::commit(br.s_full());
                         tc::commit(br.k_empty(ks));
-                        if (n == nsteps - 1) tc::commit(br.q_empty(slot));
                     }
                     __syncwarp();
                 }
@@ -640,15 +671,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
     } else {
         // =============================== softmax ===============================
-        // one thread per query row; a warp reaches tensor-memory lanes
-        // 32 * (warp % 4) ...
+        // one row per thread, half of each step's keys per group; a warp
+        // reaches tensor-memory lanes 32 * (warp % 4) ...
+        const int grp = (warp - 3) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const int64_t Tq = p.num_query_tokens;
         const float sl2 = p.scale_log2;
         int gs = 0;
+        int xs = 0;  // exchanges with the other group's warp of this row quarter
         bool ok = true;
+        // exchange one float per row with the partner warp; false on a timeout
+        auto exchange = [&](float mine, float &theirs) -> bool {
+            volatile float *x = xrow + (xs & 1) * (2 * kRows);
+            x[grp * kRows + r] = mine;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(br.xbar(quarter));
+            if (!wait_all(br.xbar(quarter), xs & 1)) return false;
+            theirs = x[(grp ^ 1) * kRows + r];
+            ++xs;
+            return true;
+        };
         for (int it = 0; ok; ++it) {
             const int slot = it & 1;
             if (!wait_all(br.q_full(slot), (it >> 1) & 1)) {
@@ -671,43 +715,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = rr >> logG;
             const int lim = row_ok ? L - Q + j : -1;  // last key position this row sees
             const int64_t orow = static_cast<int64_t>(q0 + j) * H + kvh * G + (rr & (G - 1));
-            float m_used = kNegInf, l = 0.f;
+            float m_used = kNegInf, l = 0.f;  // l: this group's keys only
 
             for (int n = 0; n < nsteps; ++n) {
-                const int g = gs + n, buf = g & 1;
-                if (!wait_all(br.s_full(buf), (g >> 1) & 1)) {
+                const int g = gs + n;
+                if (!wait_all(br.s_full(), g & 1)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                uint32_t sx[kStepKeys];  // this row's scores (fp32 bits)
+                uint32_t sx[kGroupKeys];  // this row's scores of this group's keys (fp32 bits)
 #pragma unroll
-                for (int c = 0; c < kStepKeys / 32; ++c)
-                    tc::ld32(tl + kTmemS + buf * 128 + 32 * c,
+                for (int c = 0; c < kGroupKeys / 32; ++c)
+                    tc::ld32(tl + kTmemS + kGroupKeys * grp + 32 * c,
                              *reinterpret_cast<uint32_t(*)[32]>(sx + 32 * c));
                 tc::wait_ld();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(br.s_free(buf));
+                if (lane == 0) mbar_arrive(br.s_free());
                 const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
-                const int kbase = part * kPartTokens + n * kStepKeys;
-                const int b0 = n * kStepBlocks;
-                const uint32_t vmask = (valid[b0 >> 5] >> (b0 & 31)) & 0xFFu;
+                const int nbg = min(max(nb - 4 * grp, 0), 4);  // this group's blocks
+                const int kbase = part * kPartTokens + n * kStepKeys + kGroupKeys * grp;
+                const int b0 = n * kStepBlocks + 4 * grp;
+                const uint32_t vmask = (valid[b0 >> 5] >> (b0 & 31)) & 0xFu;
                 // every key visible (and a non-negative scale): the maximum of
                 // the raw scores, scaled once; else scale and mask each score
-                const bool fast = nb == kStepBlocks && vmask == 0xFFu &&
-                                  kbase + kStepKeys - 1 <= lim && sl2 >= 0.f;
+                const bool fast = nbg == 4 && vmask == 0xFu && kbase + kGroupKeys - 1 <= lim &&
+                                  sl2 >= 0.f;
                 float mr[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mr[i] = kNegInf;
                 if (fast) {
 #pragma unroll
-                    for (int e = 0; e < kStepKeys; ++e) mr[e & 7] = fmaxf(mr[e & 7], __uint_as_float(sx[e]));
+                    for (int e = 0; e < kGroupKeys; ++e) mr[e & 7] = fmaxf(mr[e & 7], __uint_as_float(sx[e]));
                 } else {
 #pragma unroll
-                    for (int e = 0; e < kStepKeys; ++e) {
-                        const bool vis =
-                            e < nb * kBS && ((vmask >> (e >> 4)) & 1u) && kbase + e <= lim;
+                    for (int e = 0; e < kGroupKeys; ++e) {
+                        const bool vis = e < nbg * kBS && ((vmask >> (e >> 4)) & 1u) && kbase + e <= lim;
                         const float t = vis ? __uint_as_float(sx[e]) * sl2 : kNegInf;
                         sx[e] = __float_as_uint(t);
                         mr[e & 7] = fmaxf(mr[e & 7], t);
@@ -716,10 +760,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])),
                                  fmaxf(fmaxf(mr[4], mr[5]), fmaxf(mr[6], mr[7])));
                 if (fast) mx *= sl2;
-                const float m_new = fmaxf(m_used, mx);
+                float mo;
+                if (!exchange(mx, mo)) {
+                    ok = false;
+                    break;
+                }
+                const float m_new = fmaxf(m_used, fmaxf(mx, mo));
                 const bool raise = m_new > m_used + kRescaleLog2;
                 // O holds this item's earlier steps relative to m_used: rescale
-                // it before the reference moves (the previous P V done first)
+                // this group's columns before the reference moves (the
+                // previous P V done first)
                 const bool resc = raise && n > 0 && m_used != kNegInf;
                 if (__any_sync(0xffffffffu, resc)) {
                     if (!wait_all(br.pv_done((g - 1) & 1), ((g - 1) >> 1) & 1)) {
@@ -729,14 +779,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_after_sync();
                     const float alpha = resc ? ex2(m_used - m_new) : 1.f;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < DH / 32; ++c) {
                         uint32_t x[32];
-                        tc::ld32(tl + kTmemO + 32 * c, x);
+                        tc::ld32(tl + kTmemO + DH * grp + 32 * c, x);
                         tc::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
-                        tc::st32(tl + kTmemO + 32 * c, x);
+                        tc::st32(tl + kTmemO + DH * grp + 32 * c, x);
                     }
                     tc::wait_st();
                     l *= alpha;
@@ -744,8 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (raise) m_used = m_new;
                 const float ms = m_used == kNegInf ? 0.f : m_used;
                 // weights 2^(s * scale - m) (2^(t - m) for the masked scores),
-                // fp16 pairs: column i of the buffer holds keys 2i, 2i+1; the
-                // P V of two steps back must be done with this buffer
+                // fp16 pairs: column i of the group's half holds its keys 2i,
+                // 2i+1; the P V of two steps back must be done with this buffer
                 const float a = fast ? sl2 : 1.f;
                 const int pb = g & 1;
                 if (g >= 2) {
@@ -756,18 +806,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_after_sync();
                 }
                 float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t x[32];
 #pragma unroll
-                for (int c = 0; c < kStepKeys / 64; ++c) {
-                    uint32_t x[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sx[64 * c + 2 * e]), a, -ms));
-                        const float p1 = ex2(fmaf(__uint_as_float(sx[64 * c + 2 * e + 1]), a, -ms));
-                        l4[e & 3] += p0 + p1;
-                        x[e] = pack_half2(p0, p1);
-                    }
-                    tc::st32(tl + kTmemP + 64 * pb + 32 * c, x);
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sx[2 * e]), a, -ms));
+                    const float p1 = ex2(fmaf(__uint_as_float(sx[2 * e + 1]), a, -ms));
+                    l4[e & 3] += p0 + p1;
+                    x[e] = pack_half2(p0, p1);
                 }
+                tc::st32(tl + kTmemP + 64 * pb + 32 * grp, x);
                 l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 tc::wait_st();
                 tc::fence_before_sync();
@@ -777,31 +824,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             gs += nsteps;
 
-            // ---- the item's output: O / l, or the partial state (m, l, O)
+            // ---- the item's output: O / l, or the partial state (m, l, O),
+            // this group's head dimensions
             if (!wait_all(br.pv_done((gs - 1) & 1), ((gs - 1) >> 1) & 1)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            float o[D];
+            float o[DH];
             {
-                uint32_t ob[D];
+                uint32_t ob[DH];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-                    tc::ld32(tl + kTmemO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(ob + 32 * c));
+                for (int c = 0; c < DH / 32; ++c)
+                    tc::ld32(tl + kTmemO + DH * grp + 32 * c,
+                             *reinterpret_cast<uint32_t(*)[32]>(ob + 32 * c));
                 tc::wait_ld();
 #pragma unroll
-                for (int d = 0; d < D; ++d) o[d] = __uint_as_float(ob[d]);
+                for (int d = 0; d < DH; ++d) o[d] = __uint_as_float(ob[d]);
             }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(br.o_free());
+            float lo;
+            if (!exchange(l, lo)) {
+                ok = false;
+                break;
+            }
+            l += lo;  // the row's sum over both groups' keys
             if (nparts == 1) {
                 if (row_ok) {
                     const float inv = l > 0.f ? 1.f / l : 0.f;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + DH * grp);
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c)
+                    for (int c = 0; c < DH / 8; ++c)
                         dst[c] = make_uint4(pack_half2(o[8 * c] * inv, o[8 * c + 1] * inv),
                                             pack_half2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
                                             pack_half2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
@@ -810,24 +865,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             // partial state, dimension-major so a warp's 32 rows are
-            // consecutive words (coalesced)
+            // consecutive words (coalesced); each group keeps its own (m, l)
             const int64_t NR = Tq * H;
             const int64_t R = static_cast<int64_t>(kvh) * Tq * G + static_cast<int64_t>(q0) * G + rr;
+            const int64_t parts_total = p.num_parts;
+            float2 *ml = p.part_ml + grp * parts_total * NR;
             if (row_ok) {
-                p.part_ml[part * NR + R] = make_float2(m_used, l);
-                float *dst = p.part_o + static_cast<int64_t>(part) * D * NR + R;
+                ml[part * NR + R] = make_float2(m_used, l);
+                float *dst = p.part_o + (static_cast<int64_t>(part) * D + DH * grp) * NR + R;
 #pragma unroll
-                for (int d = 0; d < D; ++d) dst[d * NR] = o[d];
+                for (int d = 0; d < DH; ++d) dst[d * NR] = o[d];
             }
-            // a ticket per (sequence, kv head, tile, warp): the warp that
-            // brings the last partition of its 32 rows merges them
+            // a ticket per (sequence, kv head, tile, softmax warp): the warp
+            // that brings the last partition of its rows and dimensions
+            // merges them
             __threadfence();
             __syncwarp();
             int last = 0;
             if (lane == 0) {
                 int *ticket = p.counters +
-                              ((static_cast<int64_t>(seq) * Hk + kvh) * p.num_tiles + tile) * 4 +
-                              quarter;
+                              ((static_cast<int64_t>(seq) * Hk + kvh) * p.num_tiles + tile) *
+                                  kSoftmaxWarps +
+                              (warp - 3);
                 last = atomicAdd(ticket, 1) == nparts - 1;
                 if (last) {
                     atomicExch(ticket, 0);  // leave the workspace zeroed
@@ -838,22 +897,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!last || !row_ok) continue;
             // the tile's last partition: merge every partition's partial row
             float M = kNegInf;
-            for (int pp = 0; pp < nparts; ++pp) M = fmaxf(M, __ldcg(p.part_ml + pp * NR + R).x);
+            for (int pp = 0; pp < nparts; ++pp) M = fmaxf(M, __ldcg(ml + pp * NR + R).x);
             float den = 0.f;
 #pragma unroll
-            for (int d = 0; d < D; ++d) o[d] = 0.f;
+            for (int d = 0; d < DH; ++d) o[d] = 0.f;
             for (int pp = 0; pp < nparts; ++pp) {
-                const float2 ml = __ldcg(p.part_ml + pp * NR + R);
-                const float w = ml.x == kNegInf ? 0.f : ex2(ml.x - M);
-                den = fmaf(ml.y, w, den);
-                const float *src = p.part_o + static_cast<int64_t>(pp) * D * NR + R;
+                const float2 v = __ldcg(ml + pp * NR + R);
+                const float w = v.x == kNegInf ? 0.f : ex2(v.x - M);
+                den = fmaf(v.y, w, den);
+                const float *src = p.part_o + (static_cast<int64_t>(pp) * D + DH * grp) * NR + R;
 #pragma unroll
-                for (int d = 0; d < D; ++d) o[d] = fmaf(__ldcg(src + d * NR), w, o[d]);
+                for (int d = 0; d < DH; ++d) o[d] = fmaf(__ldcg(src + d * NR), w, o[d]);
             }
             const float inv = den > 0.f ? 1.f / den : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + DH * grp);
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c)
+            for (int c = 0; c < DH / 8; ++c)
                 dst[c] = make_uint4(pack_half2(o[8 * c] * inv, o[8 * c + 1] * inv),
                                     pack_half2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
                                     pack_half2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
@@ -892,9 +951,9 @@ Sizes sizes(int64_t S, int64_t H, int64_t Hk, int64_t D, int64_t Tq, int64_t max
     const int64_t G = H / Hk;
     z.tiles = std::max<int64_t>(1, (max_q * G + kRows - 1) / kRows);
     z.parts = std::max<int64_t>(1, (max_len + kPartTokens - 1) / kPartTokens);
-    z.counters_bytes = dec::align256(S * Hk * z.tiles * 4 * 4);  // a ticket per softmax warp
+    z.counters_bytes = dec::align256(S * Hk * z.tiles * kSoftmaxWarps * 4);  // per softmax warp
     z.list_bytes = dec::align256((2 * S + 3) * 4);  // big_seq, big_cum, n_big, work
-    z.ml_bytes = z.parts > 1 ? dec::align256(z.parts * Tq * H * 8) : 0;
+    z.ml_bytes = z.parts > 1 ? dec::align256(2 * z.parts * Tq * H * 8) : 0;  // per group
     z.o_bytes = z.parts > 1 ? z.parts * Tq * H * D * 4 : 0;
     // the balanced schedule takes the chunks of up to 8 query rows, or of up
     // to 16 when no chunk needs the tile kernel (one column tile is the
@@ -1024,6 +1083,7 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     p.max_query_len = max_query_len;
     p.max_seq_len = max_seq_len;
     p.num_tiles = static_cast<int>(z.tiles);
+    p.num_parts = static_cast<int>(z.parts);
     p.num_query_tokens = num_query_tokens;
     p.min_rows = min_rows;
     p.num_blocks = num_blocks;

@@ -98,6 +98,14 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// Copy a 128-row x 32-byte matrix (described like an MMA operand of K = 16
+// fp16) from shared memory into tensor memory: row i to lane i, its 32 bytes
+// to 8 consecutive columns (the layout an MMA reads A from tensor memory in).
+__device__ __forceinline__ void cp_128x256b(uint32_t taddr, uint64_t src_desc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(src_desc)
+                 : "memory");
+}
+
 // Arrive (once) on the mbarrier when every tcgen05 MMA this thread issued
 // before has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
