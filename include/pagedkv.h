@@ -329,8 +329,9 @@ int pkv_chunk_attention(void *out, const void *q, const void *k_cache, const voi
                         void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* Workspace bytes pkv_chunk_attention needs for these bounds (0 for an
- * invalid shape): tickets plus fp32 partial states of every query row for
- * each 512-token KV partition. */
+ * invalid shape): the short chunks' scratch, the work list, tickets, and,
+ * when max_seq_len exceeds one 2048-token KV partition, fp32 partial states
+ * of every query row for each partition. */
 size_t pkv_chunk_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t num_query_tokens,
                                  int32_t max_query_len, int32_t max_seq_len);
