@@ -76,7 +76,8 @@ constexpr int kPartBlocks = kPartTokens / kBS;
 // q (tensor-memory lanes 32 q ..) and keys 64 grp .. 64 grp + 63 of a step
 constexpr int kSoftmaxWarps = 8;
 constexpr int kGroupKeys = kStepKeys / 2;
-constexpr int kThreads = (3 + kSoftmaxWarps) * 32;
+constexpr int kPVWarp = 3 + kSoftmaxWarps;  // issues the P V MMAs (warp 2 the score MMAs)
+constexpr int kThreads = (4 + kSoftmaxWarps) * 32;
 // tensor memory: O in columns [0, head_dim), the scores in [128, 256), the
 // weights (fp16 pairs) in two buffers of 64 columns, the query tile (fp16
 // pairs, copied from shared memory) in two buffers of 64 columns
@@ -179,9 +180,9 @@ struct Bars {
     __device__ uint32_t xbar(int q) const { return b + 8 * (kS + 7 + q); }
 };
 
-// arrivals that free an item record: the value producer, the MMA warp and
-// every softmax warp, once each has read it
-constexpr int kQEmptyArrivals = 2 + kSoftmaxWarps;
+// arrivals that free an item record: the value producer, the two MMA warps
+// and every softmax warp, once each has read it
+constexpr int kQEmptyArrivals = 3 + kSoftmaxWarps;
 
 // Every lane waits (bounded); false if any lane gave up.
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity) {
@@ -568,8 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 2) {
-        // ================================= MMAs =================================
-        constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kRows, D, false, true);
+        // ============================ score MMAs ============================
+        // (one issuing thread; an MMA that depends on the previous one holds
+        // its issuer back, so the scores and the P V products have one
+        // issuing warp each and their chains overlap in the tensor pipe)
         int gs = 0;
         bool ok = true;
         for (int it = 0; ok; ++it) {
@@ -579,8 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const ItemInfo &in = info[slot];
-            const int done = in.done, nsteps = in.nsteps, nblk = in.nblk, L = in.L;
-            const int blo = in.part * kPartBlocks;
+            const int done = in.done, nsteps = in.nsteps, nblk = in.nblk;
             __syncwarp();
             if (lane == 0) mbar_arrive(br.q_empty(slot));
             if (done) break;
@@ -599,72 +601,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::commit(br.qs_empty());
             }
             __syncwarp();
-            // step n: scores of step n, then the values of step n - 1 (the
-            // softmax of step n - 1 overlaps the score MMAs of step n)
-            for (int n = 0; n <= nsteps && ok; ++n) {
-                if (n < nsteps) {
-                    const int g = gs + n, ks = g % kKStages;
-                    ok = wait_all(br.k_full(ks), (g / kKStages) & 1);
-                    // the softmax has read the previous step's scores
-                    if (ok && g >= 1) ok = wait_all(br.s_free(), (g - 1) & 1);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    if (lane == 0) {
-                        // one MMA per k step over the step's keys (each MMA
-                        // instruction costs the issuing thread about the same
-                        // whatever its N, so fewer and wider ones are faster)
-                        const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
-                        const uint32_t idesc = tc::idesc_f16_f32(kRows, nb * kBS, false, false);
-                        const uint32_t k_s = sb + Gm::kOffK + ks * Gm::kK;
+            for (int n = 0; n < nsteps && ok; ++n) {
+                const int g = gs + n, ks = g % kKStages;
+                ok = wait_all(br.k_full(ks), (g / kKStages) & 1);
+                // the softmax has read the previous step's scores
+                if (ok && g >= 1) ok = wait_all(br.s_free(), (g - 1) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    // one MMA per k step over the step's keys (each MMA
+                    // instruction costs the issuing thread about the same
+                    // whatever its N, so fewer and wider ones are faster)
+                    const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
+                    const uint32_t idesc = tc::idesc_f16_f32(kRows, nb * kBS, false, false);
+                    const uint32_t k_s = sb + Gm::kOffK + ks * Gm::kK;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            tc::mma_ts(tmem + kTmemS, q_t + 8 * kk,
-                                       tc::smem_desc(k_s + (kk >> 2) * (kStepKeys * 128) + (kk & 3) * 32,
-                                                     16, 1024, tc::kSwizzle128B),
-                                       idesc, kk > 0);
-                        tc::commit(br.s_full());
-                        tc::commit(br.k_empty(ks));
-                    }
-                    __syncwarp();
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        tc::mma_ts(tmem + kTmemS, q_t + 8 * kk,
+                                   tc::smem_desc(k_s + (kk >> 2) * (kStepKeys * 128) + (kk & 3) * 32,
+                                                 16, 1024, tc::kSwizzle128B),
+                                   idesc, kk > 0);
+                    tc::commit(br.s_full());
+                    tc::commit(br.k_empty(ks));
                 }
-                if (n > 0) {
-                    const int m = n - 1, g = gs + m, vs = g % kVStages;
-                    const int nb = min(kStepBlocks, nblk - m * kStepBlocks);
-                    ok = wait_all(br.v_full(vs), (g / kVStages) & 1);
-                    if (!ok) break;
-                    const uint32_t v_s = sb + Gm::kOffV + vs * Gm::kV;
-                    if (m == nsteps - 1) {
-                        // value rows at and past the sequence end hold anything
-                        // (their weights are 0, but 0 * NaN is not): zero them
-                        const int t0 = L - (blo + m * kStepBlocks + nb - 1) * kBS;
-                        if (t0 < kBS) {
-                            const int units = (kBS - t0) * 8;  // 16-byte units per chunk
-                            uint8_t *vb = smem + Gm::kOffV + vs * Gm::kV + (nb - 1) * Gm::kVBlock;
-                            for (int i = lane; i < units * CH; i += 32) {
-                                const int c = i / units, r = i % units;
-                                *reinterpret_cast<uint4 *>(vb + c * (kBS * 128) +
-                                                           (t0 + (r >> 3)) * 128 + (r & 7) * 16) =
-                                    make_uint4(0u, 0u, 0u, 0u);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
+                __syncwarp();
+            }
+            gs += nsteps;
+        }
+        if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
+    } else if (warp == kPVWarp) {
+        // ============================= P V MMAs =============================
+        constexpr uint32_t kIdescPV = tc::idesc_f16_f32(kRows, D, false, true);
+        int gs = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+            const int slot = it & 1;
+            if (!wait_all(br.q_full(slot), (it >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const ItemInfo &in = info[slot];
+            const int done = in.done, nsteps = in.nsteps, nblk = in.nblk, L = in.L;
+            const int blo = in.part * kPartBlocks;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(br.q_empty(slot));
+            if (done) break;
+            for (int m = 0; m < nsteps && ok; ++m) {
+                const int g = gs + m, vs = g % kVStages;
+                const int nb = min(kStepBlocks, nblk - m * kStepBlocks);
+                ok = wait_all(br.v_full(vs), (g / kVStages) & 1);
+                if (!ok) break;
+                const uint32_t v_s = sb + Gm::kOffV + vs * Gm::kV;
+                if (m == nsteps - 1) {
+                    // value rows at and past the sequence end hold anything
+                    // (their weights are 0, but 0 * NaN is not): zero them
+                    const int t0 = L - (blo + m * kStepBlocks + nb - 1) * kBS;
+                    if (t0 < kBS) {
+                        const int units = (kBS - t0) * 8;  // 16-byte units per chunk
+                        uint8_t *vb = smem + Gm::kOffV + vs * Gm::kV + (nb - 1) * Gm::kVBlock;
+                        for (int i = lane; i < units * CH; i += 32) {
+                            const int c = i / units, r = i % units;
+                            *reinterpret_cast<uint4 *>(vb + c * (kBS * 128) +
+                                                       (t0 + (r >> 3)) * 128 + (r & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
                         }
+                        fence_proxy_async_smem();
+                        __syncwarp();
                     }
-                    ok = wait_all(br.p_full(g & 1), (g >> 1) & 1);
-                    if (ok && m == 0 && it > 0) ok = wait_all(br.o_free(), (it - 1) & 1);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    if (lane == 0) {
-                        for (int b = 0; b < nb; ++b)
-                            tc::mma_ts(tmem + kTmemO, tmem + kTmemP + 64 * (g & 1) + 8 * b,
-                                       tc::smem_desc(v_s + b * Gm::kVBlock, kBS * 128, 1024,
-                                                     tc::kSwizzle128B),
-                                       kIdescPV, (m > 0 || b > 0) ? 1u : 0u);
-                        tc::commit(br.pv_done(g & 1));
-                        tc::commit(br.v_empty(vs));
-                    }
-                    __syncwarp();
                 }
+                ok = wait_all(br.p_full(g & 1), (g >> 1) & 1);
+                // the previous item's O has been read out
+                if (ok && m == 0 && it > 0) ok = wait_all(br.o_free(), (it - 1) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    for (int b = 0; b < nb; ++b)
+                        tc::mma_ts(tmem + kTmemO, tmem + kTmemP + 64 * (g & 1) + 8 * b,
+                                   tc::smem_desc(v_s + b * Gm::kVBlock, kBS * 128, 1024,
+                                                 tc::kSwizzle128B),
+                                   kIdescPV, (m > 0 || b > 0) ? 1u : 0u);
+                    tc::commit(br.pv_done(g & 1));
+                    tc::commit(br.v_empty(vs));
+                }
+                __syncwarp();
             }
             gs += nsteps;
         }
