@@ -24,11 +24,13 @@
 //    64-dimension chunk, into a 3-step ring laid out [chunk][key][128 B] so
 //    the 128 keys form one MMA operand;
 //  * warp 1 stages the values, one tensor copy per block, into a 2-step ring;
-//  * warp 2 issues the tensor-core work (one thread): it copies the query
-//    tile into tensor memory (two tiles in flight), then per step S = Q K^T
-//    (M = 128 rows, N = 128 keys, A read from tensor memory) into a
-//    128-column score buffer, and O += P V (N = head_dim, 16 keys per MMA)
-//    with the weights P read from tensor memory (two buffers);
+//  * warp 2 (one thread) copies the query tile into tensor memory (two
+//    tiles in flight) and issues per step S = Q K^T (M = 128 rows, N = 128
+//    keys, one MMA per 16-dimension k step, A read from tensor memory) into
+//    a 128-column score buffer; warp 11 (one thread) issues O += P V
+//    (N = head_dim, 16 keys per MMA) with the weights P read from tensor
+//    memory (two buffers).  An MMA that depends on the previous one holds
+//    its issuer back, so each chain has its own issuing warp;
 //  * warps 3-10 run the softmax, one thread per query row and half of each
 //    step's keys per group of four warps: they read the row's scores, mask
 //    keys past the row's position (and past the sequence or in a bad
