@@ -157,16 +157,18 @@ def test_chunk_workspace_bytes(lib):
     assert lib.pkv_chunk_workspace_bytes(4, 30, 8, 128, 10, 7, 100) == 0
     assert lib.pkv_chunk_workspace_bytes(4, 32, 8, 128, 10, 0, 100) == 0
     # the balanced schedule's scratch (short chunks: tickets + partial rows of
-    # up to 16 query columns) comes first, then the tile kernel's: tickets per
-    # (sequence, KV head, 64-row tile) and, past one 2048-token partition,
-    # partial states of every query row
+    # up to 16 query columns) comes first, then the tile kernel's: the work
+    # list, a ticket per (sequence, KV head, 128-row tile, softmax warp) and,
+    # past one 2048-token partition, partial states of every query row (two
+    # copies of (m, l), one O)
     S, H, Hk, D = 4, 32, 8, 128
     one = lib.pkv_chunk_workspace_bytes(S, H, Hk, D, 10, 7, 2048)
-    assert one >= a256(S * Hk * 1 * 4) + a256(S * Hk * 4) + 2 * Hk * 16 * (8 + 4 * D)
-    # 952 new tokens x 4 heads per KV head = 60 tiles; 3000 tokens = 2 partitions
-    Tq, P, tiles = 1015, 2, 60
+    assert one >= a256(S * Hk * 1 * 8 * 4) + a256(S * Hk * 4) + 2 * Hk * 16 * (8 + 4 * D)
+    # 952 new tokens x 4 heads per KV head = 30 tiles; 3000 tokens = 2 partitions
+    Tq, P, tiles = 1015, 2, 30
     big = lib.pkv_chunk_workspace_bytes(64, H, Hk, D, Tq, 952, 3000)
-    assert big >= a256(64 * Hk * tiles * 4) + a256(P * Tq * H * 8) + P * Tq * H * D * 4
+    assert big >= (a256(64 * Hk * tiles * 8 * 4) + a256(2 * P * Tq * H * 8) +
+                   P * Tq * H * D * 4)
 
 
 def test_workspace_bytes(lib):
