@@ -115,3 +115,47 @@ def test_config7_draft_verify_sampled(pkv_lib, orc):
     ref = oracle(orc, wl, rows=rows)
     assert_close(got[rows], ref[rows], what="config 7")
     assert np.isfinite(got).all()
+
+
+def _rows_of(wl, i):
+    return int(wl.query_start[i]), int(wl.query_start[i + 1])
+
+
+def test_bad_block_id_is_skipped_and_recorded(pkv_lib, orc):
+    # sequence 0: a 300-token chunk (tcgen05 tile kernel: the bad block is
+    # staged as zeros and its keys masked), sequence 1: 2 new tokens x G 4 =
+    # 8 rows (balanced decode schedule: the bad block is skipped), sequence 2
+    # untouched.  The error is recorded; the other sequence is exact and no
+    # output is NaN.
+    wl = W.chunk_workload(310, [700, 200, 500], [300, 2, 40], H=16, Hk=4, D=128)
+    ref = oracle(orc, wl)
+    dev = DeviceChunk(wl)
+    dev.write()
+    dev.block_tables[0, 2] = wl.num_blocks + 7
+    dev.block_tables[1, 1] = -5
+    dev.attend()
+    got = dev.out.float().cpu().numpy()
+    kind, _ = pkv.pkv_get_device_error()
+    assert pkv.DEVICE_ERRORS.get(kind) == "block_id"
+    r0, r1 = _rows_of(wl, 2)
+    assert_close(got[r0:r1], ref[r0:r1], what="sequence without bad blocks")
+    assert np.isfinite(got[:r0]).all()
+
+
+def test_bad_sequence_length_is_skipped_and_recorded(pkv_lib, orc):
+    # a length past the block table's capacity: that sequence's rows are not
+    # written, the error is recorded, the others are exact
+    wl = W.chunk_workload(311, [900, 300, 60], [200, 40, 60], H=8, Hk=2, D=64)
+    ref = oracle(orc, wl)
+    dev = DeviceChunk(wl)
+    dev.write()
+    dev.seq_lens[1] = wl.block_tables.shape[1] * wl.block_size + 16
+    dev.out.fill_(7.0)
+    dev.attend()
+    got = dev.out.float().cpu().numpy()
+    kind, _ = pkv.pkv_get_device_error()
+    assert pkv.DEVICE_ERRORS.get(kind) == "seq_len"
+    r0, r1 = _rows_of(wl, 1)
+    assert (got[r0:r1] == 7.0).all()
+    keep = np.r_[0:r0, r1:got.shape[0]]
+    assert_close(got[keep], ref[keep], what="valid sequences")
