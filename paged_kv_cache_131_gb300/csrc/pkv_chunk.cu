@@ -445,6 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the work list, the caches and the outputs are written by earlier
     // kernels of the stream
     grid_dependency_wait();
+    // the kernel launched next (the decode schedule's share of the call)
+    // needs nothing from this one: let its CTAs take the SMs this grid leaves
+    grid_launch_dependents();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -1051,11 +1054,13 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     const int row_bytes = num_kv_heads * head_dim * 2;
 
-    // ---- chunks of up to 8 * col_tiles query rows: the balanced schedule
+    // ---- chunks of up to 8 * col_tiles query rows: the balanced schedule,
+    // launched after the tile kernel (below) when there are long chunks too
     int min_rows = 1;
+    bool use_bal = false;
+    dec::BalancedParams b{};
     // (the balanced schedule indexes the flattened block list in 32 bits)
     if (z.col_tiles > 0 && static_cast<int64_t>(num_seqs) * max_blocks_per_seq <= INT32_MAX) {
-        dec::BalancedParams b{};
         b.out = static_cast<__half *>(out);
         b.q = static_cast<const __half *>(q);
         b.k_cache = static_cast<const __half *>(k_cache);
@@ -1084,13 +1089,13 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
         if (st != PKV_OK) return st;
         b.err = device_error_record();
         if (b.err == nullptr) return PKV_ERR_CUDA;
-        st = dec::launch_balanced(b, z.bal, head_dim, G, false, false, s, z.col_tiles);
-        if (st != PKV_OK) return st;
         min_rows = b.max_cols + 1;
-        if (static_cast<int64_t>(max_query_len) * G < min_rows) return PKV_OK;  // all done
+        if (static_cast<int64_t>(max_query_len) * G < min_rows)  // no long chunks
+            return dec::launch_balanced(b, z.bal, head_dim, G, false, false, s, z.col_tiles);
+        use_bal = true;
     }
 
-    // ---- the larger chunks: query tiles of 64 rows
+    // ---- the larger chunks: query tiles of 128 rows
     ChunkParams p{};
     p.out = static_cast<__half *>(out);
     p.q = static_cast<const __half *>(q);
@@ -1152,5 +1157,13 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, fn, p);
     if (e == cudaSuccess) e = cudaGetLastError();
-    return e == cudaSuccess ? PKV_OK : cuda_failure(e, "chunk attention launch");
+    if (e != cudaSuccess) return cuda_failure(e, "chunk attention launch");
+    if (!use_bal) return PKV_OK;
+    // the short chunks: their CTAs start as the tile kernel's leave (it
+    // allows dependents at its start); the caches were written before the
+    // plan kernel (a full dependency) ran, and the two kernels write disjoint
+    // rows and scratch, so this grid waits for the tile kernel only before it
+    // exits
+    b.defer_wait = 1;
+    return dec::launch_balanced(b, z.bal, head_dim, G, false, false, s, z.col_tiles);
 }

@@ -201,9 +201,7 @@ __device__ void combine_partials(const BalancedParams &p, int kvh, int c_a, int 
 }
 
 template <int D, int G, class Policy, bool kFp8>
-__global__ void __launch_bounds__(kMaxThreads, 1)
-    decode_balanced_kernel(const __grid_constant__ BalancedParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+__device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *smem_raw) {
     uint8_t *smem = smem_raw + ((kTileAlign - (smem_u32(smem_raw) & (kTileAlign - 1))) &
                                 (kTileAlign - 1));
     const int Hk = p.num_kv_heads, S = p.num_seqs, NS = p.num_stages, H = p.num_heads;
@@ -301,7 +299,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     for (int s = blockIdx.x; s < S && !zeros_due; s += gridDim.x) zeros_due = lens[s] == 0;
     if (zeros_due && (blockIdx.x >= N || warp < Hk)) {
         // the consumers (or every warp of a CTA without a range) write them
-        grid_dependency_wait();
+        if (!p.defer_wait) grid_dependency_wait();
         const int nz = blockIdx.x >= N ? nthreads : Hk * 32;
         for (int s = blockIdx.x; s < S; s += gridDim.x) {
             if (lens[s] == 0) {
@@ -352,7 +350,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         fetch(0, c_raw, c_seq, c_nv);
         int c_bid = check(0, c_raw, c_seq);
         fetch(32, n_raw, n_seq, n_nv);
-        grid_dependency_wait();  // the caches may have just been written
+        if (!p.defer_wait) grid_dependency_wait();  // the caches may have just been written
         int issued = 0;
         bool ok = true;
         for (int i = 0; i < n; ++i) {
@@ -424,7 +422,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
         }
     }
-    grid_dependency_wait();  // outputs and partials are written below
+    if (!p.defer_wait) grid_dependency_wait();  // outputs and partials are written below
 
     QueryRows qr{p.q, p.out, 0, H, kvh, G, 0};  // the current sequence's query rows
     auto finish = [&](int seq) {
@@ -564,6 +562,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         return;
     }
     if (cur >= 0) finish(cur);
+}
+
+template <int D, int G, class Policy, bool kFp8>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    decode_balanced_kernel(const __grid_constant__ BalancedParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    balanced_body<D, G, Policy, kFp8>(p, smem_raw);
+    // deferred: this grid read nothing the previous one wrote, but must not
+    // complete before it (later work in the stream relies on both)
+    if (p.defer_wait) grid_dependency_wait();
 }
 
 using BalancedFn = void (*)(const BalancedParams);

@@ -100,6 +100,10 @@ struct BalancedParams {
     const int32_t *query_start;
     int max_cols;
     int num_query_tokens;
+    // 1: nothing this kernel reads was written by the kernel launched just
+    // before it (launched with programmatic serialisation), so it waits for
+    // that kernel only before exiting; 0: it waits before touching the caches
+    int defer_wait;
     int64_t num_blocks;
     int *counters;    // [S * Hk] tickets, zero between calls
     float2 *part_ml;  // [2 * grid][Hk][G]
