@@ -3,7 +3,7 @@ draft verification: each sequence's new tokens attend causally to its cache).
 
 Every case writes the new tokens' rows with pkv_cache_write first, as a step
 does, then compares the attention element by element with the float64 oracle
-at the benchmark spec tolerance (|gpu - ref| <= 2e-3 + 1e-2 |ref|)."""
+at the tolerance |gpu - ref| <= 2e-3 + 1e-2 |ref|."""
 
 import numpy as np
 import pytest
