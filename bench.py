@@ -258,7 +258,7 @@ class OracleSampler:
         while (steps is not None and n < steps) or (budget_s is not None and total_t < budget_s):
             b, t = self.step(n_units)
             total_b, total_t, n = total_b + b, total_t + t, n + 1
-        return total_b / total_t / 1e9, total_t, n
+        return (total_b / total_t / 1e9 if total_t > 0 else 0.0), total_t, n
 
 
 class ChunkOracleSampler:
@@ -302,7 +302,7 @@ class ChunkOracleSampler:
         while (steps is not None and n < steps) or (budget_s is not None and total_t < budget_s):
             b, t = self.step(n_rows)
             total_b, total_t, n = total_b + b, total_t + t, n + 1
-        return total_b / total_t / 1e9, total_t, n
+        return (total_b / total_t / 1e9 if total_t > 0 else 0.0), total_t, n
 
 
 def run_reference(args, wl, rank):
@@ -312,8 +312,9 @@ def run_reference(args, wl, rank):
         sampler = ChunkOracleSampler(wl)
         t_row = sampler.calibrate()
         n_rows = max(1, int(90.0 / max(1, args.steps + args.warmup) / t_row))
-        sampler.run(n_rows, steps=args.warmup)
-        gbs, t, n = sampler.run(n_rows, steps=args.steps)
+        if args.warmup > 0:
+            sampler.run(n_rows, steps=args.warmup)
+        gbs, t, n = sampler.run(n_rows, steps=max(1, args.steps))
         sample = (f"{n_rows} query rows (all heads) per step, rotating over all "
                   f"{len(sampler.rows)}; single-threaded float64")
         line = {
@@ -333,8 +334,9 @@ def run_reference(args, wl, rank):
     t_unit = sampler.calibrate()
     per_step_budget = 90.0 / max(1, args.steps + args.warmup)
     n_units = max(1, int(per_step_budget / t_unit))
-    sampler.run(n_units, steps=args.warmup)
-    gbs, t, n = sampler.run(n_units, steps=args.steps)
+    if args.warmup > 0:
+        sampler.run(n_units, steps=args.warmup)
+    gbs, t, n = sampler.run(n_units, steps=max(1, args.steps))
     sample = (f"{n_units} (sequence, kv_head) units per step, rotating over all "
               f"{len(sampler.units)}, plus the write of all new rows; single-threaded float64")
     line = {
