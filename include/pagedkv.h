@@ -330,7 +330,7 @@ int pkv_chunk_attention(void *out, const void *q, const void *k_cache, const voi
 
 /* Workspace bytes pkv_chunk_attention needs for these bounds (0 for an
  * invalid shape): the short chunks' scratch, the work list, tickets, and,
- * when max_seq_len exceeds one 2048-token KV partition, fp32 partial states
+ * when max_seq_len exceeds one 4096-token KV partition, fp32 partial states
  * of every query row for each partition. */
 size_t pkv_chunk_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t num_query_tokens,

@@ -10,7 +10,7 @@
 // fifth-generation tensor cores (tcgen05) with accumulators in tensor memory.
 //
 // The work is a list of items (query tile of 128 rows, KV head, KV
-// partition of 2048 tokens, sequence), built on the device by a one-CTA plan
+// partition of 4096 tokens, sequence), built on the device by a one-CTA plan
 // kernel for the sequences this kernel takes (partitions past a tile's
 // causal range are not items).  Persistent CTAs (one per SM) pull items in
 // list order from an atomic counter, so tiles with more keys and tiles with
@@ -72,7 +72,7 @@ constexpr int kStepBlocks = 8;                 // blocks per step
 constexpr int kStepKeys = kStepBlocks * kBS;   // 128 keys: the score MMA's N
 constexpr int kKStages = 3;                    // key ring depth (steps)
 constexpr int kVStages = 2;                    // value ring depth (steps)
-constexpr int kPartTokens = 2048;              // KV partition
+constexpr int kPartTokens = 4096;              // KV partition
 constexpr int kPartBlocks = kPartTokens / kBS;
 // softmax: two groups of four warps; warp (3 + 4 grp + q) takes row quarter
 // q (tensor-memory lanes 32 q ..) and keys 64 grp .. 64 grp + 63 of a step

@@ -159,14 +159,14 @@ def test_chunk_workspace_bytes(lib):
     # the balanced schedule's scratch (short chunks: tickets + partial rows of
     # up to 16 query columns) comes first, then the tile kernel's: the work
     # list, a ticket per (sequence, KV head, 128-row tile, softmax warp) and,
-    # past one 2048-token partition, partial states of every query row (two
+    # past one 4096-token partition, partial states of every query row (two
     # copies of (m, l), one O)
     S, H, Hk, D = 4, 32, 8, 128
-    one = lib.pkv_chunk_workspace_bytes(S, H, Hk, D, 10, 7, 2048)
+    one = lib.pkv_chunk_workspace_bytes(S, H, Hk, D, 10, 7, 4096)
     assert one >= a256(S * Hk * 1 * 8 * 4) + a256(S * Hk * 4) + 2 * Hk * 16 * (8 + 4 * D)
-    # 952 new tokens x 4 heads per KV head = 30 tiles; 3000 tokens = 2 partitions
+    # 952 new tokens x 4 heads per KV head = 30 tiles; 5000 tokens = 2 partitions
     Tq, P, tiles = 1015, 2, 30
-    big = lib.pkv_chunk_workspace_bytes(64, H, Hk, D, Tq, 952, 3000)
+    big = lib.pkv_chunk_workspace_bytes(64, H, Hk, D, Tq, 952, 5000)
     assert big >= (a256(64 * Hk * tiles * 8 * 4) + a256(2 * P * Tq * H * 8) +
                    P * Tq * H * D * 4)
 

@@ -62,7 +62,8 @@ SMALL = [
     (305, [530, 1040, 77], [17, 9, 77], 16, 2, 64),                   # G = 8
     (306, [0, 12, 0, 600], [0, 4, 0, 2], 8, 4, 128),                  # empty sequences
     (307, [2049, 513, 512], [1025, 2, 512], 8, 2, 128),               # partition edges
-    (309, [2048, 2049, 4097], [200, 130, 300], 8, 2, 128),            # 2048-token edges
+    (309, [2048, 4096, 4097], [200, 130, 300], 8, 2, 128),            # 4096-token edges
+    (313, [9000, 300, 4500], [150, 20, 64], 8, 2, 64),               # three partitions
     (312, [300, 40, 1, 600], [100, 40, 1, 3], 16, 16, 64),           # Hk 16: all on the tile kernel
 ]
 
