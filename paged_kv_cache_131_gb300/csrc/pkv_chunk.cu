@@ -89,6 +89,11 @@ constexpr int kTmemS = 128;
 constexpr int kTmemP = 256;
 constexpr int kTmemQ = 384;
 constexpr float kRescaleLog2 = 8.f;            // move the reference past 2^8
+// rates of the split between the call's two kernels (see the plan kernel)
+// (single precision: this GPU's double-precision rate is low)
+constexpr float kHbmBytesPerUs = 6.0e6f;        // decode stream, whole GPU
+constexpr float kSmBytesPerUs = 58.0e3f;        // decode stream per SM
+constexpr float kTileStepUs = 1.7f;             // one 128-key step of a tile
 
 struct ChunkParams {
     CUtensorMap tm_k;  // keys: one 128-byte chunk of 16 rows per copy
@@ -110,6 +115,9 @@ struct ChunkParams {
     int num_query_tokens;
     int min_rows;   // sequences with fewer rows (new tokens x group) are not ours
     int num_seqs;
+    int head_dim;
+    int num_ctas;    // CTAs the tile kernel is launched with
+    int max_cols;    // rows the balanced schedule takes per (sequence, kv head); 0: none
     // work list: the sequences taken here (big_seq[k]) and the exclusive
     // prefix of their item counts (big_cum[k], big_cum[n_big] = total items);
     // *work is the next item to hand out
@@ -117,6 +125,9 @@ struct ChunkParams {
     int *big_cum;
     int *n_big;
     int *work;
+    // SMs left to the balanced schedule's share of the call (written by the
+    // plan kernel; that many tile CTAs exit at once)
+    int *split;
     int64_t num_blocks;
     int *counters;    // [S][Hk][num_tiles][8] tickets (one per softmax warp), zero between calls
     // partial states, row index R = kv_head * Tq * G + query_start * G + tile
@@ -244,14 +255,36 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
                                                           int G) {
     __shared__ int wsum[32];
     __shared__ int run[2];  // sequences listed, items listed
+    // work of the two kernels of the call: key/value blocks the balanced
+    // schedule streams, and 128-key steps of the tile kernel's items
+    __shared__ unsigned long long dec_blocks, tile_steps;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) run[0] = run[1] = 0;
+    if (threadIdx.x == 0) {
+        run[0] = run[1] = 0;
+        dec_blocks = tile_steps = 0ull;
+    }
     __syncthreads();
     for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
         const int s = s0 + threadIdx.x;
         SeqGeo sg;
         const bool mine = s < p.num_seqs && seq_geo(p, s, G, true, sg);
         const int cnt = mine ? seq_items(sg, G, p.num_kv_heads) : 0;
+        if (mine) {
+            unsigned long long steps = 0;
+            for (int pt = 0; pt < sg.parts; ++pt)
+                for (int t = first_tile(sg, pt, G); t < sg.tiles; ++t) {
+                    const int j_last = (min(sg.rows, (t + 1) * kRows) - 1) / G;
+                    const int k1 = min(sg.L - sg.Q + j_last + 1, (pt + 1) * kPartTokens);
+                    const int nblk = (k1 + kBS - 1) / kBS - pt * kPartBlocks;
+                    steps += (nblk + kStepBlocks - 1) / kStepBlocks;
+                }
+            atomicAdd(&tile_steps, steps * p.num_kv_heads);
+        } else if (s < p.num_seqs && p.max_cols > 0) {
+            const int L = __ldg(p.seq_lens + s);
+            const int Q = __ldg(p.query_start + s + 1) - __ldg(p.query_start + s);
+            if (Q > 0 && Q <= L && Q * G <= p.max_cols && L <= p.max_blocks_per_seq * kBS)
+                atomicAdd(&dec_blocks, static_cast<unsigned long long>((L + kBS - 1) / kBS));
+        }
         // two exclusive scans at once: (is listed, items) packed in one int2
         int a = mine ? 1 : 0, c = cnt;
 #pragma unroll
@@ -305,6 +338,43 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
         p.big_cum[run[0]] = run[1];
         *p.n_big = run[0];
         *p.work = 0;
+    }
+    // SMs for the balanced schedule: the split that evens the two kernels'
+    // estimated times when they run side by side.  Decode: its bytes at
+    // min(HBM rate, SMs x per-SM rate); tile: its steps at a per-step cost
+    // over the remaining SMs, plus half an average item for the last wave.
+    // Rates measured on this GPU (chunked prefill beside decodes: the decode
+    // kernel streams ~58 GB/s per SM when it shares the GPU, a tile step
+    // costs ~1.7 us beside it).  Thread i tries 2 + 2i SMs; the smallest
+    // estimate wins (ties: fewer SMs).
+    __shared__ unsigned long long best_w[32];
+    unsigned long long key = ~0ull;
+    if (dec_blocks > 0) {
+        const int b = 2 + 2 * static_cast<int>(threadIdx.x);
+        if (b < p.num_ctas) {
+            const float dec_bytes = static_cast<float>(dec_blocks) * kBS * p.num_kv_heads *
+                                    p.head_dim * 2 * 2;
+            const float steps = static_cast<float>(tile_steps);
+            const float items = fmaxf(1.f, static_cast<float>(run[1]));
+            const float tail = 0.5f * __fdividef(steps, items) * kTileStepUs;
+            const float t_dec = __fdividef(dec_bytes, fminf(kHbmBytesPerUs, b * kSmBytesPerUs));
+            const float t_tile = __fdividef(steps * kTileStepUs, static_cast<float>(p.num_ctas - b)) + tail;
+            // (non-negative floats order as their bits)
+            key = (static_cast<unsigned long long>(__float_as_uint(fmaxf(t_dec, t_tile))) << 32) |
+                  static_cast<unsigned>(b);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, key, o);
+        key = y < key ? y : key;
+    }
+    if (lane == 0) best_w[warp] = key;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long k = ~0ull;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) k = best_w[w] < k ? best_w[w] : k;
+        *p.split = k == ~0ull ? 0 : static_cast<int>(k & 0xffffffffu);
     }
 }
 
@@ -438,16 +508,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) mbar_init(br.xbar(q), 2);
         fence_mbarrier_init();
     }
+    // the work list, the caches and the outputs are written by earlier
+    // kernels of the stream
+    grid_dependency_wait();
+    // the last `split` CTAs leave their SMs to the balanced schedule
+    if (static_cast<int>(blockIdx.x) >= static_cast<int>(gridDim.x) - __ldcg(p.split)) return;
+    // the kernel launched next (the decode schedule's share of the call)
+    // needs nothing from this one: let its CTAs take the SMs this grid leaves
+    grid_launch_dependents();
     if (warp == 2) {
         tc::tmem_alloc(sb + Gm::kOffMisc, kTmemCols);
         tc::tmem_relinquish();
     }
-    // the work list, the caches and the outputs are written by earlier
-    // kernels of the stream
-    grid_dependency_wait();
-    // the kernel launched next (the decode schedule's share of the call)
-    // needs nothing from this one: let its CTAs take the SMs this grid leaves
-    grid_launch_dependents();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -976,7 +1048,7 @@ Sizes sizes(int64_t S, int64_t H, int64_t Hk, int64_t D, int64_t Tq, int64_t max
     z.tiles = std::max<int64_t>(1, (max_q * G + kRows - 1) / kRows);
     z.parts = std::max<int64_t>(1, (max_len + kPartTokens - 1) / kPartTokens);
     z.counters_bytes = dec::align256(S * Hk * z.tiles * kSoftmaxWarps * 4);  // per softmax warp
-    z.list_bytes = dec::align256((2 * S + 3) * 4);  // big_seq, big_cum, n_big, work
+    z.list_bytes = dec::align256((2 * S + 4) * 4);  // big_seq, big_cum, n_big, work, split
     z.ml_bytes = z.parts > 1 ? dec::align256(2 * z.parts * Tq * H * 8) : 0;  // per group
     z.o_bytes = z.parts > 1 ? z.parts * Tq * H * D * 4 : 0;
     // the balanced schedule takes the chunks of up to 8 query rows, or of up
@@ -1119,6 +1191,9 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     p.big_cum = p.big_seq + num_seqs;
     p.n_big = p.big_cum + num_seqs + 1;
     p.work = p.n_big + 1;
+    p.split = p.work + 1;
+    p.head_dim = head_dim;
+    p.max_cols = use_bal ? b.max_cols : 0;
     cws += z.list_bytes;
     p.counters = reinterpret_cast<int *>(cws);
     p.part_ml = reinterpret_cast<float2 *>(cws + z.counters_bytes);
@@ -1138,15 +1213,18 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     if (p.err == nullptr) return PKV_ERR_CUDA;
 
     // the work list (one CTA), then persistent CTAs that pull from it
+    const int smem = smem_bytes(head_dim);
+    int per_sm = 0;
+    {
+        const int st = prepare_kernel(reinterpret_cast<const void *>(fn), kThreads, smem, &per_sm);
+        if (st != PKV_OK) return st;
+    }
+    p.num_ctas = std::max(1, sm_count() * std::max(1, per_sm));
     chunk_plan_kernel<<<1, 1024, 0, s>>>(p, G);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_failure(e, "chunk plan launch");
-    const int smem = smem_bytes(head_dim);
-    int per_sm = 0;
-    const int st = prepare_kernel(reinterpret_cast<const void *>(fn), kThreads, smem, &per_sm);
-    if (st != PKV_OK) return st;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(std::max(1, sm_count() * std::max(1, per_sm))));
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_ctas));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -1165,5 +1243,6 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     // rows and scratch, so this grid waits for the tile kernel only before it
     // exits
     b.defer_wait = 1;
+    b.active_ctas = p.split;  // its ranges over the SMs the plan left it
     return dec::launch_balanced(b, z.bal, head_dim, G, false, false, s, z.col_tiles);
 }

@@ -294,7 +294,11 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
 
     // ---- empty sequences get zeros (no block of theirs is in any range)
     const int64_t T = cum[S];
-    const int64_t N = min(static_cast<int64_t>(gridDim.x), T);
+    int64_t N = min(static_cast<int64_t>(gridDim.x), T);
+    if (p.active_ctas != nullptr) {
+        const int a = __ldcg(p.active_ctas);
+        if (a > 0) N = min(N, static_cast<int64_t>(a));
+    }
     bool zeros_due = false;
     for (int s = blockIdx.x; s < S && !zeros_due; s += gridDim.x) zeros_due = lens[s] == 0;
     if (zeros_due && (blockIdx.x >= N || warp < Hk)) {

@@ -104,6 +104,9 @@ struct BalancedParams {
     // before it (launched with programmatic serialisation), so it waits for
     // that kernel only before exiting; 0: it waits before touching the caches
     int defer_wait;
+    // if non-null and > 0 there: the work is split over that many CTAs (the
+    // first ones) instead of the whole grid; written by an earlier kernel
+    const int *active_ctas;
     int64_t num_blocks;
     int *counters;    // [S * Hk] tickets, zero between calls
     float2 *part_ml;  // [2 * grid][Hk][G]
