@@ -257,11 +257,13 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
     __shared__ int run[2];  // sequences listed, items listed
     // work of the two kernels of the call: key/value blocks the balanced
     // schedule streams, and 128-key steps of the tile kernel's items
-    __shared__ unsigned long long dec_blocks, tile_steps;
+    __shared__ unsigned long long dec_blocks;
+    __shared__ float tile_steps;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         run[0] = run[1] = 0;
-        dec_blocks = tile_steps = 0ull;
+        dec_blocks = 0ull;
+        tile_steps = 0.f;
     }
     __syncthreads();
     for (int s0 = 0; s0 < p.num_seqs; s0 += blockDim.x) {
@@ -269,22 +271,32 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
         SeqGeo sg;
         const bool mine = s < p.num_seqs && seq_geo(p, s, G, true, sg);
         const int cnt = mine ? seq_items(sg, G, p.num_kv_heads) : 0;
+        float my_steps = 0.f;
+        unsigned long long my_dec = 0;
         if (mine) {
-            unsigned long long steps = 0;
-            for (int pt = 0; pt < sg.parts; ++pt)
-                for (int t = first_tile(sg, pt, G); t < sg.tiles; ++t) {
-                    const int j_last = (min(sg.rows, (t + 1) * kRows) - 1) / G;
-                    const int k1 = min(sg.L - sg.Q + j_last + 1, (pt + 1) * kPartTokens);
-                    const int nblk = (k1 + kBS - 1) / kBS - pt * kPartBlocks;
-                    steps += (nblk + kStepBlocks - 1) / kStepBlocks;
-                }
-            atomicAdd(&tile_steps, steps * p.num_kv_heads);
+            // 128-key steps of the sequence's items, estimated in closed form:
+            // tile t (128/G new tokens each, the last one clipped) sees
+            // L - Q + min(Q, (t + 1) 128/G) keys, plus on average half a step
+            // of rounding per (tile, partition) item
+            const float R = static_cast<float>(kRows / G), nt = static_cast<float>(sg.tiles);
+            const float keys = nt * static_cast<float>(sg.L - sg.Q) +
+                               R * nt * (nt - 1.f) * 0.5f + static_cast<float>(sg.Q);
+            my_steps = keys * (1.f / kStepKeys) * static_cast<float>(p.num_kv_heads) +
+                       0.5f * static_cast<float>(cnt);
         } else if (s < p.num_seqs && p.max_cols > 0) {
             const int L = __ldg(p.seq_lens + s);
             const int Q = __ldg(p.query_start + s + 1) - __ldg(p.query_start + s);
             if (Q > 0 && Q <= L && Q * G <= p.max_cols && L <= p.max_blocks_per_seq * kBS)
-                atomicAdd(&dec_blocks, static_cast<unsigned long long>((L + kBS - 1) / kBS));
+                my_dec = static_cast<unsigned long long>((L + kBS - 1) / kBS);
         }
+        // one shared atomic per warp and counter
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            my_steps += __shfl_xor_sync(0xffffffffu, my_steps, o);
+            my_dec += __shfl_xor_sync(0xffffffffu, my_dec, o);
+        }
+        if (lane == 0 && my_steps > 0.f) atomicAdd(&tile_steps, my_steps);
+        if (lane == 0 && my_dec) atomicAdd(&dec_blocks, my_dec);
         // two exclusive scans at once: (is listed, items) packed in one int2
         int a = mine ? 1 : 0, c = cnt;
 #pragma unroll
@@ -354,7 +366,7 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
         if (b < p.num_ctas) {
             const float dec_bytes = static_cast<float>(dec_blocks) * kBS * p.num_kv_heads *
                                     p.head_dim * 2 * 2;
-            const float steps = static_cast<float>(tile_steps);
+            const float steps = tile_steps;
             const float items = fmaxf(1.f, static_cast<float>(run[1]));
             const float tail = 0.5f * __fdividef(steps, items) * kTileStepUs;
             const float t_dec = __fdividef(dec_bytes, fminf(kHbmBytesPerUs, b * kSmBytesPerUs));
@@ -371,10 +383,14 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
     }
     if (lane == 0) best_w[warp] = key;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned long long k = ~0ull;
-        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) k = best_w[w] < k ? best_w[w] : k;
-        *p.split = k == ~0ull ? 0 : static_cast<int>(k & 0xffffffffu);
+    if (warp == 0) {
+        unsigned long long k = lane < static_cast<int>(blockDim.x >> 5) ? best_w[lane] : ~0ull;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, k, o);
+            k = y < k ? y : k;
+        }
+        if (lane == 0) *p.split = k == ~0ull ? 0 : static_cast<int>(k & 0xffffffffu);
     }
 }
 

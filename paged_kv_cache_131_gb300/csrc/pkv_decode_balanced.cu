@@ -222,6 +222,16 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthreads = blockDim.x, nwarps = nthreads >> 5;
 
+    // CTAs taking part: the whole grid, or the first *active_ctas of it.  The
+    // others leave before doing anything: they may be scheduled only when an
+    // SM frees up at the end of the call, and must not add to it.
+    int grid = static_cast<int>(gridDim.x);
+    if (p.active_ctas != nullptr) {
+        const int a = __ldcg(p.active_ctas);
+        if (a > 0 && a < grid) grid = a;
+    }
+    if (static_cast<int>(blockIdx.x) >= grid) return;
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
@@ -294,18 +304,14 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
 
     // ---- empty sequences get zeros (no block of theirs is in any range)
     const int64_t T = cum[S];
-    int64_t N = min(static_cast<int64_t>(gridDim.x), T);
-    if (p.active_ctas != nullptr) {
-        const int a = __ldcg(p.active_ctas);
-        if (a > 0) N = min(N, static_cast<int64_t>(a));
-    }
+    const int64_t N = min(static_cast<int64_t>(grid), T);
     bool zeros_due = false;
-    for (int s = blockIdx.x; s < S && !zeros_due; s += gridDim.x) zeros_due = lens[s] == 0;
+    for (int s = blockIdx.x; s < S && !zeros_due; s += grid) zeros_due = lens[s] == 0;
     if (zeros_due && (blockIdx.x >= N || warp < Hk)) {
         // the consumers (or every warp of a CTA without a range) write them
         if (!p.defer_wait) grid_dependency_wait();
         const int nz = blockIdx.x >= N ? nthreads : Hk * 32;
-        for (int s = blockIdx.x; s < S; s += gridDim.x) {
+        for (int s = blockIdx.x; s < S; s += grid) {
             if (lens[s] == 0) {
                 uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(s) * H * D);
                 for (int e = threadIdx.x; e < H * D / 8; e += nz) o[e] = make_uint4(0, 0, 0, 0);
@@ -574,8 +580,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     balanced_body<D, G, Policy, kFp8>(p, smem_raw);
     // deferred: this grid read nothing the previous one wrote, but must not
-    // complete before it (later work in the stream relies on both)
-    if (p.defer_wait) grid_dependency_wait();
+    // complete before it (later work in the stream relies on both); CTAs
+    // outside the active set did nothing, the first CTA always takes part
+    if (p.defer_wait) {
+        const int a = p.active_ctas != nullptr ? __ldcg(p.active_ctas) : 0;
+        if (a <= 0 || static_cast<int>(blockIdx.x) < a) grid_dependency_wait();
+    }
 }
 
 using BalancedFn = void (*)(const BalancedParams);
