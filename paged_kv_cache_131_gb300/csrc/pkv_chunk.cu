@@ -16,6 +16,10 @@
 // list order from an atomic counter, so tiles with more keys and tiles with
 // fewer balance out.  A row is (new token j, query head g of the KV head's
 // group): row = j*G + g, so a tile covers 128/G consecutive new tokens.
+// When both kernels have work, the plan kernel also estimates each one's
+// share and picks how many SMs the balanced schedule gets; this kernel's
+// last that-many CTAs leave at once and the balanced grid uses only its
+// first that-many, so the two run side by side on disjoint SMs.
 //
 // Per CTA, warp-specialised, all hand-offs through mbarriers:
 //  * warp 0 takes the items (the next one while the current one is staged),
