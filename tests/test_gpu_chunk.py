@@ -119,6 +119,26 @@ def test_config7_draft_verify_sampled(pkv_lib, orc):
     assert np.isfinite(got).all()
 
 
+def test_sm_split_extremes(pkv_lib, orc):
+    # the plan kernel hands the balanced schedule most of the SMs (24 long
+    # decodes beside a 3-token chunk: as many as HBM rewards, ~2/3) or the
+    # fewest it gives (a 1500-token prompt beside one short decode: 2); every
+    # row is still computed, once
+    rng = np.random.default_rng(318)
+    many = [int(x) for x in rng.integers(2500, 4097, size=24)]
+    wl = W.chunk_workload(318, [50] + many, [3] + [1] * 24, H=32, Hk=8, D=128)
+    _, got = run(wl)
+    assert_close(got, oracle(orc, wl), what="decode-heavy split")
+
+    wl = W.chunk_workload(319, [1500, 20], [1500, 1], H=32, Hk=8, D=128)
+    _, got = run(wl)
+    rows = sorted({0, 1, 31, 32, 767, 768, 1499, 1500} |
+                  set(int(x) for x in np.random.default_rng(319).integers(0, 1500, size=24)))
+    ref = oracle(orc, wl, rows=rows)
+    assert_close(got[rows], ref[rows], what="tile-heavy split")
+    assert np.isfinite(got).all()
+
+
 def _rows_of(wl, i):
     return int(wl.query_start[i]), int(wl.query_start[i + 1])
 
