@@ -374,7 +374,8 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
             const float items = fmaxf(1.f, static_cast<float>(run[1]));
             const float tail = 0.5f * __fdividef(steps, items) * kTileStepUs;
             const float t_dec = __fdividef(dec_bytes, fminf(kHbmBytesPerUs, b * kSmBytesPerUs));
-            const float t_tile = __fdividef(steps * kTileStepUs, static_cast<float>(p.num_ctas - b)) + tail;
+            const float t_tile =
+                __fdividef(steps * kTileStepUs, static_cast<float>(p.num_ctas - b)) + tail;
             // (non-negative floats order as their bits)
             key = (static_cast<unsigned long long>(__float_as_uint(fmaxf(t_dec, t_tile))) << 32) |
                   static_cast<unsigned>(b);
