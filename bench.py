@@ -406,7 +406,13 @@ def main_chunk(args, wl, rank, world, local):
     # the step's launches (write; one or two attention kernels and the plan
     # kernel) are captured once as CUDA graphs and replayed, so no Python
     # enqueue sits inside the timed region
-    g_write, g_attend = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # (one graph for the whole step, so the attention call may overlap the
+    # write's tail as it does on a stream; two for the pass that times each)
+    g_step, g_write, g_attend = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                 torch.cuda.CUDAGraph())
+    with torch.cuda.graph(g_step):
+        dev.write()
+        dev.attend()
     with torch.cuda.graph(g_write):
         dev.write()
     with torch.cuda.graph(g_attend):
@@ -418,10 +424,12 @@ def main_chunk(args, wl, rank, world, local):
         for i in range(K):
             flush()
             ev[i][0].record(stream)
-            g_write.replay()
             if split:
+                g_write.replay()
                 ev[i][1].record(stream)
-            g_attend.replay()
+                g_attend.replay()
+            else:
+                g_step.replay()
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         step = sum(e[0].elapsed_time(e[2]) for e in ev) / K

@@ -315,6 +315,10 @@ int pkv_decode_attention_fp8(void *out, const void *q, const void *k_cache, cons
  *   max_seq_len     host bound on every L (sizes the launch and workspace)
  *   workspace       pkv_chunk_workspace_bytes(...) bytes, zeroed once
  *                   (pkv_decode_workspace_init); every call leaves it zeroed
+ * Ordering: as for pkv_decode_attention, the launch may overlap a previous
+ * kernel that signals programmatic launch completion (pkv_cache_write does);
+ * before that kernel's completion the call reads only seq_lens, query_start,
+ * q and block_tables, so such a kernel must not write those.
  * Supported: head_dim 64 or 128, block_size 16, group size 1, 2, 4 or 8.
  * Rows of a sequence whose Q exceeds max_query_len or L, or whose L exceeds
  * its block table or max_seq_len, are skipped and recorded as

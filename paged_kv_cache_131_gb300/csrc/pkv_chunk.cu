@@ -339,6 +339,11 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
         __syncthreads();
         const int ea = run[0] + wa[warp] + a - (mine ? 1 : 0);
         const int ec = run[1] + wsum[warp] + c - cnt;
+        // launched as a programmatic dependent: the lengths and offsets above
+        // may be read while the previous kernel (the cache write) finishes,
+        // but nothing is written before it has completed -- which also makes
+        // this kernel's completion imply that kernel's for the ones after it
+        if (s0 == 0) grid_dependency_wait();
         if (mine) {
             p.big_seq[ea] = s;
             p.big_cum[ea] = ec;
@@ -350,6 +355,7 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
         }
         __syncthreads();
     }
+    grid_dependency_wait();  // (returns at once if the loop waited already)
     if (threadIdx.x == 0) {
         p.big_cum[run[0]] = run[1];
         *p.n_big = run[0];
@@ -1241,17 +1247,23 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
         if (st != PKV_OK) return st;
     }
     p.num_ctas = std::max(1, sm_count() * std::max(1, per_sm));
-    chunk_plan_kernel<<<1, 1024, 0, s>>>(p, G);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t pcfg = {};
+    pcfg.gridDim = dim3(1);
+    pcfg.blockDim = dim3(1024);
+    pcfg.stream = s;
+    pcfg.attrs = attr;
+    pcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&pcfg, chunk_plan_kernel, p, G);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_failure(e, "chunk plan launch");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.num_ctas));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, fn, p);
@@ -1260,9 +1272,9 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
     if (!use_bal) return PKV_OK;
     // the short chunks: their CTAs start as the tile kernel's leave (it
     // allows dependents at its start); the caches were written before the
-    // plan kernel (a full dependency) ran, and the two kernels write disjoint
-    // rows and scratch, so this grid waits for the tile kernel only before it
-    // exits
+    // plan kernel completed (it waits for the previous kernel), and the two
+    // kernels write disjoint rows and scratch, so this grid waits for the
+    // tile kernel only before it exits
     b.defer_wait = 1;
     b.active_ctas = p.split;  // its ranges over the SMs the plan left it
     return dec::launch_balanced(b, z.bal, head_dim, G, false, false, s, z.col_tiles);
