@@ -109,6 +109,16 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def host_cpu_info() -> dict:
+    """The host's CPU count and the size of this process's affinity set (the
+    oracle runs single-threaded on one of them)."""
+    try:
+        aff = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        aff = None
+    return {"host_cpus": os.cpu_count(), "affinity_cpus": aff}
+
+
 def decode_source_hash() -> str:
     h = hashlib.sha256()
     for p in DECODE_SOURCES:
@@ -324,7 +334,7 @@ def run_reference(args, wl, rank):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
             "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, **host_cpu_info()},
             "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
         }
@@ -346,7 +356,7 @@ def run_reference(args, wl, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
         "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, **host_cpu_info()},
         "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -481,6 +491,7 @@ def main_chunk(args, wl, rank, world, local):
         n_rows = max(1, int(1.0 / t_row))
         gbs_cpu, t_cpu, n_cpu = sampler.run(n_rows, budget_s=15.0)
         cpu = {"value": round(gbs_cpu, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               **host_cpu_info(),
                "sample": f"{n_cpu} x {n_rows} query rows (all heads), rotating, "
                          f"{t_cpu:.1f} s single-threaded float64"}
     line = {
@@ -627,6 +638,7 @@ def main():
         sampler = OracleSampler(wl)
         gbs, t_cpu, n_cpu = sampler.run(8, budget_s=15.0)
         cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               **host_cpu_info(),
                "sample": f"{n_cpu} steps x 8 (sequence, kv_head) units (all query heads) + the "
                          f"write of all new rows, {t_cpu:.1f} s single-threaded float64"}
     line = {
