@@ -90,33 +90,30 @@ double oracle_e4m3_value(uint8_t code)
 
 /* Nearest E4M3 code to y, ties to the even code, magnitudes above 448
  * saturating to 448; NaN gives 0x7F.  The non-negative finite codes 0..126
- * have increasing values, so the nearest one is found by bisection over
- * that table, then the two neighbours are compared (ties -> even code). */
+ * have increasing values, so the nearest one is found by bisection over the
+ * codes (each code's value computed from the format as it is needed; no
+ * table, no state kept between calls), then the two neighbours are compared
+ * (ties -> even code).  A scan of all 127 codes per element gives the same
+ * code but is too slow to quantize full-size caches. */
 uint8_t oracle_e4m3_encode(float y)
 {
-    static double table[127];
-    static int ready = 0;
-    if (!ready) {
-        for (int c = 0; c < 127; ++c)
-            table[c] = oracle_e4m3_value((uint8_t)c);
-        ready = 1;
-    }
     if (isnan(y))
         return 0x7f;
     double a = fabs((double)y);
     if (a > 448.0)
         a = 448.0;
-    int lo = 0, hi = 126; /* largest lo with table[lo] <= a */
+    int lo = 0, hi = 126; /* largest lo with value(lo) <= a */
     while (lo < hi) {
         int mid = (lo + hi + 1) / 2;
-        if (table[mid] <= a)
+        if (oracle_e4m3_value((uint8_t)mid) <= a)
             lo = mid;
         else
             hi = mid - 1;
     }
     int best = lo;
     if (lo < 126) {
-        double below = a - table[lo], above = table[lo + 1] - a;
+        double below = a - oracle_e4m3_value((uint8_t)lo);
+        double above = oracle_e4m3_value((uint8_t)(lo + 1)) - a;
         if (above < below || (above == below && ((lo + 1) & 1) == 0))
             best = lo + 1;
     }
