@@ -30,6 +30,31 @@ bool balanced_fits_index(int64_t num_seqs, int64_t max_blocks_per_seq) {
 }
 
 }  // namespace
+
+int check_decode_args(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *seq_lens, float scale,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t num_seqs, int32_t max_blocks_per_seq,
+                      int32_t max_seq_len, int64_t num_blocks) {
+    if (num_seqs < 0) return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_NULL;
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len < 0 ||
+        !std::isfinite(scale))
+        return PKV_ERR_INVALID;
+    const int G = num_heads / num_kv_heads;
+    if (!(G == 1 || G == 2 || G == 4 || G == 8)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!pkv::aligned(out, 16) || !pkv::aligned(q, 16) || !pkv::aligned(k_cache, 16) ||
+        !pkv::aligned(v_cache, 16) || !pkv::aligned(block_tables, 4) ||
+        !pkv::aligned(seq_lens, 4))
+        return PKV_ERR_ALIGNMENT;
+    return PKV_OK;
+}
+
 }  // namespace dec
 }  // namespace pkv
 
@@ -78,18 +103,14 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
                             pkv_stream_t stream) {
     using namespace pkv;
     using namespace pkv::dec;
-    if (num_seqs < 0) return PKV_ERR_INVALID;
     if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_NULL;
-    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
-        block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len < 0 ||
-        !std::isfinite(scale))
-        return PKV_ERR_INVALID;
+    {
+        const int st = check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                                         num_heads, num_kv_heads, head_dim, block_size, num_seqs,
+                                         max_blocks_per_seq, max_seq_len, num_blocks);
+        if (st != PKV_OK) return st;
+    }
     const int G = num_heads / num_kv_heads;
-    if (!(G == 1 || G == 2 || G == 4 || G == 8)) return PKV_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-    if (block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
     const int pt = resolve_partition(opts);
     if (pt < kBlockSize || pt > kMaxPartitionTokens || pt % kBlockSize != 0)
         return PKV_ERR_INVALID;
@@ -97,9 +118,6 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
     if (compute < PKV_COMPUTE_AUTO || compute > PKV_COMPUTE_MMA) return PKV_ERR_INVALID;
     const int schedule = opts ? opts->schedule : PKV_SCHEDULE_AUTO;
     if (schedule < PKV_SCHEDULE_AUTO || schedule > PKV_SCHEDULE_BALANCED) return PKV_ERR_INVALID;
-    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
-        return PKV_ERR_ALIGNMENT;
     if (workspace != nullptr && !aligned(workspace, 16)) return PKV_ERR_ALIGNMENT;
     const bool simt = compute == PKV_COMPUTE_SIMT;  // measured: the MMA policy is faster
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -134,5 +134,15 @@ int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, 
 
 inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
+// The argument checks every fp16 decode entry point makes before it touches
+// a stream: pointers, sizes, supported shape (G in {1,2,4,8}, head_dim 64 or
+// 128, block_size 16) and alignment.  Returns a PKV status (PKV_OK also for
+// num_seqs == 0, which launches nothing).
+int check_decode_args(const void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, const int32_t *seq_lens, float scale,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t num_seqs, int32_t max_blocks_per_seq,
+                      int32_t max_seq_len, int64_t num_blocks);
+
 }  // namespace dec
 }  // namespace pkv

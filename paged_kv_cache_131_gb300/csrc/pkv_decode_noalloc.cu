@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstdio>
 
@@ -67,9 +68,15 @@ extern "C" int pkv_decode_attention_noalloc(void *out, const void *q, const void
                                             pkv_stream_t stream) {
     using namespace pkv;
     if (num_seqs == 0) return PKV_OK;
-    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        max_seq_len < 0 || num_heads % num_kv_heads != 0)
-        return PKV_ERR_INVALID;
+    // Every check that can fail without a launch comes first, so a refused
+    // call enqueues nothing and leaves the shared scratch alone.
+    {
+        const int st = dec::check_decode_args(out, q, k_cache, v_cache, block_tables, seq_lens,
+                                              scale, num_heads, num_kv_heads, head_dim,
+                                              block_size, num_seqs, max_blocks_per_seq,
+                                              max_seq_len, num_blocks);
+        if (st != PKV_OK) return st;
+    }
     // The scratch must hold what the chosen schedule needs: the balanced
     // schedule's partials when they fit (it is then the one that runs), else
     // the grid schedule's.  Larger shapes are refused before anything runs.
@@ -80,7 +87,14 @@ extern "C" int pkv_decode_attention_noalloc(void *out, const void *q, const void
         1, (static_cast<int64_t>(max_seq_len) + dec::kDefaultPartitionTokens - 1) /
                dec::kDefaultPartitionTokens);
     const int64_t grid_need = dec::grid_workspace_bytes(num_seqs, num_heads, head_dim, P);
-    const bool bal_fits = bal.ok && bal.workspace <= static_cast<int64_t>(kScratchBytes);
+    // (the balanced schedule also needs its flattened block index to fit 31 bits)
+    const bool bal_fits = bal.ok && bal.workspace <= static_cast<int64_t>(kScratchBytes) &&
+                          static_cast<int64_t>(num_seqs) * max_blocks_per_seq <= INT32_MAX;
+    // the grid schedule's own limits: partitions per sequence, and the
+    // combine's per-partition weights held in its staging ring
+    if (!bal_fits && (P > 65535 || (P > 1 && (2 * G * P + 2 * G) * 4 >
+                                                 dec::grid_ring_bytes(head_dim))))
+        return PKV_ERR_UNSUPPORTED;
     if (!bal_fits && grid_need > static_cast<int64_t>(kScratchBytes)) {
         char msg[200];
         std::snprintf(msg, sizeof(msg),
