@@ -85,6 +85,32 @@ def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
 
 
+def _split_rows(rows, workers: int):
+    """Split a list of independent output rows into ``workers`` interleaved
+    parts (interleaving spreads long and short rows evenly)."""
+    return [rows[w::workers] for w in range(workers) if rows[w::workers]]
+
+
+def _in_threads(fn, parts):
+    """Run ``fn(part)`` for every part on its own thread and return the
+    results in order.  The C calls release the GIL, so the parts run on
+    several cores; each output row is still computed by one call of the
+    same single-threaded function, so the arithmetic of a row does not
+    depend on the split."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        return list(ex.map(fn, parts))
+
+
+def default_workers() -> int:
+    try:
+        n = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        n = os.cpu_count() or 1
+    return max(1, n)
+
+
 # --------------------------------------------------------------------------
 # Python-facing functions.  ``lib`` lets a test run the same calls against a
 # deliberately mutated build of the C source.
@@ -138,13 +164,26 @@ def copy_blocks(cache: np.ndarray, pairs, *, offset: int, layer: int, num_layers
 
 def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                      block_tables: np.ndarray, seq_lens: np.ndarray, scale: float, *,
-                     pairs=None, lib=None) -> np.ndarray:
+                     pairs=None, lib=None, workers: int = 1) -> np.ndarray:
     """Textbook paged decode attention in float64.
 
     q: fp16 [S, H, D]; caches: fp16 [NB, bs, Hk, D]; block_tables int32 [S, MB];
     seq_lens int32 [S].  Returns float64 [S, H, D]; with ``pairs`` (a list of
-    (seq, head)) only those rows are computed (the others are NaN).
+    (seq, head)) only those rows are computed (the others are NaN).  With
+    ``workers`` > 1 the (seq, head) rows are split over that many threads.
     """
+    if workers > 1:
+        S, H = q.shape[0], q.shape[1]
+        rows = [tuple(p) for p in pairs] if pairs is not None else \
+            [(i, h) for i in range(S) for h in range(H)]
+        parts = _split_rows(rows, workers)
+        outs = _in_threads(lambda part: decode_attention(
+            q, k_cache, v_cache, block_tables, seq_lens, scale, pairs=part, lib=lib), parts)
+        out = np.full((S, H, q.shape[2]), np.nan, dtype=np.float64)
+        for part, o in zip(parts, outs):
+            idx = tuple(np.asarray(part).T)
+            out[idx] = o[idx]
+        return out
     q = np.ascontiguousarray(q, dtype=np.float16)
     assert k_cache.dtype == np.float16 and v_cache.dtype == np.float16
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
@@ -190,9 +229,12 @@ def quantize_row(x: np.ndarray, lib=None):
 
 
 def cache_write_fp8(cache: np.ndarray, scales: np.ndarray, src: np.ndarray,
-                    slot_mapping: np.ndarray, *, block_size: int, lib=None) -> int:
+                    slot_mapping: np.ndarray, *, block_size: int, lib=None,
+                    workers: int = 1) -> int:
     """Quantize fp16 rows src [T, Hk, D] into cache uint8 [NB, bs, Hk, D] and
-    scales fp32 [NB, bs, Hk] (both in place)."""
+    scales fp32 [NB, bs, Hk] (both in place).  With ``workers`` > 1 and
+    distinct slots (every row then lands in its own place, whatever the
+    order), the tokens are split over that many threads."""
     assert cache.dtype == np.uint8 and scales.dtype == np.float32
     assert cache.flags.c_contiguous and scales.flags.c_contiguous
     NB, bs, Hk, D = cache.shape
@@ -200,6 +242,13 @@ def cache_write_fp8(cache: np.ndarray, scales: np.ndarray, src: np.ndarray,
     src = np.ascontiguousarray(src, dtype=np.float16).reshape(-1, Hk, D)
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     assert src.shape[0] == slots.size
+    if workers > 1 and slots.size > 1 and np.unique(slots).size == slots.size:
+        bounds = np.linspace(0, slots.size, min(workers, slots.size) + 1).astype(np.int64)
+        parts = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        counts = _in_threads(lambda ab: cache_write_fp8(
+            cache, scales, src[ab[0]:ab[1]], slots[ab[0]:ab[1]], block_size=block_size,
+            lib=lib), parts)
+        return int(sum(counts))
     n = (lib or _load()).oracle_cache_write_fp8(_ptr(cache), _ptr(scales), _ptr(src),
                                                 _ptr(slots), slots.size, Hk, D, bs, NB)
     if n < 0:
@@ -208,9 +257,23 @@ def cache_write_fp8(cache: np.ndarray, scales: np.ndarray, src: np.ndarray,
 
 
 def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
-                         scale: float, *, pairs=None, lib=None) -> np.ndarray:
+                         scale: float, *, pairs=None, lib=None, workers: int = 1) -> np.ndarray:
     """Textbook paged decode attention in float64 over E4M3 caches (dequantized
-    exactly: value(code) * scale of the row)."""
+    exactly: value(code) * scale of the row).  ``workers`` as in
+    ``decode_attention``."""
+    if workers > 1:
+        S, H = q.shape[0], q.shape[1]
+        rows = [tuple(p) for p in pairs] if pairs is not None else \
+            [(i, h) for i in range(S) for h in range(H)]
+        parts = _split_rows(rows, workers)
+        outs = _in_threads(lambda part: decode_attention_fp8(
+            q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, scale, pairs=part,
+            lib=lib), parts)
+        out = np.full((S, H, q.shape[2]), np.nan, dtype=np.float64)
+        for part, o in zip(parts, outs):
+            idx = tuple(np.asarray(part).T)
+            out[idx] = o[idx]
+        return out
     q = np.ascontiguousarray(q, dtype=np.float16)
     S, H, D = q.shape
     NB, bs, Hk, D2 = k_cache.shape
@@ -238,15 +301,26 @@ def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, se
 
 def chunk_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                     block_tables: np.ndarray, seq_lens: np.ndarray, query_start: np.ndarray,
-                    scale: float, *, rows=None, lib=None) -> np.ndarray:
+                    scale: float, *, rows=None, lib=None, workers: int = 1) -> np.ndarray:
     """Causal attention of each sequence's last Q_i = query_start[i+1] -
     query_start[i] tokens over its cache, in float64.
 
     q: fp16 [Tq, H, D] (Tq = query_start[-1]); caches fp16 [NB, bs, Hk, D];
     block_tables int32 [S, MB]; seq_lens int32 [S] (tokens in the cache,
     the new ones included).  Returns float64 [Tq, H, D]; with ``rows`` only
-    those query rows are computed (the others are NaN).
+    those query rows are computed (the others are NaN).  With ``workers`` > 1
+    the query rows are split over that many threads.
     """
+    if workers > 1:
+        all_rows = list(range(q.shape[0])) if rows is None else [int(r) for r in rows]
+        parts = _split_rows(all_rows, workers)
+        outs = _in_threads(lambda part: chunk_attention(
+            q, k_cache, v_cache, block_tables, seq_lens, query_start, scale, rows=part,
+            lib=lib), parts)
+        out = np.full(q.shape, np.nan, dtype=np.float64)
+        for part, o in zip(parts, outs):
+            out[part] = o[part]
+        return out
     q = np.ascontiguousarray(q, dtype=np.float16)
     assert k_cache.dtype == np.float16 and v_cache.dtype == np.float16
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous

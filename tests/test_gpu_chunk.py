@@ -50,7 +50,7 @@ def run(wl, reps=1):
 def oracle(orc, wl, rows=None):
     k, v = written_caches(wl)
     return orc.chunk_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.query_start,
-                               wl.scale, rows=rows)
+                               wl.scale, rows=rows, workers=orc.default_workers())
 
 
 SMALL = [
@@ -86,37 +86,28 @@ def test_repeated_calls_are_identical(pkv_lib):
     assert torch.equal(a, dev.out)
 
 
-def _sampled_rows(wl, rng, per_seq=3, seqs=12):
-    rows = set()
-    pick = rng.choice(wl.num_seqs, size=min(seqs, wl.num_seqs), replace=False)
-    for i in pick:
-        r0, r1 = int(wl.query_start[i]), int(wl.query_start[i + 1])
-        if r1 > r0:
-            rows.update([r0, r1 - 1])
-            rows.update(int(x) for x in rng.integers(r0, r1, size=per_seq))
-    return sorted(rows)
-
-
-def test_config6_chunked_prefill_sampled(pkv_lib, orc):
+def test_config6_chunked_prefill(pkv_lib, orc):
+    """The chunked-prefill step: all 63 decodes, and every row of the
+    952-token chunk that starts or ends one of the tile kernel's 128-row query
+    tiles (32 tokens x G 4), plus rows spread over the chunk."""
     wl = W.config6_chunked_prefill()
     _, got = run(wl)
+    G = wl.num_heads // wl.num_kv_heads
+    per_tile = 128 // G
+    r0, r1 = _rows_of(wl, 0)
+    edges = {r for t in range(r0, r1, per_tile) for r in (t, min(t + per_tile, r1) - 1)}
     rng = np.random.default_rng(16)
-    rows = _sampled_rows(wl, rng, seqs=8)
-    # and spread over the 952-token chunk (sequence 0)
-    rows = sorted(set(rows) | {0, 1, 63, 64, 511, 512, 951} |
-                  set(int(x) for x in rng.integers(0, 952, size=12)))
+    rows = sorted(edges | set(range(r1, wl.q.shape[0])) |
+                  set(int(x) for x in rng.integers(r0, r1, size=24)))
     ref = oracle(orc, wl, rows=rows)
     assert_close(got[rows], ref[rows], what="config 6")
     assert np.isfinite(got).all()
 
 
-def test_config7_draft_verify_sampled(pkv_lib, orc):
+def test_config7_draft_verify_all_rows(pkv_lib, orc):
     wl = W.config7_draft_verify()
     _, got = run(wl)
-    rows = _sampled_rows(wl, np.random.default_rng(17))
-    ref = oracle(orc, wl, rows=rows)
-    assert_close(got[rows], ref[rows], what="config 7")
-    assert np.isfinite(got).all()
+    assert_close(got, oracle(orc, wl), what="config 7")
 
 
 def test_sm_split_extremes(pkv_lib, orc):
