@@ -13,20 +13,33 @@ token per sequence.  Synthetic seeded data; the KV cache is resident state.
 
 Prints one JSON line.  `value` is KV-read GB/s of the whole step (key+value
 bytes the decode must read / step time, inputs resident in HBM, L2 flushed
-between timed steps).  `e2e` is the same metric through the public API with
-the step's inputs copied from pinned host memory and the output copied back
-inside the timed region.  `roofline` is the decode kernel's algorithmic bytes
-per launch / its event-timed duration against the measured HBM copy
-bandwidth.  `cpu_baseline` times the float64 oracle on the host.
+between timed steps).  The K-step timed pass is repeated until about a second
+of timed device work has accumulated (`passes`); `value` and `ms_per_step`
+are the median over passes, `spread` gives the 10th / 90th percentiles.
+`e2e` is the same metric through the public API with the step's inputs
+copied from pinned host memory and the output copied back inside the timed
+region.  `roofline` is the decode kernel's algorithmic bytes per launch / its
+event-timed duration against the measured HBM copy bandwidth.
+`cpu_baseline` times the float64 oracle on the host.
+
+With the default workload (N=1) the line also carries `configs`: the other
+workloads of the hot path, each event-timed the same way (L2 flushed before
+every step) with its own roofline and clock record -- long-context decode,
+shared-prefix decode (logical bytes, DRAM bytes and L2 hit rate), the
+two-cache byte-strided write in both layouts (one launch and one launch per
+(cache, layer) view), FP8 decode of the first two, and the multi-token
+steps (chunked prefill, draft verification).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config 2|3|4|6|7] [--compute auto|simt|mma] [--kv fp16|fp8]
+                  [--config 2|3|4|5|6|7] [--compute auto|simt|mma] [--kv fp16|fp8]
+                  [--extras LIST|none]
 
-Configs 6 and 7 time the multi-token step instead: the write of every new
-token's row, then the causal attention of each sequence's new tokens
-(pkv_chunk_attention) -- 6 is one engine step of chunked prefill (a
-952-token prompt chunk beside 63 decodes), 7 is 4-token draft verification
-on 64 sequences.
+Config 5 times the two-cache write alone (MLA 656-byte and indexer 132-byte
+rows, 2 layers, block-outer and layer-outer views).  Configs 6 and 7 time the
+multi-token step instead: the write of every new token's row, then the causal
+attention of each sequence's new tokens (pkv_chunk_attention) -- 6 is one
+engine step of chunked prefill (a 952-token prompt chunk beside 63 decodes),
+7 is 4-token draft verification on 64 sequences.
 """
 
 from __future__ import annotations
@@ -34,6 +47,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import subprocess
 import sys
@@ -49,12 +63,22 @@ METRIC = "paged decode KV-read GB/s (% of HBM peak), seqs/s; cache-write GB/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 
+# the headline's K-step pass is repeated until this much timed device work
+# has accumulated; each `configs` entry gets EXTRA_TIMED_S per timed pass kind
+HEADLINE_TIMED_S = 1.0
+EXTRA_TIMED_S = 0.3
+MAX_PASSES = 4000
+EXTRAS_DEFAULT = "3,4,5,2.fp8,3.fp8,6,7"
+
 WORKLOAD_NAMES = {
     2: "llama3-8b decode layer: S=64, L~U[256,4096], bs=16, H=32, Hk=8, D=128, "
        "fp16 cache [16384,16,8,128], 1 new token/seq written",
     3: "long context: S=8, L=32768, bs=16, H=32, Hk=8, D=128, 16384 shuffled blocks, decode only",
     4: "shared prefix: S=256, 2000-token shared prefix + tail U[1,300], bs=16, H=64, Hk=8, "
        "D=128, 16384 blocks, 1 new token/seq written",
+    5: "two-cache DSA write: 2 layers, bs=64, 4096 blocks, 16384 tokens of random bytes at "
+       "seeded slots (no repeats), MLA 656 B + indexer 132 B rows, block-outer (BLHNC) and "
+       "layer-outer (LBNHC) views",
     6: "chunked-prefill step: 952-token chunk of a 3000-token prompt (positions 2048..2999) + "
        "63 decodes L~U[256,4096], bs=16, H=32, Hk=8, D=128, 16384 shuffled blocks, new rows "
        "written first",
@@ -62,19 +86,25 @@ WORKLOAD_NAMES = {
        "16384 shuffled blocks, new rows written first",
 }
 
-DECODE_SOURCES = [os.path.join(ROOT, "paged_kv_cache_131_gb300", "csrc", f)
+L2_NOTE = ("flushed between timed steps (write a 2x L2 buffer, then read another 2x L2 buffer: "
+           "cold, clean L2)")
+
+CSRC = os.path.join(ROOT, "paged_kv_cache_131_gb300", "csrc")
+DECODE_SOURCES = [os.path.join(CSRC, f)
                   for f in ("pkv_decode_balanced.cu", "pkv_decode_common.cuh", "pkv_device.cuh",
                             "pkv_tensor_map.cu")]
+WRITE_SOURCES = [os.path.join(CSRC, "pkv_write.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_dram_traffic.txt")
+WRITE_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cache_write_kernel_dram_traffic.txt")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 6, 7])
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5, 6, 7])
     ap.add_argument("--compute", choices=["auto", "simt", "mma"], default="auto")
     ap.add_argument("--schedule", choices=["auto", "grid", "balanced"], default="auto")
     ap.add_argument("--kv", choices=["fp16", "fp8"], default="fp16",
@@ -82,7 +112,12 @@ def parse():
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    return ap.parse_args()
+    ap.add_argument("--timed-s", type=float, default=HEADLINE_TIMED_S,
+                    help="repeat the K-step timed pass until this much timed device work")
+    ap.add_argument("--extras", default=EXTRAS_DEFAULT,
+                    help="comma list of other workloads timed into `configs` with the default "
+                         "workload (3, 4, 5, 2.fp8, 3.fp8, 6, 7), or 'none'")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -119,29 +154,62 @@ def host_cpu_info() -> dict:
     return {"host_cpus": os.cpu_count(), "affinity_cpus": aff}
 
 
-def decode_source_hash() -> str:
+# --------------------------------------------------------------------------- ncu records
+
+
+def source_hash(paths) -> str:
     h = hashlib.sha256()
-    for p in DECODE_SOURCES:
+    for p in paths:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_key: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode kernel source (else None)."""
-    if not os.path.exists(TRAFFIC_FILE):
-        return None
+def decode_source_hash() -> str:
+    return source_hash(DECODE_SOURCES)
+
+
+def write_source_hash() -> str:
+    return source_hash(WRITE_SOURCES)
+
+
+def _read_record(path: str, current_hash: str) -> dict:
+    """key = value lines of a committed ncu summary, or {} when the file is
+    missing or was taken on other kernel sources than the current ones."""
+    if not os.path.exists(path):
+        return {}
     rec = {}
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         for line in f:
             if "=" in line and not line.startswith("#"):
                 k, v = line.split("=", 1)
                 rec[k.strip()] = v.strip()
-    if rec.get("source_hash") != decode_source_hash():
-        return None
-    v = rec.get(f"traffic_bytes_per_launch.{workload_key}")
+    return rec if rec.get("source_hash") == current_hash else {}
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    v = _read_record(TRAFFIC_FILE, decode_source_hash()).get(
+        f"traffic_bytes_per_launch.{workload_key}")
     return float(v) if v else None
+
+
+def recorded_decode_value(key: str):
+    """Another figure of the decode ncu record (e.g. an L2 hit rate), same gate."""
+    v = _read_record(TRAFFIC_FILE, decode_source_hash()).get(key)
+    return float(v) if v else None
+
+
+def recorded_write_traffic(workload_key: str):
+    """DRAM bytes per cache-write launch from its committed ncu summary, if it
+    was taken on the current write kernel source (else None)."""
+    v = _read_record(WRITE_TRAFFIC_FILE, write_source_hash()).get(
+        f"traffic_bytes_per_launch.{workload_key}")
+    return float(v) if v else None
+
+
+# --------------------------------------------------------------------------- timing helpers
 
 
 def max_over_ranks(x: float, dist=None, device=None) -> float:
@@ -160,6 +228,52 @@ def whole_job_gbs(bytes_per_rank: int, world: int, step_ms_max: float) -> float:
     """Weak scaling: every rank reads its own replica's bytes each step; the
     job's step takes as long as its slowest rank."""
     return world * bytes_per_rank / (step_ms_max * 1e-3) / 1e9
+
+
+def passes_needed(first_pass_ms: float, min_s: float, max_passes: int = MAX_PASSES) -> int:
+    """Passes (the first included) that bring the timed device work to at
+    least ``min_s`` seconds, given the first pass's total."""
+    if first_pass_ms <= 0:
+        return max_passes
+    return int(min(max_passes, max(1, math.ceil(min_s * 1e3 / first_pass_ms))))
+
+
+def spread(values) -> dict:
+    """Median and 10th / 90th percentiles."""
+    a = np.asarray(values, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90))}
+
+
+def timed_passes(K, step, flush, stream, min_s, split=False, dist=None, device=None):
+    """K-step passes, repeated until ``min_s`` seconds of timed device work.
+
+    ``step(mid)`` enqueues one step; with ``split`` it records the event
+    ``mid`` between the step's two parts (else ``mid`` is None).  L2 is
+    flushed before every step, outside the events.  Returns the per-pass mean
+    step times (ms) and, with ``split``, every step's two part times."""
+    import torch
+
+    means, first, second = [], [], []
+    target = None
+    while target is None or len(means) < target:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            flush()
+            ev[i][0].record(stream)
+            step(ev[i][1] if split else None)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        ms = [e[0].elapsed_time(e[2]) for e in ev]
+        means.append(sum(ms) / K)
+        if split:
+            first += [e[0].elapsed_time(e[1]) for e in ev]
+            second += [e[1].elapsed_time(e[2]) for e in ev]
+        if target is None:
+            target = passes_needed(sum(ms), min_s)
+            # every rank runs the same number of passes
+            target = int(max_over_ranks(float(target), dist, device))
+    return means, first, second
 
 
 class ClockSampler:
@@ -315,8 +429,69 @@ class ChunkOracleSampler:
         return (total_b / total_t / 1e9 if total_t > 0 else 0.0), total_t, n
 
 
+class WriteOracleSampler:
+    """Times the oracle's two-cache write: every (cache, layer) view of one
+    layout per step, alternating block-outer and layer-outer layouts; bytes =
+    rows read + written + the slot mapping once."""
+
+    def __init__(self, wl):
+        import oracle as orc
+
+        orc.build()
+        self.orc, self.wl = orc, wl
+        self.cache = wl.init.copy()
+        self.layouts = sorted(wl.views)
+        self.n = 0
+
+    def step(self):
+        wl = self.wl
+        layout = self.layouts[self.n % len(self.layouts)]
+        self.n += 1
+        nbytes = 8 * wl.slot_mapping.size
+        t0 = time.perf_counter()
+        for c, v in wl.views[layout].items():
+            for layer in range(wl.num_layers):
+                self.orc.cache_write(self.cache, wl.rows[(c, layer)], wl.slot_mapping,
+                                     offset=v.offset, layer=layer, layer_stride=v.layer_stride,
+                                     block_stride=v.block_stride, row_width=v.row_width,
+                                     block_size=wl.block_size, num_blocks=wl.num_blocks)
+                nbytes += 2 * wl.slot_mapping.size * v.row_width
+        return nbytes, time.perf_counter() - t0
+
+    def run(self, steps=None, budget_s=None):
+        total_b, total_t, n = 0, 0.0, 0
+        while (steps is not None and n < steps) or (budget_s is not None and total_t < budget_s):
+            b, t = self.step()
+            total_b, total_t, n = total_b + b, total_t + t, n + 1
+        return (total_b / total_t / 1e9 if total_t > 0 else 0.0), total_t, n
+
+
+def reference_line(args, gbs, t, n, sample):
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / max(n, 1) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64" if args.config != 5 else "u8",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample, **host_cpu_info()},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, wl, rank):
     if rank != 0:
+        return
+    if args.config == 5:
+        sampler = WriteOracleSampler(wl)
+        if args.warmup > 0:
+            sampler.run(steps=args.warmup)
+        gbs, t, n = sampler.run(steps=max(1, args.steps))
+        sample = ("every (cache, layer) view of one layout per step, block-outer and "
+                  "layer-outer alternating, all 16384 tokens; single-threaded")
+        print(json.dumps(reference_line(args, gbs, t, n, sample)), flush=True)
         return
     if args.config in (6, 7):
         sampler = ChunkOracleSampler(wl)
@@ -327,18 +502,7 @@ def run_reference(args, wl, rank):
         gbs, t, n = sampler.run(n_rows, steps=max(1, args.steps))
         sample = (f"{n_rows} query rows (all heads) per step, rotating over all "
                   f"{len(sampler.rows)}; single-threaded float64")
-        line = {
-            "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(t / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
-            "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
-                             "kind": "oracle", "sample": sample, **host_cpu_info()},
-            "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0},
-        }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(reference_line(args, gbs, t, n, sample)), flush=True)
         return
     sampler = OracleSampler(wl)
     t_unit = sampler.calibrate()
@@ -349,18 +513,7 @@ def run_reference(args, wl, rank):
     gbs, t, n = sampler.run(n_units, steps=max(1, args.steps))
     sample = (f"{n_units} (sequence, kv_head) units per step, rotating over all "
               f"{len(sampler.units)}, plus the write of all new rows; single-threaded float64")
-    line = {
-        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT,
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(t / n * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample, **host_cpu_info()},
-        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(reference_line(args, gbs, t, n, sample)), flush=True)
 
 
 # --------------------------------------------------------------------------- our arm
@@ -377,9 +530,21 @@ def chunk_launches_per_step(wl) -> int:
     return 1 + 1 + (2 if rows > 8 * col_tiles else 0)
 
 
-def main_chunk(args, wl, rank, world, local):
-    """Multi-token step: write every new token's row, then the causal
-    attention of each sequence's new tokens."""
+def decode_alg_bytes(wl, kv_bytes: int) -> int:
+    """Algorithmic bytes of one decode launch: the key/value bytes, q in, out,
+    the block-table entries of every sequence's blocks and the lengths."""
+    S, H, D = wl.num_seqs, wl.num_heads, wl.head_dim
+    nblk = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
+    return kv_bytes + S * H * D * 2 * 2 + nblk * 4 + S * 4
+
+
+def check_device_error(pkv):
+    kind, idx = pkv.pkv_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error {pkv.DEVICE_ERRORS.get(kind)} at {idx}")
+
+
+def setup_device(args, local, world):
     import torch
 
     torch.cuda.set_device(local)
@@ -389,35 +554,113 @@ def main_chunk(args, wl, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     import paged_kv_cache_131_gb300 as pkv
     from paged_kv_cache_131_gb300 import _build
-    from paged_kv_cache_131_gb300.harness import DeviceChunk, L2Flush
 
-    if rank == 0 or not os.path.exists(_build.LIB):
+    if int(os.environ.get("RANK", "0")) == 0 or not os.path.exists(_build.LIB):
         _build.build()
     if dist is not None:
         dist.barrier()
+    return pkv, dist
+
+
+def measure_decode(wl, args, kv, local, flush, stream, min_s, dist=None, compute=0, schedule=0,
+                   partition=0):
+    """Warm up, then time the decode step (write + decode) in K-step passes:
+    whole steps, then with an event between the write and the decode for each
+    kernel's own time.  Returns the device staging and the measurements."""
+    import torch
+
+    import paged_kv_cache_131_gb300 as pkv
+    from paged_kv_cache_131_gb300.harness import DeviceDecode, DeviceDecodeFp8
+
+    if kv == "fp8":
+        dev = DeviceDecodeFp8(wl, device=f"cuda:{local}")
+    else:
+        dev = DeviceDecode(wl, device=f"cuda:{local}", partition_size=partition,
+                           compute=compute, schedule=schedule)
+
+    def step(mid):
+        dev.write()
+        if mid is not None:
+            mid.record(stream)
+        dev.decode()
+
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        step(None)
+    torch.cuda.synchronize()
+    check_device_error(pkv)
+    K = args.steps
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        means, _, _ = timed_passes(K, step, flush, stream, min_s, dist=dist,
+                                   device=f"cuda:{local}")
+        t_wall = time.perf_counter() - t_wall
+        split_means, w_ms, d_ms = timed_passes(K, step, flush, stream, min_s / 2, split=True,
+                                               dist=dist, device=f"cuda:{local}")
+    check_device_error(pkv)
+    launches = (1 if dev.has_write else 0) + 1
+    return dev, {
+        "step_passes": means, "write_ms": w_ms, "decode_ms": d_ms, "clocks": clocks.summary(),
+        "wall_s": t_wall, "passes": len(means), "split_passes": len(split_means),
+        "gpu_launches": launches * K * (len(means) + len(split_means)),
+    }
+
+
+def decode_entry(key, wl, dev, m, kv, peak, peak_kind):
+    """One `configs` entry for a decode workload."""
+    kv_bytes = dev.kv_bytes() if kv == "fp8" else wl.kv_bytes()
+    alg = decode_alg_bytes(wl, kv_bytes)
+    st, dk = spread(m["step_passes"]), spread(m["decode_ms"])
+    achieved = alg / (dk["median"] * 1e-3) / 1e9
+    entry = {
+        "workload": WORKLOAD_NAMES[int(key.split(".")[0])] + (", FP8 (E4M3) cache" if kv == "fp8"
+                                                               else ""),
+        "kv": kv,
+        "value": round(kv_bytes / (st["median"] * 1e-3) / 1e9, 2), "unit": UNIT,
+        "ms_per_step": round(st["median"], 5),
+        "ms_per_step_p10_p90": [round(st["p10"], 5), round(st["p90"], 5)],
+        "decode_kernel_ms": round(dk["median"], 5),
+        "decode_kernel_ms_p10_p90": [round(dk["p10"], 5), round(dk["p90"], 5)],
+        "seqs_per_s": round(wl.num_seqs / (st["median"] * 1e-3), 1),
+        "passes": m["passes"], "steps": len(m["decode_ms"]) // max(m["split_passes"], 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(f"config{key.split('.')[0]}.{kv}"),
+                     "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+                     "kernel": "decode_balanced_kernel" + (" (FP8 MMA policy)" if kv == "fp8"
+                                                           else " (MMA policy)"),
+                     "alg_bytes_per_launch": alg},
+        "gpu_launches": m["gpu_launches"],
+        "clocks": m["clocks"],
+    }
+    if dev.has_write:
+        wk = spread(m["write_ms"])
+        entry["write_kernel_ms"] = round(wk["median"], 5)
+    return entry
+
+
+def measure_chunk(wl, args, local, flush, stream, min_s, dist=None):
+    """The multi-token step (write + attention call), captured as CUDA graphs
+    and replayed: whole steps, then write and call with an event between."""
+    import torch
+
+    import paged_kv_cache_131_gb300 as pkv
+    from paged_kv_cache_131_gb300.harness import DeviceChunk
+
     dev = DeviceChunk(wl, device=f"cuda:{local}")
-    flush = L2Flush(f"cuda:{local}")
-    stream = torch.cuda.current_stream()
-    kv_bytes = wl.kv_bytes()
-    flops = wl.flops()
-    Tq, H, D = wl.q.shape
-    nblk = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
-    # algorithmic bytes of the attention: every sequence's K and V once, q in,
-    # out, block tables, lengths and query offsets
-    attn_bytes = kv_bytes + Tq * H * D * 2 * 2 + nblk * 4 + wl.num_seqs * 8 + 4
-    for _ in range(args.warmup):
+    for _ in range(max(args.warmup, 3)):
         flush()
         dev.step()
     torch.cuda.synchronize()
-    kind, idx = pkv.pkv_get_device_error()
-    if kind:
-        raise RuntimeError(f"device error {pkv.DEVICE_ERRORS.get(kind)} at {idx}")
-    K = args.steps
+    check_device_error(pkv)
     # the step's launches (write; one or two attention kernels and the plan
     # kernel) are captured once as CUDA graphs and replayed, so no Python
-    # enqueue sits inside the timed region
-    # (one graph for the whole step, so the attention call may overlap the
-    # write's tail as it does on a stream; two for the pass that times each)
+    # enqueue sits inside the timed region (one graph for the whole step, so
+    # the attention call may overlap the write's tail as it does on a stream;
+    # two for the pass that times each)
     g_step, g_write, g_attend = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
                                  torch.cuda.CUDAGraph())
     with torch.cuda.graph(g_step):
@@ -429,42 +672,41 @@ def main_chunk(args, wl, rank, world, local):
         dev.attend()
     torch.cuda.synchronize()
 
-    def timed_loop(split: bool):
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-        for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            if split:
-                g_write.replay()
-                ev[i][1].record(stream)
-                g_attend.replay()
-            else:
-                g_step.replay()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
-        step = sum(e[0].elapsed_time(e[2]) for e in ev) / K
-        if not split:
-            return step, None, None
-        return (step, float(np.median([e[0].elapsed_time(e[1]) for e in ev])),
-                float(np.median([e[1].elapsed_time(e[2]) for e in ev])))
+    def step(mid):
+        if mid is None:
+            g_step.replay()
+        else:
+            g_write.replay()
+            mid.record(stream)
+            g_attend.replay()
 
+    K = args.steps
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        step_ms, _, _ = timed_loop(split=False)
-        _, write_ms, attn_ms = timed_loop(split=True)
-    if dist is not None:
-        step_ms = max_over_ranks(step_ms, dist, f"cuda:{local}")
-        dist.barrier()
-    if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
-        return
-    peak_hbm, peak_kind = measured_peaks()
+        means, _, _ = timed_passes(K, step, flush, stream, min_s, dist=dist,
+                                   device=f"cuda:{local}")
+        split_means, w_ms, a_ms = timed_passes(K, step, flush, stream, min_s / 2, split=True,
+                                               dist=dist, device=f"cuda:{local}")
+    check_device_error(pkv)
+    Tq, H, D = wl.q.shape
+    nblk = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
+    # algorithmic bytes of the attention: every sequence's K and V once, q in,
+    # out, block tables, lengths and query offsets
+    attn_bytes = wl.kv_bytes() + Tq * H * D * 2 * 2 + nblk * 4 + wl.num_seqs * 8 + 4
+    return dev, {"step_passes": means, "write_ms": w_ms, "attn_ms": a_ms,
+                 "clocks": clocks.summary(), "passes": len(means),
+                 "split_passes": len(split_means), "attn_bytes": attn_bytes,
+                 "gpu_launches": chunk_launches_per_step(wl) * K * (len(means) +
+                                                                    len(split_means))}
+
+
+def chunk_roofline(wl, m, peak_hbm, peak_kind):
     peak_tf = measured_bf16_tflops()
-    value = whole_job_gbs(kv_bytes, world, step_ms)
-    gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
+    attn_ms = spread(m["attn_ms"])["median"]
+    flops = wl.flops()
+    gbs = m["attn_bytes"] / (attn_ms * 1e-3) / 1e9
     tfs = flops / (attn_ms * 1e-3) / 1e12
     hbm_frac, tf_frac = gbs / peak_hbm, tfs / peak_tf
     if hbm_frac >= tf_frac:
@@ -480,10 +722,161 @@ def main_chunk(args, wl, rank, world, local):
     # the balanced decode schedule, longer ones on the tcgen05 tile kernel
     roof.update({"kernel": "attention call (decode_balanced_kernel for short chunks, "
                            "chunk_attention_kernel on tcgen05 for the rest)",
-                 "alg_bytes_per_launch": attn_bytes,
+                 "alg_bytes_per_launch": m["attn_bytes"],
                  "flops_per_launch": flops, "achieved_gbs": round(gbs, 1),
                  "achieved_tflops": round(tfs, 2), "hbm_frac": round(hbm_frac, 4),
                  "tensor_frac": round(tf_frac, 4)})
+    return roof, attn_ms
+
+
+def chunk_entry(key, wl, m, peak, peak_kind):
+    roof, attn_ms = chunk_roofline(wl, m, peak, peak_kind)
+    st, ak = spread(m["step_passes"]), spread(m["attn_ms"])
+    Tq = wl.q.shape[0]
+    return {
+        "workload": WORKLOAD_NAMES[int(key)],
+        "value": round(wl.kv_bytes() / (st["median"] * 1e-3) / 1e9, 2), "unit": UNIT,
+        "ms_per_step": round(st["median"], 5),
+        "ms_per_step_p10_p90": [round(st["p10"], 5), round(st["p90"], 5)],
+        "attention_call_ms": round(attn_ms, 5),
+        "attention_call_ms_p10_p90": [round(ak["p10"], 5), round(ak["p90"], 5)],
+        "write_kernel_ms": round(spread(m["write_ms"])["median"], 5),
+        "query_tokens_per_s": round(Tq / (st["median"] * 1e-3), 1),
+        "passes": m["passes"], "roofline": roof, "gpu_launches": m["gpu_launches"],
+        "clocks": m["clocks"],
+    }
+
+
+def measure_write(wl, args, local, flush, stream, min_s, peak, peak_kind, dist=None):
+    """The two-cache write of config 5: for each layout, all (cache, layer)
+    views in one launch and in one launch per view.  Returns the device
+    staging and the entries per layout and mode."""
+    import torch
+
+    import paged_kv_cache_131_gb300 as pkv
+    from paged_kv_cache_131_gb300.harness import DeviceWrite
+
+    dev = DeviceWrite(wl, device=f"cuda:{local}")
+    out = {}
+    K = args.steps
+    for layout in ("BLHNC", "LBNHC"):
+        out[layout] = {}
+        alg = dev.layout_bytes(layout)
+        for mode, fn in (("one_launch", dev.write_layout_batched),
+                         ("per_view_launches", dev.write_layout)):
+            nviews = len(wl.views[layout]) * wl.num_layers
+            for _ in range(max(args.warmup, 3)):
+                flush()
+                fn(layout)
+            torch.cuda.synchronize()
+            check_device_error(pkv)
+            if dist is not None:
+                dist.barrier()
+            with ClockSampler(local) as clocks:
+                means, _, _ = timed_passes(K, lambda mid: fn(layout), flush, stream, min_s,
+                                           dist=dist, device=f"cuda:{local}")
+            check_device_error(pkv)
+            sp = spread(means)
+            gbs = alg / (sp["median"] * 1e-3) / 1e9
+            launches = 1 if mode == "one_launch" else nviews
+            out[layout][mode] = {
+                "ms": round(sp["median"], 5), "ms_p10_p90": [round(sp["p10"], 5),
+                                                             round(sp["p90"], 5)],
+                "value": round(gbs, 2), "unit": UNIT,
+                "tokens_per_s": round(wl.slot_mapping.size / (sp["median"] * 1e-3), 1),
+                "launches_per_step": launches, "passes": len(means),
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                             "unit": "GB/s", "frac": round(gbs / peak, 4),
+                             "traffic": recorded_write_traffic(f"config5.{layout}.{mode}"),
+                             "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+                             "kernel": "cache_write_kernel",
+                             "alg_bytes_per_launch" if launches == 1 else "alg_bytes_per_step":
+                                 alg},
+                "gpu_launches": launches * K * len(means),
+                "clocks": clocks.summary(),
+            }
+    return dev, out
+
+
+def run_extras(args, keys, local, flush, stream, peak, peak_kind):
+    """The `configs` entries: every other workload, measured one after the
+    other on this GPU (each staged, timed and freed in turn)."""
+    import torch
+
+    from paged_kv_cache_131_gb300 import workloads as W
+
+    out = {}
+    for key in keys:
+        cfg = int(key.split(".")[0])
+        kv = "fp8" if key.endswith(".fp8") else "fp16"
+        wl = W.config(cfg)
+        if cfg == 5:
+            dev, entry = measure_write(wl, args, local, flush, stream, EXTRA_TIMED_S, peak,
+                                       peak_kind)
+            entry = {"workload": WORKLOAD_NAMES[5], **entry}
+        elif cfg in (6, 7):
+            dev, m = measure_chunk(wl, args, local, flush, stream, EXTRA_TIMED_S)
+            entry = chunk_entry(key, wl, m, peak, peak_kind)
+        else:
+            dev, m = measure_decode(wl, args, kv, local, flush, stream, EXTRA_TIMED_S)
+            entry = decode_entry(key, wl, dev, m, kv, peak, peak_kind)
+            if cfg == 4:
+                # the shared prefix is read once from DRAM and then from L2:
+                # logical bytes per second, and the DRAM bytes / L2 hit rate of
+                # the committed ncu record for this kernel source
+                entry["logical_kv_gbs"] = round(
+                    wl.kv_bytes() / (entry["decode_kernel_ms"] * 1e-3) / 1e9, 1)
+                entry["dram_bytes_per_launch"] = entry["roofline"]["traffic"]
+                entry["l2_sector_hit_rate_pct"] = recorded_decode_value(
+                    f"l2_sector_hit_rate_pct.config4.{kv}")
+                entry["unique_kv_bytes"] = unique_kv_bytes(wl)
+        out[key] = entry
+        del dev
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+def unique_kv_bytes(wl) -> int:
+    """Key+value bytes of the distinct (physical block, in-block slot) rows
+    the sequences read: the shared prefix counted once."""
+    seen = set()
+    for i, L in enumerate(wl.seq_lens):
+        L = int(L)
+        nb = -(-L // wl.block_size)
+        for j in range(nb):
+            rows = min(wl.block_size, L - j * wl.block_size)
+            seen.add((int(wl.block_tables[i, j]), rows))
+    # a block shared by several sequences is read up to its longest use
+    longest = {}
+    for b, rows in seen:
+        longest[b] = max(longest.get(b, 0), rows)
+    return sum(longest.values()) * wl.num_kv_heads * wl.head_dim * 4
+
+
+def main_chunk(args, wl, rank, world, local):
+    """Multi-token step: write every new token's row, then the causal
+    attention of each sequence's new tokens."""
+    import torch
+
+    pkv, dist = setup_device(args, local, world)
+    from paged_kv_cache_131_gb300.harness import L2Flush
+
+    flush = L2Flush(f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    dev, m = measure_chunk(wl, args, local, flush, stream, args.timed_s, dist=dist)
+    st = spread(m["step_passes"])
+    step_ms = max_over_ranks(st["median"], dist, f"cuda:{local}")
+    if dist is not None:
+        dist.barrier()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peak_hbm, peak_kind = measured_peaks()
+    roof, attn_ms = chunk_roofline(wl, m, peak_hbm, peak_kind)
+    kv_bytes = wl.kv_bytes()
+    Tq = wl.q.shape[0]
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         sampler = ChunkOracleSampler(wl)
@@ -496,12 +889,14 @@ def main_chunk(args, wl, rank, world, local):
                          f"{t_cpu:.1f} s single-threaded float64"}
     line = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": round(whole_job_gbs(kv_bytes, world, step_ms), 2),
         "unit": UNIT,
         "n_gpus": world,
-        "steps": K,
+        "steps": args.steps,
         "warmup": args.warmup,
+        "passes": m["passes"],
         "ms_per_step": round(step_ms, 5),
+        "spread": {"ms_per_step_p10": round(st["p10"], 5), "ms_per_step_p90": round(st["p90"], 5)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -509,17 +904,99 @@ def main_chunk(args, wl, rank, world, local):
         "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
         "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": wl.num_seqs * world,
                    "query_tokens": Tq, "seq_len": int(wl.max_seq_len),
-                   "parallelism": f"replicas x{world}",
-                   "l2": "flushed between timed steps (write a 2x L2 buffer, then read another "
-                         "2x L2 buffer: cold, clean L2)",
+                   "parallelism": f"replicas x{world}", "l2": L2_NOTE,
                    "kv_cache": "resident in HBM (state), not copied per step"},
         "query_tokens_per_s": round(world * Tq / (step_ms * 1e-3), 1),
         "attention_kernel_ms": round(attn_ms, 5),
-        "write_kernel_ms": round(write_ms, 5),
+        "write_kernel_ms": round(spread(m["write_ms"])["median"], 5),
         "roofline": roof,
         "e2e": None,
-        "gpu_launches": chunk_launches_per_step(wl) * K,
-        "clocks": clocks.summary(),
+        "gpu_launches": m["gpu_launches"],
+        "clocks": m["clocks"],
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main_write(args, wl, rank, world, local):
+    """Config 5: the two-cache byte-strided write.  Headline = the block-outer
+    layout's four (cache, layer) writes in one launch."""
+    import torch
+
+    pkv, dist = setup_device(args, local, world)
+    from paged_kv_cache_131_gb300.harness import L2Flush
+
+    flush = L2Flush(f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    dev, entries = measure_write(wl, args, local, flush, stream, args.timed_s / 4, peak,
+                                 peak_kind, dist=dist)
+    head = entries["BLHNC"]["one_launch"]
+    step_ms = max_over_ranks(head["ms"], dist, f"cuda:{local}")
+    alg = dev.layout_bytes("BLHNC")
+
+    # end to end through the API from pinned host memory: every step copies
+    # the rows and slot mapping in (one packed copy), writes, and reads the
+    # device error word back (the write's result is the cache itself)
+    host = dev.host_inputs(pinned=True)
+    e2e_ms = []
+    for i in range(5 + args.e2e_steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dev.inputs.copy_(host, non_blocking=True)
+        dev.write_layout_batched("BLHNC")
+        kind, _ = pkv.pkv_get_device_error()
+        e1.record(stream)
+        e1.synchronize()
+        if kind:
+            raise RuntimeError(f"device error {pkv.DEVICE_ERRORS.get(kind)}")
+        if i >= 5:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_med = float(np.median(e2e_ms))
+    if dist is not None:
+        dist.barrier()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs_cpu, t_cpu, n_cpu = WriteOracleSampler(wl).run(budget_s=10.0)
+        cpu = {"value": round(gbs_cpu, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               **host_cpu_info(),
+               "sample": f"{n_cpu} steps of every (cache, layer) view of one layout, "
+                         f"{t_cpu:.1f} s single-threaded"}
+    line = {
+        "metric": METRIC,
+        "value": round(whole_job_gbs(alg, world, step_ms), 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "passes": head["passes"],
+        "ms_per_step": round(step_ms, 5),
+        "spread": {"ms_per_step_p10": head["ms_p10_p90"][0],
+                   "ms_per_step_p90": head["ms_p10_p90"][1]},
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8",
+        "data": "synthetic (seeded random bytes, slots drawn without replacement)",
+        "config": {"workload": WORKLOAD_NAMES[5], "global_batch": int(wl.slot_mapping.size),
+                   "parallelism": f"replicas x{world}", "l2": L2_NOTE,
+                   "headline": "block-outer (BLHNC) layout, 4 (cache, layer) views in one launch"},
+        "cache_write_gbs": head["value"],
+        "roofline": head["roofline"],
+        "layouts": entries,
+        "e2e": {"value": round(alg / (e2e_med * 1e-3) / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(host.numel()), "d2h_bytes_per_step": 8,
+                "ms_per_step": round(e2e_med, 5)},
+        "gpu_launches": sum(e["gpu_launches"] for lay in entries.values()
+                            for e in lay.values()),
+        "clocks": head["clocks"],
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
@@ -539,92 +1016,48 @@ def main():
     if args.config in (6, 7):
         main_chunk(args, wl, rank, world, local)
         return
+    if args.config == 5:
+        main_write(args, wl, rank, world, local)
+        return
 
     import torch
 
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    pkv, dist = setup_device(args, local, world)
+    from paged_kv_cache_131_gb300.harness import L2Flush
 
-    import paged_kv_cache_131_gb300 as pkv
-    from paged_kv_cache_131_gb300 import _build
-    from paged_kv_cache_131_gb300.harness import DeviceDecode, L2Flush
-
-    if rank == 0 or not os.path.exists(_build.LIB):
-        _build.build()
-    if dist is not None:
-        dist.barrier()
     compute = {"auto": 0, "simt": 1, "mma": 2}[args.compute]
     schedule = {"auto": 0, "grid": 1, "balanced": 2}[args.schedule]
-    if args.kv == "fp8":
-        from paged_kv_cache_131_gb300.harness import DeviceDecodeFp8
-        dev = DeviceDecodeFp8(wl, device=f"cuda:{local}")
-    else:
-        dev = DeviceDecode(wl, device=f"cuda:{local}", partition_size=args.partition,
-                           compute=compute, schedule=schedule)
     flush = L2Flush(f"cuda:{local}")
     stream = torch.cuda.current_stream()
-
+    dev, m = measure_decode(wl, args, args.kv, local, flush, stream, args.timed_s, dist=dist,
+                            compute=compute, schedule=schedule, partition=args.partition)
     kv_bytes = dev.kv_bytes() if args.kv == "fp8" else wl.kv_bytes()
-    S, H, D = wl.num_seqs, wl.num_heads, wl.head_dim
-    nblk = int(sum(-(-int(L) // wl.block_size) for L in wl.seq_lens))
-    decode_alg_bytes = kv_bytes + S * H * D * 2 * 2 + nblk * 4 + S * 4
+    S = wl.num_seqs
+    alg = decode_alg_bytes(wl, kv_bytes)
     if args.kv == "fp8":
         t = wl.slot_mapping.size if dev.has_write else 0
         write_bytes = t * wl.num_kv_heads * (wl.head_dim * 3 + 4) * 2 + 8 * t
     else:
         write_bytes = dev.write_bytes()
-    launches_per_step = (1 if dev.has_write else 0) + 1
-
-    for _ in range(args.warmup):
-        flush()
-        dev.step()
-    torch.cuda.synchronize()
-    kind, idx = pkv.pkv_get_device_error()
-    if kind:
-        raise RuntimeError(f"device error {pkv.DEVICE_ERRORS.get(kind)} at {idx}")
-
-    K = args.steps
-
-    def timed_loop(split: bool):
-        """K steps, L2 flushed before each (outside the events).  Without
-        `split` only the step's ends are marked, so the decode launch may
-        overlap the write kernel's tail as it does in use; with `split` an
-        event between them gives each kernel's own duration."""
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-        for i in range(K):
-            flush()
-            ev[i][0].record(stream)
-            dev.write()
-            if split:
-                ev[i][1].record(stream)
-            dev.decode()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
-        step = sum(e[0].elapsed_time(e[2]) for e in ev) / K
-        if not split:
-            return step, None, None
-        # per-kernel durations: medians, so a step where the host fell behind
-        # the GPU (launch latency landing between two events) does not skew them
-        return (step, float(np.median([e[0].elapsed_time(e[1]) for e in ev])),
-                float(np.median([e[1].elapsed_time(e[2]) for e in ev])))
-
+    st = spread(m["step_passes"])
+    step_ms = max_over_ranks(st["median"], dist, f"cuda:{local}")
+    decode_ms = spread(m["decode_ms"])["median"]
+    write_ms = spread(m["write_ms"])["median"] if dev.has_write else None
     if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_wall = time.perf_counter()
-        step_ms, _, _ = timed_loop(split=False)
-        t_wall = time.perf_counter() - t_wall
-        _, write_ms, decode_ms = timed_loop(split=True)
-    if dist is not None:
-        step_ms = max_over_ranks(step_ms, dist, f"cuda:{local}")
         dist.barrier()
 
     # end to end through the public API: pinned host inputs in, output out
     e2e = e2e_measure(dev, wl, args.e2e_steps, stream, flush) if args.kv == "fp16" else None
+
+    extras = None
+    keys = [] if args.extras in ("", "none") else args.extras.split(",")
+    if (rank == 0 and world == 1 and keys and args.config == 2 and args.kv == "fp16"
+            and compute == 0 and schedule == 0 and args.partition == 0):
+        del dev
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        peak, peak_kind = measured_peaks()
+        extras = run_extras(args, keys, local, flush, stream, peak, peak_kind)
 
     if rank != 0:
         if dist is not None:
@@ -632,7 +1065,7 @@ def main():
         return
     peak, peak_kind = measured_peaks()
     value = whole_job_gbs(kv_bytes, world, step_ms)
-    achieved = decode_alg_bytes / (decode_ms * 1e-3) / 1e9
+    achieved = alg / (decode_ms * 1e-3) / 1e9
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         sampler = OracleSampler(wl)
@@ -646,9 +1079,13 @@ def main():
         "value": round(value, 2),
         "unit": UNIT,
         "n_gpus": world,
-        "steps": K,
+        "steps": args.steps,
         "warmup": args.warmup,
+        "passes": m["passes"],
         "ms_per_step": round(step_ms, 5),
+        "spread": {"ms_per_step_p10": round(st["p10"], 5), "ms_per_step_p90": round(st["p90"], 5),
+                   "value_p10": round(whole_job_gbs(kv_bytes, world, st["p90"]), 2),
+                   "value_p90": round(whole_job_gbs(kv_bytes, world, st["p10"]), 2)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -656,8 +1093,7 @@ def main():
         "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
         "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": S * world,
                    "seq_len": int(wl.max_seq_len), "parallelism": f"replicas x{world}",
-                   "l2": "flushed between timed steps (write a 2x L2 buffer, then read another "
-                         "2x L2 buffer: cold, clean L2); KV read per step > L2",
+                   "l2": L2_NOTE + "; KV read per step > L2",
                    "kv_cache": "resident in HBM (state), not copied per step",
                    "compute": args.compute, "schedule": args.schedule, "kv": args.kv},
         "pct_hbm_peak": round(100 * value / world / peak, 2),
@@ -665,8 +1101,8 @@ def main():
         "decode_tokens_per_s": round(world * S / (step_ms * 1e-3), 1),
         "cache_write_gbs": round(write_bytes / (write_ms * 1e-3) / 1e9, 2) if write_bytes else None,
         "decode_kernel_ms": round(decode_ms, 5),
-        "write_kernel_ms": round(write_ms, 5),
-        "wall_s_timed_loop": round(t_wall, 3),
+        "write_kernel_ms": round(write_ms, 5) if write_ms is not None else None,
+        "wall_s_timed_loop": round(m["wall_s"], 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      # recorded for the balanced schedule with the MMA policies only
@@ -677,12 +1113,14 @@ def main():
                                 "decode_balanced_kernel") +
                                (" (FP8 MMA policy)" if args.kv == "fp8" else
                                 " (SIMT policy)" if compute == 1 else " (MMA policy)"),
-                     "alg_bytes_per_launch": decode_alg_bytes},
+                     "alg_bytes_per_launch": alg},
         "e2e": e2e,
-        "gpu_launches": launches_per_step * K,
-        "clocks": clocks.summary(),
+        "gpu_launches": m["gpu_launches"],
+        "clocks": m["clocks"],
         "cpu_baseline": cpu,
     }
+    if extras is not None:
+        line["configs"] = extras
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -718,7 +1156,7 @@ def e2e_measure(dev, wl, steps, stream, flush):
         one()
         e1.record(stream)
     torch.cuda.synchronize()
-    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / steps
+    ms = float(np.median([e0.elapsed_time(e1) for e0, e1 in ev]))
     return {"value": round(wl.kv_bytes() / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 5)}

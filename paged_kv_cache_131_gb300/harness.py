@@ -187,8 +187,35 @@ class DeviceWrite:
     def __init__(self, wl: WriteWorkload, device="cuda"):
         self.wl = wl
         self.cache = to_dev(wl.init, device)
-        self.slot_mapping = to_dev(wl.slot_mapping, device)
-        self.rows = {key: to_dev(r, device) for key, r in wl.rows.items()}
+        # the per-step inputs (every (cache, layer) row set and the slot
+        # mapping) live in one device buffer at 256-byte aligned offsets, so a
+        # host step can bring them in with a single copy
+        fields = [(key, r) for key, r in wl.rows.items()] + [("slot_mapping", wl.slot_mapping)]
+        self._layout, off = [], 0
+        for key, a in fields:
+            a = np.ascontiguousarray(a)
+            self._layout.append((key, off, a.dtype, a.shape))
+            off += (a.nbytes + 255) // 256 * 256
+        self.inputs_nbytes = off
+        self.inputs = self.host_inputs(pinned=False).to(device)
+        self.rows = {}
+        for key, o, dtype, shape in self._layout:
+            n = int(np.prod(shape)) * np.dtype(dtype).itemsize
+            t = self.inputs[o:o + n].view(torch.from_numpy(np.empty(0, dtype)).dtype).view(shape)
+            if key == "slot_mapping":
+                self.slot_mapping = t
+            else:
+                self.rows[key] = t
+
+    def host_inputs(self, pinned: bool = True) -> torch.Tensor:
+        """The per-step inputs packed as in ``self.inputs`` (uint8, host)."""
+        buf = np.zeros(self.inputs_nbytes, dtype=np.uint8)
+        for key, o, dtype, shape in self._layout:
+            src = self.wl.slot_mapping if key == "slot_mapping" else self.wl.rows[key]
+            a = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
+            buf[o:o + a.size] = a
+        t = torch.from_numpy(buf)
+        return t.pin_memory() if pinned else t
 
     def reset(self) -> None:
         self.cache.copy_(torch.from_numpy(self.wl.init))
@@ -218,9 +245,12 @@ class DeviceWrite:
         return 1
 
     def layout_bytes(self, layout: str) -> int:
+        """Algorithmic bytes of one layout's writes: every row read once and
+        written once, plus the slot mapping read once (it is shared by all
+        (cache, layer) views)."""
         t = self.wl.slot_mapping.size
         per = sum(v.row_width for v in self.wl.views[layout].values()) * self.wl.num_layers
-        return 2 * t * per + 8 * t * len(self.wl.views[layout]) * self.wl.num_layers
+        return 2 * t * per + 8 * t
 
 
 class DeviceChunk:
