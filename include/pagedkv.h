@@ -95,8 +95,8 @@ typedef struct pkv_view {
  *  Rows are copied byte for byte (no conversion); 16-byte vectors are used
  *  when every address and stride allows, else 8, 4, 2 or 1 byte.
  *  Returns PKV_OK (num_tokens == 0 launches nothing), PKV_ERR_NULL,
- *  PKV_ERR_INVALID (block_size <= 0, num_blocks <= 0, row_width <= 0,
- *  block_stride <= 0, offset/layer/layer_stride < 0), PKV_ERR_CUDA.
+ *  PKV_ERR_INVALID (block_size <= 0, num_blocks <= 0, row_width <= 0 or
+ *  > 2^30, block_stride <= 0, offset/layer/layer_stride < 0), PKV_ERR_CUDA.
  */
 int pkv_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
                     int64_t num_tokens, void *k_cache, void *v_cache, pkv_view view,
@@ -117,8 +117,8 @@ typedef struct pkv_write_desc {
  * address of slot_mapping[t] in d's view, exactly as pkv_cache_write does.
  * This is how every layer and cache of one block table is written at once:
  * the two caches (MLA and indexer) of "vLLM KV Cache Layout 可视化" --
- * 两种 cache 共用一张 block table share a slot_mapping ("MLA 和 indexer 共用
- * 同一个值", 查一个 token).
+ * 两种 cache 共用一张 block table share one slot number per token (查一个
+ * token).
  *  descs       HOST array of num_descs (0..PKV_MAX_WRITE_DESCS) descriptors;
  *              read during the call only.  Rows of different descriptors must
  *              not overlap in memory (which lands is then unspecified).
@@ -166,8 +166,9 @@ int pkv_copy_blocks(void *cache, pkv_view view, int32_t num_layers, int32_t bloc
  *
  * Two schedules (pkv_decode_options.schedule):
  *  - balanced (default): one wave of persistent CTAs, each owning an equal
- *    share of all sequences' blocks; needs num_kv_heads <= 8 and a workspace
- *    of pkv_decode_workspace_bytes(...) bytes;
+ *    share of all (KV head group, sequence, block) triples -- a CTA serves up
+ *    to 8 KV heads of one group, so more KV heads make more groups; needs a
+ *    workspace of pkv_decode_workspace_bytes(...) bytes;
  *  - grid: one CTA per (kv head, sequence, partition of 512 tokens); needs a
  *    workspace only when max_seq_len > 512.
  * With AUTO the balanced schedule runs when the shape and the workspace
@@ -280,7 +281,7 @@ int pkv_cache_write_fp8(const void *k, const void *v, const int64_t *slot_mappin
  * pkv_decode_attention over FP8 caches (balanced schedule, MMA policy): keys
  * and values are dequantized as value(code) * scale of their row; the result
  * is the attention of pkv_decode_attention on those values.  Needs
- * num_kv_heads <= 8, 16-byte aligned caches and scales, and a workspace of
+ * 16-byte aligned caches and scales and a workspace of
  * pkv_decode_workspace_bytes(...) bytes (zero-filled before first use, left
  * zero-filled).  Other arguments and errors as pkv_decode_attention.
  */

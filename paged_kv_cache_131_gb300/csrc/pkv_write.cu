@@ -6,15 +6,20 @@
 // One launch serves a list of write descriptors that share one slot_mapping
 // (K and V of a layer, or every (cache, layer) view of a multi-cache layout
 // such as the two-cache MLA + indexer example of "两种 cache 共用一张 block
-// table").  One warp per token, grid-stride over tokens: the warp splits the
-// slot once and copies the token's row for every descriptor, each with the
-// widest vector (16, 8, 4, 2 or 1 bytes) its addresses and strides allow (a
-// kernel instance per width when all descriptors share one, else one that
-// switches per descriptor).
-// This is a byte copy bound by HBM bandwidth, or by latency for small calls.
+// table").  The work is cut into items: for one descriptor, a batch of
+// consecutive tokens whose source rows -- contiguous in the source -- fill
+// about 16 KB.  A CTA takes an item, issues the loads of the whole batch at
+// once (perfectly coalesced, every thread a few vectors of the widest size
+// the descriptor's addresses and strides allow), meanwhile splits the
+// batch's slots into destination offsets in shared memory, then stores each
+// vector at its token's destination row.  Every load of a batch is in
+// flight together, so the copy is not one round trip per row; the CTAs are
+// small (8 KB of shared memory) and fit beside the decode kernel that may
+// start early on the same SMs (see below).
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 
 #include "../../include/pagedkv.h"
@@ -25,15 +30,19 @@ namespace pkv {
 namespace {
 
 constexpr int kWriteThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kVecsPerThread = 4;
+constexpr int kBatchVecs = kWriteThreads * kVecsPerThread;  // vectors of one item
 constexpr int kMaxDescs = PKV_MAX_WRITE_DESCS;
+constexpr int64_t kMaxRowWidth = int64_t(1) << 30;  // byte offsets in a batch stay 32-bit
 
 struct Desc {
     const uint8_t *src;  // num_tokens rows of row_width bytes
     uint8_t *dst;        // cache + view.offset + view.layer * view.layer_stride
     int64_t block_stride;
-    int64_t row_width;
-    int32_t vec;         // bytes per vector: 16, 8, 4, 2 or 1
+    int64_t item0;       // first item of this descriptor
+    int32_t row_width;
+    int32_t vec;           // bytes per vector: 16, 8, 4, 2 or 1
+    int32_t batch_tokens;  // tokens per item
 };
 
 struct WriteParams {
@@ -43,98 +52,88 @@ struct WriteParams {
     int64_t num_tokens;
     int64_t block_size;
     int64_t num_slots;  // num_blocks * block_size
+    int64_t num_items;
     ErrorRecord *err;
 };
 
+// One item: tokens t0 .. t0+n-1 of descriptor d (k: its index).  The batch's
+// source bytes are loaded as VT vectors (a row is a whole number of them, so
+// no vector straddles two rows), its slots are split into destination byte
+// offsets (-1: skipped) in dst_off, and each vector is stored at its row.
 template <typename VT>
-__device__ __forceinline__ void copy_row(uint8_t *dst_bytes, const uint8_t *src_bytes,
-                                         int64_t nvec, int lane) {
-    VT *dst = reinterpret_cast<VT *>(dst_bytes);
-    const VT *src = reinterpret_cast<const VT *>(src_bytes);
-    for (int64_t base = 0; base < nvec; base += 32 * kUnroll) {
-        VT r[kUnroll];
+__device__ __forceinline__ void write_item(const WriteParams &p, const Desc &d, int k, int64_t t0,
+                                           int n, int64_t *dst_off) {
+    constexpr int V = sizeof(VT);
+    const int64_t R = d.row_width;
+    const int64_t nvec = static_cast<int64_t>(n) * R / V;
+    const VT *src = reinterpret_cast<const VT *>(d.src + t0 * R);
+    for (int64_t base = 0; base < nvec; base += kBatchVecs) {
+        VT r[kVecsPerThread];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
+        for (int u = 0; u < kVecsPerThread; ++u) {
+            const int64_t i = base + u * kWriteThreads + threadIdx.x;
             if (i < nvec) r[u] = __ldg(src + i);
         }
+        if (base == 0) {
+            // the slot split, while the row loads are in flight
+            for (int j = threadIdx.x; j < n; j += kWriteThreads) {
+                const int64_t t = t0 + j;
+                const int64_t slot = __ldg(p.slot_mapping + t);
+                int64_t off = -1;  // padding (negative slot) or out of range: skipped
+                if (slot >= p.num_slots) {
+                    if (k == 0) record_error(p.err, PKV_DEVERR_SLOT, t);
+                } else if (slot >= 0) {
+                    const int64_t block = slot / p.block_size;
+                    off = block * d.block_stride + (slot - block * p.block_size) * R;
+                }
+                dst_off[j] = off;
+            }
+            __syncthreads();
+        }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int64_t i = base + u * 32 + lane;
-            if (i < nvec) dst[i] = r[u];
+        for (int u = 0; u < kVecsPerThread; ++u) {
+            const int64_t i = base + u * kWriteThreads + threadIdx.x;
+            if (i < nvec) {
+                const int64_t byte = i * V;
+                // n > 1 only when the batch holds at most kBatchVecs * 16 bytes
+                const int tok = n == 1 ? 0
+                                       : static_cast<int>(static_cast<uint32_t>(byte) /
+                                                          static_cast<uint32_t>(R));
+                const int64_t off = dst_off[tok];
+                if (off >= 0)
+                    *reinterpret_cast<VT *>(d.dst + off + (byte - tok * R)) = r[u];
+            }
         }
     }
 }
 
-__device__ __forceinline__ void copy_any(uint8_t *dst, const uint8_t *src, int64_t nvec, int vec,
-                                         int lane) {
-    switch (vec) {
-        case 16: copy_row<uint4>(dst, src, nvec, lane); break;
-        case 8: copy_row<uint2>(dst, src, nvec, lane); break;
-        case 4: copy_row<unsigned int>(dst, src, nvec, lane); break;
-        case 2: copy_row<unsigned short>(dst, src, nvec, lane); break;
-        default: copy_row<unsigned char>(dst, src, nvec, lane); break;
-    }
-}
-
-// VEC > 0: every descriptor moves VEC-byte vectors; VEC == 0: each its own.
-template <int VEC>
-struct VecType;
-template <> struct VecType<16> { using T = uint4; };
-template <> struct VecType<8> { using T = uint2; };
-template <> struct VecType<4> { using T = unsigned int; };
-template <> struct VecType<2> { using T = unsigned short; };
-template <> struct VecType<1> { using T = unsigned char; };
-
-template <int VEC>
-__device__ __forceinline__ void copy_desc(uint8_t *dst, const uint8_t *src, const Desc &d,
-                                          int lane) {
-    if constexpr (VEC == 0) {
-        copy_any(dst, src, d.row_width / d.vec, d.vec, lane);
-    } else {
-        copy_row<typename VecType<VEC>::T>(dst, src, d.row_width / VEC, lane);
-    }
-}
-
-template <int VEC>
-__global__ void __launch_bounds__(kWriteThreads, VEC == 0 ? 4 : 1)
+__global__ void __launch_bounds__(kWriteThreads)
     cache_write_kernel(const __grid_constant__ WriteParams p) {
     // a dependent launch (the decode kernel) may be scheduled now; it still
     // waits for this grid's completion before it reads the caches
     grid_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-         t < p.num_tokens; t += nwarps) {
-        const int64_t slot = __ldg(p.slot_mapping + t);
-        if (slot < 0) continue;  // padding
-        if (slot >= p.num_slots) {
-            if (lane == 0) record_error(p.err, PKV_DEVERR_SLOT, t);
-            continue;
-        }
-        const int64_t block = slot / p.block_size;
-        const int64_t pos = slot - block * p.block_size;
-        if (p.num_descs > 1) {
-            // warm L2 with every source row of this token first (one 128-byte
-            // line per lane and prefetch, no registers held), so the row copies
-            // below wait on L2 rather than on DRAM one descriptor after another
-            for (int k = 0; k < p.num_descs; ++k) {
-                const uint8_t *src = p.d[k].src + t * p.d[k].row_width;
-                for (int64_t off = lane * 128; off < p.d[k].row_width; off += 32 * 128)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(src + off));
-            }
-        }
-        for (int k = 0; k < p.num_descs; ++k) {
-            const Desc &d = p.d[k];
-            copy_desc<VEC>(d.dst + block * d.block_stride + pos * d.row_width,
-                           d.src + t * d.row_width, d, lane);
+    __shared__ int64_t dst_off[kBatchVecs];
+    for (int64_t item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+        int k = 0;
+        while (k + 1 < p.num_descs && p.d[k + 1].item0 <= item) ++k;
+        const Desc &d = p.d[k];
+        const int64_t t0 = (item - d.item0) * d.batch_tokens;
+        const int n = static_cast<int>(min(static_cast<int64_t>(d.batch_tokens),
+                                           p.num_tokens - t0));
+        __syncthreads();  // the previous item's stores have read dst_off
+        switch (d.vec) {
+            case 16: write_item<uint4>(p, d, k, t0, n, dst_off); break;
+            case 8: write_item<uint2>(p, d, k, t0, n, dst_off); break;
+            case 4: write_item<unsigned int>(p, d, k, t0, n, dst_off); break;
+            case 2: write_item<unsigned short>(p, d, k, t0, n, dst_off); break;
+            default: write_item<unsigned char>(p, d, k, t0, n, dst_off); break;
         }
     }
 }
 
 bool view_ok(const pkv_view &v) {
-    if (v.row_width <= 0 || v.block_stride <= 0 || v.offset < 0 || v.layer < 0 ||
-        v.layer_stride < 0)
+    if (v.row_width <= 0 || v.row_width > kMaxRowWidth || v.block_stride <= 0 ||
+        v.offset < 0 || v.layer < 0 || v.layer_stride < 0)
         return false;
     return !(v.layer > 0 && v.layer_stride > (INT64_MAX - v.offset) / v.layer);
 }
@@ -142,39 +141,41 @@ bool view_ok(const pkv_view &v) {
 // One descriptor; its vector is the widest size that every address and
 // stride of the descriptor is a multiple of.
 Desc make_desc(const void *src, void *cache, const pkv_view &v) {
-    Desc d;
+    Desc d{};
     d.src = static_cast<const uint8_t *>(src);
     d.dst = static_cast<uint8_t *>(cache) + v.offset +
             static_cast<int64_t>(v.layer) * v.layer_stride;
     d.block_stride = v.block_stride;
-    d.row_width = v.row_width;
+    d.row_width = static_cast<int32_t>(v.row_width);
     const uintptr_t bits = reinterpret_cast<uintptr_t>(d.src) |
                            reinterpret_cast<uintptr_t>(d.dst) |
                            static_cast<uintptr_t>(v.block_stride) |
                            static_cast<uintptr_t>(v.row_width);
     d.vec = (bits & 15) == 0 ? 16 : (bits & 7) == 0 ? 8 : (bits & 3) == 0 ? 4
           : (bits & 1) == 0 ? 2 : 1;
+    // tokens per item: as many whole rows as one item's vectors hold
+    d.batch_tokens = static_cast<int32_t>(
+        std::max<int64_t>(1, static_cast<int64_t>(kBatchVecs) * d.vec / v.row_width));
     return d;
 }
 
 int launch_write(WriteParams &p, cudaStream_t stream) {
-    const int64_t warps_per_cta = kWriteThreads / 32;
-    const int64_t want = (p.num_tokens + warps_per_cta - 1) / warps_per_cta;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min(want, cap)));
+    int64_t items = 0;
+    for (int k = 0; k < p.num_descs; ++k) {
+        p.d[k].item0 = items;
+        items += (p.num_tokens + p.d[k].batch_tokens - 1) / p.d[k].batch_tokens;
+    }
+    p.num_items = items;
+    // one wave of resident CTAs, each taking items in turn
+    int per_sm = 0;
+    const int st = prepare_kernel(reinterpret_cast<const void *>(cache_write_kernel),
+                                  kWriteThreads, 0, &per_sm);
+    if (st != PKV_OK) return st;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * std::max(1, per_sm);
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min(items, cap)));
     p.err = device_error_record();
     if (p.err == nullptr) return PKV_ERR_CUDA;
-    int common = p.d[0].vec;
-    for (int k = 1; k < p.num_descs; ++k)
-        if (p.d[k].vec != common) common = 0;
-    switch (common) {
-        case 16: cache_write_kernel<16><<<grid, kWriteThreads, 0, stream>>>(p); break;
-        case 8: cache_write_kernel<8><<<grid, kWriteThreads, 0, stream>>>(p); break;
-        case 4: cache_write_kernel<4><<<grid, kWriteThreads, 0, stream>>>(p); break;
-        case 2: cache_write_kernel<2><<<grid, kWriteThreads, 0, stream>>>(p); break;
-        case 1: cache_write_kernel<1><<<grid, kWriteThreads, 0, stream>>>(p); break;
-        default: cache_write_kernel<0><<<grid, kWriteThreads, 0, stream>>>(p); break;
-    }
+    cache_write_kernel<<<grid, kWriteThreads, 0, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_failure(e, "cache_write_kernel launch");
 }

@@ -77,11 +77,13 @@ def test_dsa_two_cache_write_bit_exact(pkv, dsa, layout):
     (24, 8, 64 * 24 + 8),      # 8-byte rows
     (6, 2, 64 * 6 + 2),        # 2-byte rows
     (7, 3, 64 * 7 + 1),        # byte rows, odd offset
-    (4096, 0, 64 * 4096),      # wide rows (several vector rounds per lane)
+    (4096, 0, 64 * 4096),      # wide rows (4 rows per 16 KB batch)
+    (20000, 0, 64 * 20000),    # a row wider than one batch: one token, two rounds
+    (50000, 8, 64 * 50000 + 8),  # 8-byte vectors, seven rounds of one row
 ])
 def test_write_alignment_paths(pkv, row_width, offset, block_stride):
     rng = np.random.default_rng(row_width)
-    bs, nb, T, layers = 64, 12, 300, 2
+    bs, nb, T, layers = 64, 12, 300 if row_width < 10000 else 40, 2
     layer_stride = nb * block_stride + 16
     total = offset + layers * layer_stride + nb * block_stride
     init = rng.integers(0, 256, size=total, dtype=np.uint8)
@@ -138,3 +140,35 @@ def test_write_out_of_range_slot_recorded_and_skipped(pkv):
     got[1:3] = 0
     assert got.sum() == 0
     assert pkv.pkv_get_device_error() == (0, -1)  # reading clears it
+
+
+@pytest.mark.parametrize("row_width,T,vec_note", [
+    (24, 430001, "8-byte vectors, a tail past the last 16-byte multiple"),
+    (18, 580001, "2-byte vectors, odd tail"),
+    (656, 16385, "16-byte vectors, one token past a full item"),
+])
+def test_large_write_many_items_per_cta(pkv, row_width, T, vec_note):
+    """Writes of ~10 MB of rows: several batches per CTA, odd row widths and
+    token counts; bytes exact, padding and a bad slot skipped, the bad slot
+    recorded once."""
+    rng = np.random.default_rng(T)
+    bs = 64
+    nb = T // bs + 50
+    offset, block_stride = 16, bs * row_width + (8 if row_width % 8 == 0 else 2)
+    total = offset + nb * block_stride
+    init = rng.integers(0, 256, size=total, dtype=np.uint8)
+    slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int64)
+    slots[::1001] = -1
+    slots[7] = nb * bs + 3  # out of range: skipped and recorded
+    rows = rng.integers(0, 256, size=(T, row_width), dtype=np.uint8)
+    cache = torch.from_numpy(init.copy()).cuda()
+    view = pkv.pkv_view(offset, 0, block_stride, row_width, 0)
+    pkv.pkv_cache_write(torch.from_numpy(rows).cuda(), None, torch.from_numpy(slots).cuda(),
+                        cache, None, view, bs, nb)
+    assert pkv.pkv_get_device_error() == (1, 7)
+    ok = slots < nb * bs
+    ref = init.copy()
+    oracle.cache_write(ref, rows[ok], slots[ok], offset=offset, layer=0, layer_stride=0,
+                       block_stride=block_stride, row_width=row_width, block_size=bs,
+                       num_blocks=nb)
+    assert np.array_equal(cache.cpu().numpy(), ref), vec_note
