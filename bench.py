@@ -110,6 +110,8 @@ def parse(argv=None):
     ap.add_argument("--kv", choices=["fp16", "fp8"], default="fp16",
                     help="KV cache format (fp8: E4M3 codes + per-row fp32 scales)")
     ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--kv-heads", type=int, default=8,
+                    help="config 2 only: KV heads of the layer (query heads = 4x), same lengths")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--timed-s", type=float, default=HEADLINE_TIMED_S,
@@ -1009,7 +1011,8 @@ def main():
     rank, world, local = dist_env()
     from paged_kv_cache_131_gb300 import workloads as W
 
-    wl = W.config(args.config)
+    wl = (W.config2_llama8b(num_kv_heads=args.kv_heads) if args.config == 2 and
+          args.kv_heads != 8 else W.config(args.config))
     if args.impl == "reference":
         run_reference(args, wl, rank)
         return
@@ -1052,7 +1055,7 @@ def main():
     extras = None
     keys = [] if args.extras in ("", "none") else args.extras.split(",")
     if (rank == 0 and world == 1 and keys and args.config == 2 and args.kv == "fp16"
-            and compute == 0 and schedule == 0 and args.partition == 0):
+            and compute == 0 and schedule == 0 and args.partition == 0 and args.kv_heads == 8):
         del dev
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -1091,7 +1094,11 @@ def main():
         "vs_baseline": None,
         "dtype": "f16xf16->f32" if args.kv == "fp16" else "e4m3 KV (dequantized to f16) -> f32",
         "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
-        "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": S * world,
+        "config": {"workload": WORKLOAD_NAMES[args.config] if args.kv_heads == 8 or
+                   args.config != 2 else
+                   WORKLOAD_NAMES[2].replace("H=32, Hk=8", f"H={wl.num_heads}, Hk={wl.num_kv_heads}")
+                   .replace("[16384,16,8,128]", f"[16384,16,{wl.num_kv_heads},128]"),
+                   "global_batch": S * world,
                    "seq_len": int(wl.max_seq_len), "parallelism": f"replicas x{world}",
                    "l2": L2_NOTE + "; KV read per step > L2",
                    "kv_cache": "resident in HBM (state), not copied per step",

@@ -1171,20 +1171,11 @@ extern "C" int pkv_chunk_attention(void *out, const void *q, const void *k_cache
         b.num_heads = num_heads;
         b.num_kv_heads = num_kv_heads;
         b.max_blocks_per_seq = max_blocks_per_seq;
-        b.num_stages = z.bal.stages;
-        b.row_bytes = z.bal.row_bytes;
         b.num_blocks = num_blocks;
         b.query_start = query_start;
         b.max_cols = 8 * z.col_tiles;
         b.num_query_tokens = num_query_tokens;
-        const int64_t c_bytes = dec::align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
-        const int64_t slots = 2 * static_cast<int64_t>(z.bal.grid) * num_kv_heads * b.max_cols;
-        b.counters = reinterpret_cast<int *>(ws);
-        b.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
-        b.part_o = reinterpret_cast<float *>(ws + c_bytes + dec::align256(slots * 8));
-        const int box = row_bytes / dec::chunk_bytes_for_row(row_bytes);
-        int st = dec::make_kv_tensor_map(&b.tm_k, k_cache, num_blocks, row_bytes, box);
-        if (st == PKV_OK) st = dec::make_kv_tensor_map(&b.tm_v, v_cache, num_blocks, row_bytes, box);
+        const int st = dec::setup_balanced(b, z.bal, b.max_cols, ws, k_cache, v_cache);
         if (st != PKV_OK) return st;
         b.err = device_error_record();
         if (b.err == nullptr) return PKV_ERR_CUDA;

@@ -151,19 +151,8 @@ int pkv_decode_attention_ex(void *out, const void *q, const void *k_cache, const
             p.num_heads = num_heads;
             p.num_kv_heads = num_kv_heads;
             p.max_blocks_per_seq = max_blocks_per_seq;
-            p.num_stages = shape.stages;
-            p.row_bytes = shape.row_bytes;
             p.num_blocks = num_blocks;
-            uint8_t *ws = static_cast<uint8_t *>(workspace);
-            const int64_t c_bytes = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
-            const int64_t slots = 2 * static_cast<int64_t>(shape.grid) * num_kv_heads * G;
-            p.counters = reinterpret_cast<int *>(ws);
-            p.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
-            p.part_o = reinterpret_cast<float *>(ws + c_bytes + align256(slots * 8));
-            const int box = shape.row_bytes / chunk_bytes_for_row(shape.row_bytes);
-            int st = make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, shape.row_bytes, box);
-            if (st == PKV_OK)
-                st = make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, shape.row_bytes, box);
+            const int st = setup_balanced(p, shape, G, workspace, k_cache, v_cache);
             if (st != PKV_OK) return st;
             p.err = device_error_record();
             if (p.err == nullptr) return PKV_ERR_CUDA;
@@ -277,18 +266,8 @@ extern "C" int pkv_decode_attention_fp8(void *out, const void *q, const void *k_
     p.num_heads = num_heads;
     p.num_kv_heads = num_kv_heads;
     p.max_blocks_per_seq = max_blocks_per_seq;
-    p.num_stages = shape.stages;
-    p.row_bytes = shape.row_bytes;
     p.num_blocks = num_blocks;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const int64_t c_bytes = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4);
-    const int64_t slots = 2 * static_cast<int64_t>(shape.grid) * num_kv_heads * G;
-    p.counters = reinterpret_cast<int *>(ws);
-    p.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
-    p.part_o = reinterpret_cast<float *>(ws + c_bytes + align256(slots * 8));
-    const int box = shape.row_bytes / chunk_bytes_for_row(shape.row_bytes);
-    int st = make_kv_tensor_map(&p.tm_k, k_cache, num_blocks, shape.row_bytes, box);
-    if (st == PKV_OK) st = make_kv_tensor_map(&p.tm_v, v_cache, num_blocks, shape.row_bytes, box);
+    const int st = setup_balanced(p, shape, G, workspace, k_cache, v_cache);
     if (st != PKV_OK) return st;
     p.err = device_error_record();
     if (p.err == nullptr) return PKV_ERR_CUDA;

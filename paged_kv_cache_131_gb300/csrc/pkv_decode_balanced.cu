@@ -1,24 +1,29 @@
 // pkv_decode_balanced.cu -- paged decode attention, balanced schedule.
 //
-// The work is the flattened list of (sequence, logical block) pairs: T =
-// sum_i ceil(L_i / 16) blocks, each carrying all KV heads of 16 tokens.  The
-// launch is one wave of persistent CTAs; CTA c owns the contiguous range
-// [c*T/N, (c+1)*T/N) of that list, so every CTA reads the same number of
-// bytes whatever the length mix, and no CTA is empty.
+// The KV heads are taken in groups of up to 8 (heads_per_cta, a divisor of
+// num_kv_heads).  The work is the flattened list of (head group, sequence,
+// logical block) triples, groups outermost: T = groups * sum_i ceil(L_i / 16)
+// blocks, each carrying one head group of 16 tokens.  The launch is one wave
+// of persistent CTAs; CTA c owns the contiguous range [c*T/N, (c+1)*T/N) of
+// that list, so every CTA reads the same number of bytes whatever the length
+// mix, and no CTA is empty.  A (head group, sequence) pair is a "virtual
+// sequence": a contiguous interval of the list, numbered group * S + seq.
 //
-// A CTA has one producer warp and one consumer warp per KV head.
+// A CTA has one producer warp and one consumer warp per KV head of a group.
 //  - The producer walks its range.  For each block it takes the next stage
 //    of a `num_stages`-deep ring (waiting on the stage's "empty" mbarrier),
-//    publishes the block's (sequence, valid tokens, block id), and issues
-//    one tiled tensor copy (TMA) for the block's 16 key rows and one for its
-//    16 value rows (a row = all KV heads of one token, num_kv_heads*
-//    head_dim*elem contiguous bytes; FP8 adds two bulk copies of the rows'
-//    scales), completing on the stage's "full" mbarrier.  One copy per tile
+//    publishes the block's (virtual sequence, valid tokens, block id), and
+//    issues one tiled tensor copy (TMA) for the block's 16 key rows and one
+//    for its 16 value rows (a staged row = the group's KV heads of one token,
+//    heads_per_cta*head_dim*elem contiguous bytes; FP8 adds two bulk copies
+//    of the block's scales, all heads), completing on the stage's "full"
+//    mbarrier.  One copy per tile
 //    keeps the producer's issue cost per block small: issuing a copy takes
 //    the warp about as long whatever its size, and per-row copies made the
 //    producer the bottleneck.  Block-table entries are loaded a 32-block
 //    window ahead.
-//  - Consumer warp h waits on "full", folds head h's 16 keys/values into its
+//  - Consumer warp h waits on "full", folds head h of the group (KV head
+//    group*heads_per_cta + h) 16 keys/values into its
 //    online-softmax state (compute policy of pkv_decode_common.cuh) and
 //    arrives on "empty".  When the sequence changes it finishes the previous
 //    one: a sequence wholly inside the range is normalised and written as
@@ -29,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 
 #include "../../include/pagedkv.h"
@@ -54,7 +60,7 @@ constexpr int kMaxThreads = (kMaxBalancedKvHeads + 1) * 32;
 //   cum    S + 1 int32: exclusive prefix sum of the sequences' block counts
 //   lens   S int32: sequence lengths (clamped to the block table)
 //   misc   4 int32
-//   pbuf   Hk * 16 * G fp32 (SIMT policy: one block's softmax weights)
+//   pbuf   heads_per_cta * 16 * G fp32 (SIMT policy: one block's softmax weights)
 // (plus kTileAlign bytes to align the dynamic shared memory base)
 int smem_bytes(int stages, int stage_bytes, int S, int Hk, int G) {
     return kTileAlign + stages * stage_bytes + stages * 16 + stages * 16 + (2 * S + 1) * 4 + 16 +
@@ -92,21 +98,23 @@ __device__ __forceinline__ int cta_of(int64_t f, int64_t T, int64_t N) {
 // R partial rows per (sequence, kv head); row r is query row
 // (row0 + r / Gq) * H + kvh * Gq + r % Gq, rows >= ncols unused.  Rows are
 // merged eight at a time (bounded registers).
+// kvh is the KV head, hl its index within its head group (the partial rows
+// are laid out per group member).
 template <int D, int R>
-__device__ void combine_partials(const BalancedParams &p, int kvh, int c_a, int c_b,
+__device__ void combine_partials(const BalancedParams &p, int kvh, int hl, int c_a, int c_b,
                                  int64_t f_s, int64_t T, int64_t N, int lane, int64_t row0,
                                  int ncols, int Gq) {
     constexpr int G = R < 8 ? R : 8;  // rows per pass
     constexpr int DPL = D / 32;
     constexpr int U = (32 / (G * DPL)) < 1 ? 1 : ((32 / (G * DPL)) > 4 ? 4 : 32 / (G * DPL));
-    const int Hk = p.num_kv_heads;
+    const int Hc = p.heads_per_cta;
     const int nc = c_b - c_a + 1;
     // first partial row of contributor c_a + j
     auto row_of = [&](int j) -> int64_t {
         const int c = c_a + j;
         const int64_t fc = static_cast<int64_t>(c) * T / N;
         const int64_t slot = 2 * static_cast<int64_t>(c) + ((j == 0 && fc < f_s) ? 1 : 0);
-        return (slot * Hk + kvh) * R;
+        return (slot * Hc + hl) * R;
     };
     for (int r0 = 0; r0 < R && r0 < ncols; r0 += G) {
         // pass 1: the running maximum of every row over all contributors
@@ -204,9 +212,12 @@ template <int D, int G, class Policy, bool kFp8>
 __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *smem_raw) {
     uint8_t *smem = smem_raw + ((kTileAlign - (smem_u32(smem_raw) & (kTileAlign - 1))) &
                                 (kTileAlign - 1));
-    const int Hk = p.num_kv_heads, S = p.num_seqs, NS = p.num_stages, H = p.num_heads;
+    const int Hk = p.num_kv_heads, Hc = p.heads_per_cta, S = p.num_seqs, NS = p.num_stages;
+    const int H = p.num_heads;
     const SwizzledTile tile{chunk_bytes_for_row(p.row_bytes) == 128 ? 7u : 6u};
     const int tile_bytes = kBS * p.row_bytes;
+    // tensor-copy boxes: the group's chunks of a row; group g starts at chunk g * box
+    const int box_chunks = p.row_bytes / chunk_bytes_for_row(p.row_bytes);
     // FP8: a stage also holds the block's key and value scales ([16][Hk] fp32 each)
     const int scale_bytes = kFp8 ? kBS * Hk * 4 : 0;
     const int stage_bytes = stage_bytes_for(p.row_bytes, Hk, kFp8);
@@ -235,7 +246,7 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), Hk);
+            mbar_init(smem_u32(&empty[s]), Hc);
         }
         fence_mbarrier_init();
     }
@@ -303,14 +314,15 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
     __syncthreads();
 
     // ---- empty sequences get zeros (no block of theirs is in any range)
-    const int64_t T = cum[S];
+    const int64_t Tb = cum[S];                 // blocks of one head group
+    const int64_t T = Tb * p.groups;           // the whole (group, sequence, block) list
     const int64_t N = min(static_cast<int64_t>(grid), T);
     bool zeros_due = false;
     for (int s = blockIdx.x; s < S && !zeros_due; s += grid) zeros_due = lens[s] == 0;
-    if (zeros_due && (blockIdx.x >= N || warp < Hk)) {
+    if (zeros_due && (blockIdx.x >= N || warp < Hc)) {
         // the consumers (or every warp of a CTA without a range) write them
         if (!p.defer_wait) grid_dependency_wait();
-        const int nz = blockIdx.x >= N ? nthreads : Hk * 32;
+        const int nz = blockIdx.x >= N ? nthreads : Hc * 32;
         for (int s = blockIdx.x; s < S; s += grid) {
             if (lens[s] == 0) {
                 uint4 *o = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(s) * H * D);
@@ -326,40 +338,53 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
     const uint32_t ring_s = smem_u32(ring);
     const uint32_t full_s = smem_u32(full), empty_s = smem_u32(empty);
 
-    if (warp == Hk) {
+    // (head group, sequence, block in the sequence) of flattened block f
+    const bool grouped = p.groups > 1;
+    auto locate = [&](int64_t f, int &hg, int &seq, int &blk) {
+        hg = grouped ? static_cast<int>(f / Tb) : 0;
+        const int64_t fl = f - static_cast<int64_t>(hg) * Tb;
+        seq = find_seq(cum, S, fl);
+        blk = static_cast<int>(fl - cum[seq]);
+    };
+
+    if (warp == Hc) {
         // ================================ producer ================================
-        // window of 32 blocks: lane j describes block base + j
-        auto fetch = [&](int base, int &raw, int &seq, int &nv) {
+        // window of 32 blocks: lane j describes block base + j (vseq: its
+        // virtual sequence group * S + seq; blk: its index in the sequence;
+        // z: the first chunk of its group's box)
+        auto fetch = [&](int base, int &raw, int &vseq, int &nv, int &blk, int &z) {
             const int i = base + lane;
             raw = -1;
-            seq = -1;
+            vseq = -1;
             nv = 0;
+            blk = 0;
+            z = 0;
             if (i < n) {
-                const int64_t f = f0 + i;
-                seq = find_seq(cum, S, f);
-                const int blk = static_cast<int>(f - cum[seq]);
-                // (the block's index in its sequence is f - cum[seq])
+                int hg, seq;
+                locate(f0 + i, hg, seq, blk);
+                vseq = hg * S + seq;
+                z = hg * box_chunks;
                 nv = min(kBS, lens[seq] - blk * kBS);
                 // checked when its window becomes current, so the load's latency
                 // hides behind the 32 blocks before it
                 raw = __ldg(p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk);
             }
         };
-        auto check = [&](int base, int raw, int seq) -> int {
+        auto check = [&](int base, int raw, int vseq, int blk) -> int {
             const int i = base + lane;
             if (i >= n) return -1;
             if (raw < 0 || static_cast<int64_t>(raw) >= p.num_blocks) {
-                const int blk = static_cast<int>(f0 + i - cum[seq]);
+                const int seq = vseq % S;
                 record_error(p.err, PKV_DEVERR_BLOCK_ID,
                              static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk);
                 return -1;
             }
             return raw;
         };
-        int c_raw, c_seq, c_nv, n_raw, n_seq, n_nv;
-        fetch(0, c_raw, c_seq, c_nv);
-        int c_bid = check(0, c_raw, c_seq);
-        fetch(32, n_raw, n_seq, n_nv);
+        int c_raw, c_seq, c_nv, c_blk, c_z, n_raw, n_seq, n_nv, n_blk, n_z;
+        fetch(0, c_raw, c_seq, c_nv, c_blk, c_z);
+        int c_bid = check(0, c_raw, c_seq, c_blk);
+        fetch(32, n_raw, n_seq, n_nv, n_blk, n_z);
         if (!p.defer_wait) grid_dependency_wait();  // the caches may have just been written
         int issued = 0;
         bool ok = true;
@@ -373,21 +398,25 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
                 }
             }
             if (i > 0 && (i & 31) == 0) {
-                c_bid = check(i, n_raw, n_seq);
+                c_bid = check(i, n_raw, n_seq, n_blk);
                 c_seq = n_seq;
                 c_nv = n_nv;
-                fetch(i + 32, n_raw, n_seq, n_nv);
+                c_blk = n_blk;
+                c_z = n_z;
+                fetch(i + 32, n_raw, n_seq, n_nv, n_blk, n_z);
             }
             const int bid = __shfl_sync(0xffffffffu, c_bid, i & 31);
-            const int seq = __shfl_sync(0xffffffffu, c_seq, i & 31);
+            const int vseq = __shfl_sync(0xffffffffu, c_seq, i & 31);
             const int nv = __shfl_sync(0xffffffffu, c_nv, i & 31);
+            const int blk = __shfl_sync(0xffffffffu, c_blk, i & 31);
+            const int z = grouped ? __shfl_sync(0xffffffffu, c_z, i & 31) : 0;
             // the whole 16-row tiles (rows past the last valid token still
             // belong to the physical block)
             const bool copy = bid >= 0 && nv > 0;
             const uint32_t stage = ring_s + st * stage_bytes;
             if (lane == 0) {
                 // .w: the block's index in its sequence
-                meta[st] = make_int4(seq, nv, bid, static_cast<int>(f0 + i - cum[max(seq, 0)]));
+                meta[st] = make_int4(vseq, nv, bid, blk);
                 mbar_arrive_expect_tx(full_s + st * 8,
                                       copy ? 2u * tile_bytes + (kFp8 ? 2u * scale_bytes : 0u)
                                            : 0u);
@@ -395,7 +424,7 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
             __syncwarp();
             if (copy && lane < 2)
                 tensor_g2s_3d(stage + lane * tile_bytes, lane == 0 ? &p.tm_k : &p.tm_v, 0,
-                              bid * kBS, 0, full_s + st * 8);
+                              bid * kBS, z, full_s + st * 8);
             if (kFp8 && copy && (lane == 2 || lane == 3)) {
                 // the block's scales: 16 tokens x Hk heads, contiguous
                 const float *src = (lane == 2 ? p.k_scale : p.v_scale) +
@@ -413,21 +442,26 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
         }
         return;
     }
-    if (warp > Hk) return;
+    if (warp > Hc) return;
 
     // ================================ consumers ================================
-    const int kvh = warp;
+    const int hl = warp;  // head within the group: its bytes in the staged rows
+    int kvh = warp;       // KV head of the current virtual sequence
     Policy st;
-    float *pbuf = pbuf_all + kvh * kBS * G;
+    float *pbuf = pbuf_all + hl * kBS * G;
     int cur = -1;
     {
-        // warm L2 with the query rows of the (up to 8) sequences this range
-        // touches, so a sequence switch does not stall on a cold load
-        const int s_first = find_seq(cum, S, f0), s_last = find_seq(cum, S, f1 - 1);
+        // warm L2 with the query rows of the (up to 8) virtual sequences this
+        // range touches, so a sequence switch does not stall on a cold load
+        int hg0, s0, b0, hg1, s1, b1;
+        locate(f0, hg0, s0, b0);
+        locate(f1 - 1, hg1, s1, b1);
+        const int v_first = hg0 * S + s0, v_last = hg1 * S + s1;
         const int bytes = G * D * 2;
-        for (int s = s_first; s <= s_last && s < s_first + 8; ++s) {
+        for (int v = v_first; v <= v_last && v < v_first + 8; ++v) {
+            const int s = v % S, h = (v / S) * Hc + hl;
             const char *row = reinterpret_cast<const char *>(
-                p.q + (static_cast<int64_t>(s) * H + kvh * G) * D);
+                p.q + (static_cast<int64_t>(s) * H + h * G) * D);
             for (int off = lane * 128; off < bytes; off += 32 * 128)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
         }
@@ -435,8 +469,10 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
     if (!p.defer_wait) grid_dependency_wait();  // outputs and partials are written below
 
     QueryRows qr{p.q, p.out, 0, H, kvh, G, 0};  // the current sequence's query rows
-    auto finish = [&](int seq) {
-        const int64_t f_s = cum[seq], f_e = cum[seq + 1];
+    auto finish = [&](int vseq) {
+        const int hg = grouped ? vseq / S : 0, seq = vseq - hg * S;
+        const int64_t fg = static_cast<int64_t>(hg) * Tb;
+        const int64_t f_s = fg + cum[seq], f_e = fg + cum[seq + 1];
         const int64_t qrow = static_cast<int64_t>(seq) * H + kvh * G;
         if (f_s >= f0 && f_e <= f1) {
             if constexpr (Policy::kColumns) st.write_output(qr, lane);
@@ -444,7 +480,7 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
             return;
         }
         const int64_t slot = 2 * static_cast<int64_t>(blockIdx.x) + (f_s <= f0 ? 0 : 1);
-        const int64_t base = (slot * Hk + kvh) * Policy::kRows;
+        const int64_t base = (slot * Hc + hl) * Policy::kRows;
         if constexpr (Policy::kColumns)
             st.write_partial(p.part_ml + base, p.part_o + base * D, qr.ncols, lane);
         else
@@ -466,10 +502,10 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             if constexpr (Policy::kColumns)
-                combine_partials<D, Policy::kRows>(p, kvh, c_a, c_b, f_s, T, N, lane, qr.row0,
-                                                   qr.ncols, G);
+                combine_partials<D, Policy::kRows>(p, kvh, hl, c_a, c_b, f_s, T, N, lane,
+                                                   qr.row0, qr.ncols, G);
             else
-                combine_partials<D, G>(p, kvh, c_a, c_b, f_s, T, N, lane, seq, G, G);
+                combine_partials<D, G>(p, kvh, hl, c_a, c_b, f_s, T, N, lane, seq, G, G);
         }
     };
 
@@ -498,14 +534,17 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
         if (mt.x != cur) {
             if (cur >= 0) finish(cur);
             cur = mt.x;
+            const int hg = grouped ? cur / S : 0, seq = cur - hg * S;
+            kvh = hg * Hc + hl;
             if constexpr (Policy::kColumns) {
-                const int qs0 = __ldg(p.query_start + cur), qs1 = __ldg(p.query_start + cur + 1);
+                const int qs0 = __ldg(p.query_start + seq), qs1 = __ldg(p.query_start + seq + 1);
                 qr.row0 = qs0;
+                qr.kvh = kvh;
                 qr.ncols = (qs1 - qs0) * G;
-                qr.lim0 = lens[cur] - (qs1 - qs0);
+                qr.lim0 = lens[seq] - (qs1 - qs0);
                 st.init(qr, lane);
             } else {
-                st.init(p.q + (static_cast<int64_t>(cur) * H + kvh * G) * D, p.scale_log2, lane);
+                st.init(p.q + (static_cast<int64_t>(seq) * H + kvh * G) * D, p.scale_log2, lane);
             }
         }
         int used = 1;
@@ -526,7 +565,7 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
                 mt2 = meta[s2];
             }
             const uint32_t kb8 = ring_s + s * stage_bytes;
-            const uint32_t head = kvh * D;
+            const uint32_t head = hl * D;
             if (mt2.x == mt.x && mt2.z >= 0 && mt2.y > 0) {
                 const uint32_t kb8b = ring_s + s2 * stage_bytes;
                 if (mt2.y < kBS) zero_tail_bytes<D>(kb8b + tile_bytes, tile, head, mt2.y, lane);
@@ -551,7 +590,7 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
             if (mt.z >= 0 && mt.y > 0) {
                 const uint32_t kb = ring_s + s * stage_bytes;
                 const uint32_t vb = kb + tile_bytes;
-                const uint32_t head = kvh * D * 2;
+                const uint32_t head = hl * D * 2;
                 if (Policy::kZeroTailRows && mt.y < kBS)
                     zero_tail_rows<D>(vb, tile, head, mt.y, lane);
                 if constexpr (Policy::kColumns)
@@ -614,36 +653,69 @@ BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int n
                              bool fp8, int rows) {
     if (rows <= 0) rows = G;
     BalancedShape r{};
-    r.ok = num_kv_heads >= 1 && num_kv_heads <= kMaxBalancedKvHeads && num_seqs >= 1 &&
-           (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
+    r.ok = num_kv_heads >= 1 && num_seqs >= 1 && (D == 64 || D == 128) &&
+           (G == 1 || G == 2 || G == 4 || G == 8);
     if (!r.ok) return r;
-    const int row_bytes = num_kv_heads * D * (fp8 ? 1 : 2);
+    // heads per CTA: the largest divisor of num_kv_heads up to 8 whose staged
+    // row has the swizzle chunk of the whole row (the tensor maps span whole
+    // rows; a group's box starts at a chunk boundary)
+    const int elem = fp8 ? 1 : 2;
+    const int chunk = chunk_bytes_for_row(num_kv_heads * D * elem);
+    int hc = 0;
+    for (int h = std::min(num_kv_heads, kMaxBalancedKvHeads); h >= 1 && hc == 0; --h)
+        if (num_kv_heads % h == 0 && chunk_bytes_for_row(h * D * elem) == chunk) hc = h;
+    // (virtual sequence numbers group * S + seq stay 32-bit)
+    if (hc == 0 || static_cast<int64_t>(num_seqs) * (num_kv_heads / hc) > INT32_MAX) {
+        r.ok = false;
+        return r;
+    }
+    const int row_bytes = hc * D * elem;
     const int stage_bytes = stage_bytes_for(row_bytes, num_kv_heads, fp8);
     int stages = fp8 ? kMaxStagesFp8 : kMaxStages;
-    while (stages >= 2 &&
-           smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G) > kSmemPerSM)
-        --stages;
+    while (stages >= 2 && smem_bytes(stages, stage_bytes, num_seqs, hc, G) > kSmemPerSM) --stages;
     if (stages < 2) {
         r.ok = false;
         return r;
     }
     r.stages = stages;
+    r.heads = hc;
+    r.groups = num_kv_heads / hc;
     r.row_bytes = row_bytes;
-    r.smem = smem_bytes(stages, stage_bytes, num_seqs, num_kv_heads, G);
-    const int threads = (num_kv_heads + 1) * 32;
+    r.smem = smem_bytes(stages, stage_bytes, num_seqs, hc, G);
+    const int threads = (hc + 1) * 32;
     r.ctas_per_sm = std::max(1, std::min({(228 * 1024) / (r.smem + 1024), 2048 / threads, 32}));
     r.grid = std::max(1, num_sms) * r.ctas_per_sm;
-    const int64_t slots = 2 * static_cast<int64_t>(r.grid) * num_kv_heads * rows;
+    const int64_t slots = 2 * static_cast<int64_t>(r.grid) * hc * rows;
     r.workspace = align256(static_cast<int64_t>(num_seqs) * num_kv_heads * 4) +
                   align256(slots * 8) + slots * D * 4;
     return r;
+}
+
+int setup_balanced(BalancedParams &p, const BalancedShape &shape, int rows, void *workspace,
+                   const void *k_cache, const void *v_cache) {
+    p.num_stages = shape.stages;
+    p.row_bytes = shape.row_bytes;
+    p.heads_per_cta = shape.heads;
+    p.groups = shape.groups;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t c_bytes = align256(static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * 4);
+    const int64_t slots = 2 * static_cast<int64_t>(shape.grid) * shape.heads * rows;
+    p.counters = reinterpret_cast<int *>(ws);
+    p.part_ml = reinterpret_cast<float2 *>(ws + c_bytes);
+    p.part_o = reinterpret_cast<float *>(ws + c_bytes + align256(slots * 8));
+    // maps over whole rows (all heads); a box covers one head group
+    const int full_row = shape.row_bytes * shape.groups;
+    const int box = shape.row_bytes / chunk_bytes_for_row(shape.row_bytes);
+    int st = make_kv_tensor_map(&p.tm_k, k_cache, p.num_blocks, full_row, box);
+    if (st == PKV_OK) st = make_kv_tensor_map(&p.tm_v, v_cache, p.num_blocks, full_row, box);
+    return st;
 }
 
 int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
                     bool fp8, cudaStream_t stream, int col_tiles) {
     BalancedFn fn = select(D, G, simt, fp8, col_tiles);
     if (fn == nullptr) return PKV_ERR_UNSUPPORTED;
-    const int threads = (p.num_kv_heads + 1) * 32;
+    const int threads = (p.heads_per_cta + 1) * 32;
     int per_sm = 0;
     const int st = prepare_kernel(reinterpret_cast<const void *>(fn), threads, shape.smem, &per_sm);
     if (st != PKV_OK) return st;

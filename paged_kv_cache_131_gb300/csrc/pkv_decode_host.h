@@ -18,7 +18,7 @@ constexpr int kGridWarps = 4;
 constexpr int kGridStages = 2;
 constexpr int kMaxPartitionTokens = 8192;
 constexpr int kDefaultPartitionTokens = 512;
-constexpr int kMaxBalancedKvHeads = 8;   // consumer warps per CTA (+1 producer)
+constexpr int kMaxBalancedKvHeads = 8;   // KV heads (consumer warps) per CTA (+1 producer)
 constexpr int kSmemPerSM = 227 * 1024;   // opt-in dynamic shared memory per CTA
 constexpr int kTileAlign = 1024;         // staged tiles start 1024-byte aligned (swizzle)
 
@@ -90,7 +90,11 @@ struct BalancedParams {
     int num_kv_heads;
     int max_blocks_per_seq;
     int num_stages;  // staging ring depth (blocks in flight per CTA)
-    int row_bytes;   // staged row: all KV heads of one token, Hk*D*elem bytes
+    int row_bytes;   // staged row: one head group of one token, heads_per_cta*D*elem bytes
+    // the KV heads are taken in groups of heads_per_cta (<= 8, one consumer
+    // warp each); the work list is (group, sequence, block), groups outermost
+    int heads_per_cta;
+    int groups;      // num_kv_heads / heads_per_cta
     const float *k_scale;  // FP8 caches: [NB, 16, Hk] per-row scales (else null)
     const float *v_scale;
     // several new tokens per sequence (MmaColsPolicy): sequence i's query
@@ -109,15 +113,17 @@ struct BalancedParams {
     const int *active_ctas;
     int64_t num_blocks;
     int *counters;    // [S * Hk] tickets, zero between calls
-    float2 *part_ml;  // [2 * grid][Hk][G]
-    float *part_o;    // [2 * grid][Hk][G][D]
+    float2 *part_ml;  // [2 * grid][heads_per_cta][rows]
+    float *part_o;    // [2 * grid][heads_per_cta][rows][D]
     ErrorRecord *err;
 };
 
 struct BalancedShape {
     bool ok;          // the schedule supports this shape
     int stages;       // ring depth
-    int row_bytes;    // staged row bytes
+    int heads;        // KV heads per CTA (a divisor of num_kv_heads, <= 8)
+    int groups;       // num_kv_heads / heads
+    int row_bytes;    // staged row bytes (one head group)
     int smem;         // dynamic shared memory per CTA
     int ctas_per_sm;  // resident CTAs per SM
     int grid;         // CTAs launched
@@ -128,6 +134,13 @@ struct BalancedShape {
 // rows per (sequence, kv head): G for decode, 8 * col_tiles for chunks.
 BalancedShape balanced_shape(int num_seqs, int num_kv_heads, int G, int D, int num_sms,
                              bool fp8, int rows = 0);
+// Sets the fields of p that follow from the shape -- ring depth, staged row,
+// head groups, the scratch layout inside `workspace` (counters, partial
+// states for `rows` rows per (sequence, kv head)) and the tensor maps of the
+// two caches (p.num_seqs, p.num_kv_heads and p.num_blocks must be set).
+// Returns a PKV status.
+int setup_balanced(BalancedParams &p, const BalancedShape &shape, int rows, void *workspace,
+                   const void *k_cache, const void *v_cache);
 // col_tiles: 0 for decode, else the column n-tiles (1 or 2) of MmaColsPolicy.
 int launch_balanced(const BalancedParams &p, const BalancedShape &shape, int D, int G, bool simt,
                     bool fp8, cudaStream_t stream, int col_tiles = 0);

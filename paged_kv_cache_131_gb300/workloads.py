@@ -292,14 +292,15 @@ def config1_tiny() -> DecodeWorkload:
                             order=order[::-1])
 
 
-def config2_llama8b(num_seqs: int = 64) -> DecodeWorkload:
+def config2_llama8b(num_seqs: int = 64, num_kv_heads: int = 8) -> DecodeWorkload:
     """Llama-3-8B-shaped decode layer: 64 sequences, lengths U[256, 4096], bs 16,
     H 32 / Hk 8, D 128, 16384 blocks from a seeded shuffled free list, one new
-    token per sequence written."""
+    token per sequence written.  ``num_kv_heads`` widens the layer with the
+    same group size (H = 4 * Hk) and the same lengths and block tables."""
     rng = rng_for(2)
     lens = rng.integers(256, 4096, size=num_seqs, endpoint=True)
-    return _decode_workload("llama8b", rng, lens, H=32, Hk=8, D=128, bs=16, NB=16384,
-                            order=rng.permutation(16384))
+    return _decode_workload("llama8b", rng, lens, H=4 * num_kv_heads, Hk=num_kv_heads, D=128,
+                            bs=16, NB=16384, order=rng.permutation(16384))
 
 
 def config3_long(num_seqs: int = 8, seq_len: int = 32768) -> DecodeWorkload:

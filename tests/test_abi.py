@@ -113,11 +113,12 @@ def test_decode_validation(lib):
     grid_bytes = a256(4 * 32 * 4) + a256(4 * 32 * 2 * 8) + 4 * 32 * 2 * 128 * 4
     assert need_grid >= grid_bytes
     assert _decode(lib, maxL=513, ws=FAKE, wsb=grid_bytes - 1, opts=grid) == -5
-    # balanced schedule: always needs its workspace; more than 8 KV heads unsupported
+    # balanced schedule: always needs its workspace; a sequence count whose
+    # per-sequence tables overflow its shared memory is unsupported
     bal = (0, 0, 2)
     assert _decode(lib, opts=bal) == -5
     assert _decode(lib, ws=FAKE, wsb=need_grid - 1, opts=bal) == -5 or need_grid == grid_bytes
-    assert _decode(lib, H=64, Hk=16, ws=FAKE, wsb=1 << 30, opts=bal) == -3
+    assert _decode(lib, S=28000, ws=FAKE, wsb=1 << 30, opts=bal) == -3
 
 
 def _chunk(lib, out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, qs=FAKE, scale=0.1, H=32,

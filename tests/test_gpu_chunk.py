@@ -64,7 +64,7 @@ SMALL = [
     (307, [2049, 513, 512], [1025, 2, 512], 8, 2, 128),               # partition edges
     (309, [2048, 4096, 4097], [200, 130, 300], 8, 2, 128),            # 4096-token edges
     (313, [9000, 300, 4500], [150, 20, 64], 8, 2, 64),               # three partitions
-    (312, [300, 40, 1, 600], [100, 40, 1, 3], 16, 16, 64),           # Hk 16: all on the tile kernel
+    (312, [300, 40, 1, 600], [100, 40, 1, 3], 16, 16, 64),           # Hk 16: 2 head groups
 ]
 
 

@@ -126,6 +126,24 @@ def test_balanced_many_short_sequences(pkv):
     assert pkv.pkv_get_device_error() == (0, -1)
 
 
+@pytest.mark.parametrize("index,lens,H,Hk,D", [
+    (221, [0, 1, 17, 600, 1500, 33, 2100], 32, 16, 128),  # 2 groups of 8 KV heads
+    (222, [5, 300, 999, 64], 128, 16, 64),                # G 8, 2 groups
+    (223, [1, 250, 1300, 16, 700], 12, 12, 128),          # 2 groups of 6
+    (224, [40, 700, 3], 40, 40, 64),                      # 5 groups of 8
+])
+@pytest.mark.parametrize("compute", [MMA, SIMT])
+def test_balanced_more_kv_heads_than_a_cta_holds(pkv, index, lens, H, Hk, D, compute):
+    """More than 8 KV heads: the balanced schedule takes them in groups (each
+    CTA range walks (group, sequence, block)), every element as the oracle."""
+    wl = W.small_decode(index, lens, H=H, Hk=Hk, D=D)
+    k, v = oracle_after_write(wl)
+    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale)
+    _, out = run(wl, compute=compute, schedule=BALANCED)
+    assert_close(out, ref, what=f"Hk {Hk}")
+    assert pkv.pkv_get_device_error() == (0, -1)
+
+
 def test_schedules_agree(pkv):
     wl = W.small_decode(218, [100, 900, 1600, 3], H=32, Hk=8, D=128)
     a = run(wl, schedule=BALANCED)[1].astype(np.float64)

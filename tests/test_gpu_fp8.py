@@ -97,6 +97,11 @@ def _close(out, ref, pairs=None):
     dict(index=502, lens=[5, 47, 999, 1500], H=32, Hk=8, D=128),
     dict(index=503, lens=[3, 64, 700], H=16, Hk=2, D=64),
     dict(index=504, lens=[9, 200, 520], H=8, Hk=1, D=64),
+    # more KV heads than a CTA holds: groups of 8, 8 and 2 (64-byte FP8 rows
+    # per head: a group must keep whole 128-byte chunks)
+    dict(index=505, lens=[1, 33, 1200, 600], H=32, Hk=16, D=128),
+    dict(index=506, lens=[700, 17, 2100], H=64, Hk=16, D=64),
+    dict(index=507, lens=[250, 999, 5], H=20, Hk=10, D=64),
 ])
 def test_fp8_decode_small(pkv, case):
     from paged_kv_cache_131_gb300.harness import DeviceDecodeFp8

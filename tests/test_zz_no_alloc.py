@@ -82,13 +82,19 @@ def _check_twice(lib, wl):
 @pytest.mark.parametrize("case", [
     dict(index=301, lens=[1, 17, 600, 1500, 2100, 33, 0, 900], H=32, Hk=8, D=128),
     dict(index=302, lens=[5, 700, 1300, 64], H=8, Hk=1, D=64),
-    # 16 KV heads with 8 query heads each: the balanced schedule's partials
-    # would not fit the built-in scratch, so the grid schedule runs (its own
-    # scratch layout: counters per query head, partials per partition)
-    dict(index=303, lens=[600, 1000, 70, 1500], H=128, Hk=16, D=128),
+    dict(index=303, lens=[600, 1000, 70, 1500], H=128, Hk=16, D=128),  # 2 head groups
 ])
 def test_noalloc_matches_workspace_entry_point_twice(lib, case):
     wl = W.small_decode(case["index"], case["lens"], H=case["H"], Hk=case["Hk"], D=case["D"])
+    _check_twice(lib, wl)
+
+
+def test_noalloc_grid_schedule_twice(lib):
+    # 28000 short sequences: the balanced schedule's per-sequence tables do
+    # not fit its shared memory, so the grid schedule runs (one partition per
+    # sequence; its own counter layout, per query head)
+    lens = [1 + (7 * i) % 40 for i in range(28000)]
+    wl = W.small_decode(306, lens, H=8, Hk=2, D=64)
     _check_twice(lib, wl)
 
 
@@ -129,10 +135,11 @@ def test_noalloc_refused_calls_return_before_any_work(lib):
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
-    # 64 sequences of up to 32768 tokens with 16 KV heads: too many KV heads for
-    # the balanced schedule and 64 partitions x 64 heads x 128 dims of fp32
-    # partials for the grid schedule -- far beyond the built-in scratch
-    S, H, Hk, D, L = 64, 64, 16, 128, 32768
+    # 28000 sequences of up to 8192 tokens: too many sequences for the
+    # balanced schedule's shared memory, and 16 partitions x 8 heads x 64 dims
+    # of fp32 partials per sequence for the grid schedule -- far beyond the
+    # built-in scratch
+    S, H, Hk, D, L = 28000, 8, 2, 64, 8192
     q = torch.zeros(S, H, D, dtype=torch.float16, device="cuda")
     cache = torch.zeros(4, 16, Hk, D, dtype=torch.float16, device="cuda")
     bt = torch.zeros(S, L // 16, dtype=torch.int32, device="cuda")
