@@ -37,6 +37,7 @@ def assert_close(gpu, ref, pairs=None, what=""):
         idx = tuple(np.array(pairs).T)
         g, ref = g[idx], ref[idx]
     assert not np.isnan(ref).any()
+    assert np.isfinite(g).all(), f"{what}: {int((~np.isfinite(g)).sum())} non-finite outputs"
     err = np.abs(g - ref)
     bound = ATOL + RTOL * np.abs(ref)
     bad = err > bound
@@ -141,6 +142,40 @@ def test_balanced_more_kv_heads_than_a_cta_holds(pkv, index, lens, H, Hk, D, com
     ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale)
     _, out = run(wl, compute=compute, schedule=BALANCED)
     assert_close(out, ref, what=f"Hk {Hk}")
+    assert pkv.pkv_get_device_error() == (0, -1)
+
+
+REPEAT = [
+    # (index, lens, H, Hk, D): ranges of many blocks per CTA
+    (231, [3000 + 37 * i for i in range(16)], 32, 8, 128),         # long sequences
+    (232, [200 + (i * 53) % 300 for i in range(256)], 32, 8, 128),  # many short ones
+    (233, [5000, 17, 2500, 1, 4000, 300] * 4, 64, 8, 128),          # mixed lengths, G 8
+    (234, [2000 + 11 * i for i in range(24)], 32, 16, 128),         # 2 head groups
+]
+
+
+@pytest.mark.parametrize("case", REPEAT, ids=lambda c: str(c[0]))
+def test_repeated_calls_every_element_same_bits(pkv, case):
+    """Calls in a row on one workspace: every call within tolerance of the
+    oracle on every element (outputs poisoned before each call, so a merge
+    that did not happen shows), the same bits every call (the split is fixed
+    by the lengths), the scratch left clean for the next call."""
+    from paged_kv_cache_131_gb300.harness import DeviceDecode
+    index, lens, H, Hk, D = case
+    wl = W.small_decode(index, lens, H=H, Hk=Hk, D=D)
+    k, v = oracle_after_write(wl)
+    ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale,
+                                  workers=oracle.default_workers())
+    dev = DeviceDecode(wl, schedule=BALANCED)
+    dev.write()
+    first = None
+    for _ in range(4):
+        dev.out.fill_(float("nan"))
+        out = dev.decode().clone()
+        assert_close(out.cpu().numpy(), ref, what=f"case {index}")
+        if first is None:
+            first = out
+        assert torch.equal(out, first)
     assert pkv.pkv_get_device_error() == (0, -1)
 
 

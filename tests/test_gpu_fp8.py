@@ -141,3 +141,19 @@ def test_fp8_full_size_all_elements(pkv, cfg):
     ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.seq_lens,
                                       wl.scale, workers=workers)
     _close(out, ref)
+
+
+def test_fp8_repeated_calls_every_element(pkv):
+    """FP8 decode, calls in a row on one workspace: every call within
+    tolerance of the oracle (outputs poisoned before each call)."""
+    from paged_kv_cache_131_gb300.harness import DeviceDecodeFp8
+    wl = W.small_decode(508, [3000 + 41 * i for i in range(16)], H=32, Hk=8, D=128)
+    dev = DeviceDecodeFp8(wl)
+    dev.write()
+    k8, v8, ks, vs = _oracle_fp8_state(wl, workers=oracle.default_workers())
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.seq_lens,
+                                      wl.scale, workers=oracle.default_workers())
+    for _ in range(5):
+        dev.out.fill_(float("nan"))
+        _close(dev.decode().cpu().numpy(), ref)
+    assert pkv.pkv_get_device_error() == (0, -1)

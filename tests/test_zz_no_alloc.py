@@ -83,6 +83,8 @@ def _check_twice(lib, wl):
     dict(index=301, lens=[1, 17, 600, 1500, 2100, 33, 0, 900], H=32, Hk=8, D=128),
     dict(index=302, lens=[5, 700, 1300, 64], H=8, Hk=1, D=64),
     dict(index=303, lens=[600, 1000, 70, 1500], H=128, Hk=16, D=128),  # 2 head groups
+    # many blocks per CTA range, every sequence cut several times
+    dict(index=307, lens=[3000 + 37 * i for i in range(16)], H=8, Hk=8, D=128),
 ])
 def test_noalloc_matches_workspace_entry_point_twice(lib, case):
     wl = W.small_decode(case["index"], case["lens"], H=case["H"], Hk=case["Hk"], D=case["D"])
