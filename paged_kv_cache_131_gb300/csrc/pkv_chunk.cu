@@ -1001,8 +1001,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // a ticket per (sequence, kv head, tile, softmax warp): the warp
             // that brings the last partition of its rows and dimensions
-            // merges them
-            __threadfence();
+            // merges them.  The warp barrier orders every lane's partial
+            // before lane 0's releasing ticket; the last taker acquires the
+            // other partitions' partials.
             __syncwarp();
             int last = 0;
             if (lane == 0) {
@@ -1010,13 +1011,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                               ((static_cast<int64_t>(seq) * Hk + kvh) * p.num_tiles + tile) *
                                   kSoftmaxWarps +
                               (warp - 3);
-                last = atomicAdd(ticket, 1) == nparts - 1;
-                if (last) {
-                    atomicExch(ticket, 0);  // leave the workspace zeroed
-                    __threadfence();
-                }
+                last = atom_add_acq_rel_gpu(ticket, 1) == nparts - 1;
+                // every partition has taken its ticket: leave the workspace zeroed
+                if (last) st_relaxed_gpu(ticket, 0);
             }
             last = __shfl_sync(0xffffffffu, last, 0);
+            __syncwarp();  // memory order: lane 0's acquire before every lane's loads
             if (!last || !row_ok) continue;
             // the tile's last partition: merge every partition's partial row
             float M = kNegInf;

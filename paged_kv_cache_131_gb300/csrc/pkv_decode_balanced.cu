@@ -485,22 +485,22 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
             st.write_partial(p.part_ml + base, p.part_o + base * D, qr.ncols, lane);
         else
             st.write_partial(p.part_ml + base, p.part_o + base * D, lane);
-        __threadfence();
+        // The warp barrier orders every lane's partial stores before lane 0's
+        // releasing ticket; the last taker acquires all contributors' stores,
+        // and the shuffle below passes that on to the other lanes.
         __syncwarp();
         const int c_a = cta_of(f_s, T, N), c_b = cta_of(f_e - 1, T, N);
         int last = 0;
         if (lane == 0) {
             int *ticket = p.counters + static_cast<int64_t>(seq) * Hk + kvh;
-            __threadfence();
-            const int prev = atomicAdd(ticket, 1);
+            const int prev = atom_add_acq_rel_gpu(ticket, 1);
             last = prev == c_b - c_a;
-            if (last) {
-                atomicExch(ticket, 0);  // leave the workspace zeroed
-                __threadfence();
-            }
+            // every contributor has taken its ticket: leave the workspace zeroed
+            if (last) st_relaxed_gpu(ticket, 0);
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
+            __syncwarp();  // memory order: lane 0's acquire before every lane's loads
             if constexpr (Policy::kColumns)
                 combine_partials<D, Policy::kRows>(p, kvh, hl, c_a, c_b, f_s, T, N, lane,
                                                    qr.row0, qr.ncols, G);

@@ -225,18 +225,16 @@ __global__ void __launch_bounds__(kThreads)
     if (nparts == 1) return;
 
     // ---- split-KV: the last CTA of this (sequence, kv_head) combines.  The
-    // barrier makes every thread's partial visible to thread 0, whose fence
-    // (cumulative) orders them before its ticket.
+    // barrier orders every thread's partial before thread 0's releasing
+    // ticket (a release is cumulative); the last taker acquires the other
+    // CTAs' partials, and the second barrier passes that on to its threads.
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
         int *ticket = p.counters + static_cast<int64_t>(seq) * p.num_kv_heads + kvh;
-        const int prev = atomicAdd(ticket, 1);
+        const int prev = atom_add_acq_rel_gpu(ticket, 1);
         const int last = prev == nparts - 1;
-        if (last) {
-            atomicExch(ticket, 0);  // leave the workspace zeroed
-            __threadfence();
-        }
+        // every partition has taken its ticket: leave the workspace zeroed
+        if (last) st_relaxed_gpu(ticket, 0);
         misc[1] = last;
     }
     __syncthreads();

@@ -148,6 +148,27 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 
 // ---------------------------------------------------------------------------
+// Device-scope tickets.
+
+// Atomic add with acquire-release semantics at GPU scope: writes that happen
+// before it (this thread's, and those of threads that reached a barrier with
+// this thread first) are visible to whoever later acquires the location, and
+// writes released by earlier adders are visible to this thread afterwards.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Relaxed store at GPU scope (no ordering with this thread's other accesses).
+__device__ __forceinline__ void st_relaxed_gpu(int *p, int v) {
+    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Warp-level matrix helpers (fp16 in, fp32 accumulate).
 
 __device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
