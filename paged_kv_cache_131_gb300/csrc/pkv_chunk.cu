@@ -35,16 +35,16 @@
 //    (N = head_dim, 16 keys per MMA) with the weights P read from tensor
 //    memory (two buffers).  An MMA that depends on the previous one holds
 //    its issuer back, so each chain has its own issuing warp;
-//  * warps 3-10 run the softmax, one thread per query row and half of each
-//    step's keys per group of four warps: they read the row's scores, mask
-//    keys past the row's position (and past the sequence or in a bad
-//    block), exchange the half-row maxima with the other group's thread of
-//    the row, keep the row's running maximum m and the sums l in the log2
-//    domain and write the fp16 weights P = 2^(s - m) back to tensor memory.
-//    The reference m moves only when the maximum grows by more than 2^8
-//    (the weights stay <= 256): then each group rescales its half of O in
-//    tensor memory first.  The result O / l does not depend on which
-//    reference was used.
+//  * warps 3-10 run the softmax, two threads of one warp per query row,
+//    each with half of each step's keys (tensor-memory loads of two 16-lane
+//    halves): they read the row's scores, mask keys past the row's position
+//    (and past the sequence or in a bad block), combine the two half-row
+//    maxima with one shuffle, keep the row's running maximum m and the sums
+//    l in the log2 domain and write the fp16 weights P = 2^(s - m) back to
+//    tensor memory.  The reference m moves only when the maximum grows by
+//    more than 2^8 (the weights stay <= 256): then each thread rescales its
+//    half of the row's O in tensor memory first.  The result O / l does not
+//    depend on which reference was used.
 // A tile whose causal range fits one partition writes fp16 out; otherwise
 // every partition leaves fp32 partial states (m, l, O) and, per softmax warp,
 // the last CTA of the tile to take a ticket merges them with a log-sum-exp
@@ -78,8 +78,9 @@ constexpr int kKStages = 3;                    // key ring depth (steps)
 constexpr int kVStages = 2;                    // value ring depth (steps)
 constexpr int kPartTokens = 4096;              // KV partition
 constexpr int kPartBlocks = kPartTokens / kBS;
-// softmax: two groups of four warps; warp (3 + 4 grp + q) takes row quarter
-// q (tensor-memory lanes 32 q ..) and keys 64 grp .. 64 grp + 63 of a step
+// softmax: eight warps; warp 3 + 4 wh + q takes the rows (tensor-memory
+// lanes) 32 q + 16 wh .. + 15, two threads per row: lanes 16 h + i take keys
+// 64 h .. 64 h + 63 of a step and the head dimensions (D/2) h .. of O
 constexpr int kSoftmaxWarps = 8;
 constexpr int kGroupKeys = kStepKeys / 2;
 constexpr int kPVWarp = 3 + kSoftmaxWarps;  // issues the P V MMAs (warp 2 the score MMAs)
@@ -135,8 +136,8 @@ struct ChunkParams {
     int64_t num_blocks;
     int *counters;    // [S][Hk][num_tiles][8] tickets (one per softmax warp), zero between calls
     // partial states, row index R = kv_head * Tq * G + query_start * G + tile
-    // row (the rows of a warp are consecutive): (m, l) [2 groups][parts][R]
-    // (each softmax group keeps a copy), O [parts][D][R]
+    // row (the rows of a half-warp are consecutive): (m, l) [2 halves][parts][R]
+    // (each half-warp keeps a copy), O [parts][D][R]
     float2 *part_ml;
     float *part_o;
     ErrorRecord *err;
@@ -151,8 +152,8 @@ struct ItemInfo {
 };
 
 // Shared memory (from a 1024-aligned base): the query tile being staged,
-// the key ring, the value ring, the mbarriers, two item records, the row
-// maxima the two softmax groups exchange, and a few words.
+// the key ring, the value ring, the mbarriers, two item records and a few
+// words.
 template <int D>
 struct Geo {
     static constexpr int kChunks = D / 64;                   // 128-byte chunks of a head row
@@ -163,10 +164,9 @@ struct Geo {
     static constexpr int kOffK = kQ;
     static constexpr int kOffV = kOffK + kKStages * kK;
     static constexpr int kOffBar = kOffV + kVStages * kV;
-    static constexpr int kBars = 2 + 2 + 1 + 1 + 2 * kKStages + 2 * kVStages + 1 + 1 + 2 + 2 + 1 + 4;
+    static constexpr int kBars = 2 + 2 + 1 + 1 + 2 * kKStages + 2 * kVStages + 1 + 1 + 2 + 2 + 1;
     static constexpr int kOffInfo = kOffBar + kBars * 8;
-    static constexpr int kOffX = kOffInfo + 2 * static_cast<int>(sizeof(ItemInfo));
-    static constexpr int kOffMisc = kOffX + 2 * 2 * kRows * 4;  // float [2 phases][2 groups][rows]
+    static constexpr int kOffMisc = kOffInfo + 2 * static_cast<int>(sizeof(ItemInfo));
     static constexpr int kBytes = kOffMisc + 16;
 };
 
@@ -193,8 +193,6 @@ struct Bars {
     __device__ uint32_t p_full(int s) const { return b + 8 * (kS + 2 + s); }
     __device__ uint32_t pv_done(int s) const { return b + 8 * (kS + 4 + s); }
     __device__ uint32_t o_free() const { return b + 8 * (kS + 6); }
-    // row-maximum exchange between the two softmax warps of a row quarter
-    __device__ uint32_t xbar(int q) const { return b + 8 * (kS + 7 + q); }
 };
 
 // arrivals that free an item record: the value producer, the two MMA warps
@@ -498,14 +496,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     chunk_attention_kernel(const __grid_constant__ ChunkParams p) {
     using Gm = Geo<D>;
     constexpr int CH = Gm::kChunks;
-    constexpr int DH = D / 2;  // the head dimensions (of O) each softmax group owns
+    constexpr int DH = D / 2;  // the head dimensions (of O) each softmax thread owns
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((dec::kTileAlign - (smem_u32(smem_raw) & (dec::kTileAlign - 1))) &
                                 (dec::kTileAlign - 1));
     const uint32_t sb = smem_u32(smem);
     const Bars br{sb + Gm::kOffBar};
     ItemInfo *info = reinterpret_cast<ItemInfo *>(smem + Gm::kOffInfo);
-    volatile float *xrow = reinterpret_cast<volatile float *>(smem + Gm::kOffX);
     // misc: [0] tensor-memory base
     volatile int *misc = reinterpret_cast<volatile int *>(smem + Gm::kOffMisc);
 
@@ -532,7 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(br.s_full(), 1);
         mbar_init(br.s_free(), kSoftmaxWarps);
         mbar_init(br.o_free(), kSoftmaxWarps);
-        for (int q = 0; q < 4; ++q) mbar_init(br.xbar(q), 2);
         fence_mbarrier_init();
     }
     // the work list, the caches and the outputs are written by earlier
@@ -794,28 +790,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) record_error(p.err, PKV_DEVERR_TIMEOUT, blockIdx.x);
     } else {
         // =============================== softmax ===============================
-        // one row per thread, half of each step's keys per group; a warp
-        // reaches tensor-memory lanes 32 * (warp % 4) ...
-        const int grp = (warp - 3) >> 2;
+        // two threads per row: lane 16 h + i of warp 3 + 4 wh + q holds row
+        // 32 q + 16 wh + i, keys 64 h .. of each step and head dimensions
+        // DH h .. of O; a warp reaches tensor-memory lanes 32 * (warp % 4) ..
+        const int wh = (warp - 3) >> 2;
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;
-        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int h = lane >> 4;
+        const int r = quarter * 32 + wh * 16 + (lane & 15);
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32 + wh * 16) << 16);
         const int64_t Tq = p.num_query_tokens;
         const float sl2 = p.scale_log2;
         int gs = 0;
-        int xs = 0;  // exchanges with the other group's warp of this row quarter
         bool ok = true;
-        // exchange one float per row with the partner warp; false on a timeout
-        auto exchange = [&](float mine, float &theirs) -> bool {
-            volatile float *x = xrow + (xs & 1) * (2 * kRows);
-            x[grp * kRows + r] = mine;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(br.xbar(quarter));
-            if (!wait_all(br.xbar(quarter), xs & 1)) return false;
-            theirs = x[(grp ^ 1) * kRows + r];
-            ++xs;
-            return true;
-        };
         for (int it = 0; ok; ++it) {
             const int slot = it & 1;
             if (!wait_all(br.q_full(slot), (it >> 1) & 1)) {
@@ -838,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = rr >> logG;
             const int lim = row_ok ? L - Q + j : -1;  // last key position this row sees
             const int64_t orow = static_cast<int64_t>(q0 + j) * H + kvh * G + (rr & (G - 1));
-            float m_used = kNegInf, l = 0.f;  // l: this group's keys only
+            float m_used = kNegInf, l = 0.f;  // l: this thread's keys only
 
             for (int n = 0; n < nsteps; ++n) {
                 const int g = gs + n;
@@ -847,24 +833,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc::fence_after_sync();
-                uint32_t sx[kGroupKeys];  // this row's scores of this group's keys (fp32 bits)
+                uint32_t sx[kGroupKeys];  // this row's scores of this thread's keys (fp32 bits)
 #pragma unroll
                 for (int c = 0; c < kGroupKeys / 32; ++c)
-                    tc::ld32(tl + kTmemS + kGroupKeys * grp + 32 * c,
-                             *reinterpret_cast<uint32_t(*)[32]>(sx + 32 * c));
+                    tc::ld32_halves<kGroupKeys>(tl + kTmemS + 32 * c,
+                                                *reinterpret_cast<uint32_t(*)[32]>(sx + 32 * c));
                 tc::wait_ld();
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(br.s_free());
                 const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
-                const int nbg = min(max(nb - 4 * grp, 0), 4);  // this group's blocks
-                const int kbase = part * kPartTokens + n * kStepKeys + kGroupKeys * grp;
-                const int b0 = n * kStepBlocks + 4 * grp;
+                const int nbg = min(max(nb - 4 * h, 0), 4);  // this thread's blocks
+                const int kbase = part * kPartTokens + n * kStepKeys + kGroupKeys * h;
+                const int b0 = n * kStepBlocks + 4 * h;
                 const uint32_t vmask = (valid[b0 >> 5] >> (b0 & 31)) & 0xFu;
-                // every key visible (and a non-negative scale): the maximum of
-                // the raw scores, scaled once; else scale and mask each score
-                const bool fast = nbg == 4 && vmask == 0xFu && kbase + kGroupKeys - 1 <= lim &&
-                                  sl2 >= 0.f;
+                // every key of the warp visible (and a non-negative scale):
+                // the maximum of the raw scores, scaled once; else scale and
+                // mask each score
+                const bool fast = __all_sync(0xffffffffu, nbg == 4 && vmask == 0xFu &&
+                                                              kbase + kGroupKeys - 1 <= lim &&
+                                                              sl2 >= 0.f);
                 float mr[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mr[i] = kNegInf;
@@ -883,15 +871,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])),
                                  fmaxf(fmaxf(mr[4], mr[5]), fmaxf(mr[6], mr[7])));
                 if (fast) mx *= sl2;
-                float mo;
-                if (!exchange(mx, mo)) {
-                    ok = false;
-                    break;
-                }
+                // the row's other half: the thread 16 lanes away
+                const float mo = __shfl_xor_sync(0xffffffffu, mx, 16);
                 const float m_new = fmaxf(m_used, fmaxf(mx, mo));
                 const bool raise = m_new > m_used + kRescaleLog2;
                 // O holds this item's earlier steps relative to m_used: rescale
-                // this group's columns before the reference moves (the
+                // this thread's columns before the reference moves (the
                 // previous P V done first)
                 const bool resc = raise && n > 0 && m_used != kNegInf;
                 if (__any_sync(0xffffffffu, resc)) {
@@ -904,12 +889,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < DH / 32; ++c) {
                         uint32_t x[32];
-                        tc::ld32(tl + kTmemO + DH * grp + 32 * c, x);
+                        tc::ld32_halves<DH>(tl + kTmemO + 32 * c, x);
                         tc::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             x[e] = __float_as_uint(__uint_as_float(x[e]) * alpha);
-                        tc::st32(tl + kTmemO + DH * grp + 32 * c, x);
+                        tc::st32_halves<DH>(tl + kTmemO + 32 * c, x);
                     }
                     tc::wait_st();
                     l *= alpha;
@@ -917,8 +902,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (raise) m_used = m_new;
                 const float ms = m_used == kNegInf ? 0.f : m_used;
                 // weights 2^(s * scale - m) (2^(t - m) for the masked scores),
-                // fp16 pairs: column i of the group's half holds its keys 2i,
-                // 2i+1; the P V of two steps back must be done with this buffer
+                // fp16 pairs: column 32 h + i of the buffer holds keys
+                // 64 h + 2i, 2i+1; the P V of two steps back must be done
+                // with this buffer
                 const float a = fast ? sl2 : 1.f;
                 const int pb = g & 1;
                 if (g >= 2) {
@@ -937,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l4[e & 3] += p0 + p1;
                     x[e] = pack_half2(p0, p1);
                 }
-                tc::st32(tl + kTmemP + 64 * pb + 32 * grp, x);
+                tc::st32_halves<32>(tl + kTmemP + 64 * pb, x);
                 l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 tc::wait_st();
                 tc::fence_before_sync();
@@ -948,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             gs += nsteps;
 
             // ---- the item's output: O / l, or the partial state (m, l, O),
-            // this group's head dimensions
+            // this thread's head dimensions
             if (!wait_all(br.pv_done((gs - 1) & 1), ((gs - 1) >> 1) & 1)) {
                 ok = false;
                 break;
@@ -959,8 +945,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t ob[DH];
 #pragma unroll
                 for (int c = 0; c < DH / 32; ++c)
-                    tc::ld32(tl + kTmemO + DH * grp + 32 * c,
-                             *reinterpret_cast<uint32_t(*)[32]>(ob + 32 * c));
+                    tc::ld32_halves<DH>(tl + kTmemO + 32 * c,
+                                        *reinterpret_cast<uint32_t(*)[32]>(ob + 32 * c));
                 tc::wait_ld();
 #pragma unroll
                 for (int d = 0; d < DH; ++d) o[d] = __uint_as_float(ob[d]);
@@ -968,16 +954,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(br.o_free());
-            float lo;
-            if (!exchange(l, lo)) {
-                ok = false;
-                break;
-            }
-            l += lo;  // the row's sum over both groups' keys
+            l += __shfl_xor_sync(0xffffffffu, l, 16);  // the row's sum over both halves' keys
             if (nparts == 1) {
                 if (row_ok) {
                     const float inv = l > 0.f ? 1.f / l : 0.f;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + DH * grp);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + DH * h);
 #pragma unroll
                     for (int c = 0; c < DH / 8; ++c)
                         dst[c] = make_uint4(pack_half2(o[8 * c] * inv, o[8 * c + 1] * inv),
@@ -987,23 +968,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 continue;
             }
-            // partial state, dimension-major so a warp's 32 rows are
-            // consecutive words (coalesced); each group keeps its own (m, l)
+            // partial state, dimension-major so the rows of a half-warp are
+            // consecutive words; each half keeps its own copy of (m, l)
             const int64_t NR = Tq * H;
             const int64_t R = static_cast<int64_t>(kvh) * Tq * G + static_cast<int64_t>(q0) * G + rr;
             const int64_t parts_total = p.num_parts;
-            float2 *ml = p.part_ml + grp * parts_total * NR;
+            float2 *ml = p.part_ml + h * parts_total * NR;
             if (row_ok) {
                 ml[part * NR + R] = make_float2(m_used, l);
-                float *dst = p.part_o + (static_cast<int64_t>(part) * D + DH * grp) * NR + R;
+                float *dst = p.part_o + (static_cast<int64_t>(part) * D + DH * h) * NR + R;
 #pragma unroll
                 for (int d = 0; d < DH; ++d) dst[d * NR] = o[d];
             }
             // a ticket per (sequence, kv head, tile, softmax warp): the warp
-            // that brings the last partition of its rows and dimensions
-            // merges them.  The warp barrier orders every lane's partial
-            // before lane 0's releasing ticket; the last taker acquires the
-            // other partitions' partials.
+            // that brings the last partition of its rows merges them.  The
+            // warp barrier orders every lane's partial before lane 0's
+            // releasing ticket; the last taker acquires the other
+            // partitions' partials.
             __syncwarp();
             int last = 0;
             if (lane == 0) {
@@ -1028,12 +1009,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 v = __ldcg(ml + pp * NR + R);
                 const float w = v.x == kNegInf ? 0.f : ex2(v.x - M);
                 den = fmaf(v.y, w, den);
-                const float *src = p.part_o + (static_cast<int64_t>(pp) * D + DH * grp) * NR + R;
+                const float *src = p.part_o + (static_cast<int64_t>(pp) * D + DH * h) * NR + R;
 #pragma unroll
                 for (int d = 0; d < DH; ++d) o[d] = fmaf(__ldcg(src + d * NR), w, o[d]);
             }
             const float inv = den > 0.f ? 1.f / den : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + DH * grp);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + DH * h);
 #pragma unroll
             for (int c = 0; c < DH / 8; ++c)
                 dst[c] = make_uint4(pack_half2(o[8 * c] * inv, o[8 * c + 1] * inv),
