@@ -27,8 +27,9 @@ workloads of the hot path, each event-timed the same way (L2 flushed before
 every step) with its own roofline and clock record -- long-context decode,
 shared-prefix decode (logical bytes, DRAM bytes and L2 hit rate), the
 two-cache byte-strided write in both layouts (one launch and one launch per
-(cache, layer) view), FP8 decode of the first two, and the multi-token
-steps (chunked prefill, draft verification).
+(cache, layer) view), FP8 decode of the first two, the multi-token steps
+(chunked prefill, draft verification), and the chunked-prefill chunk alone
+(`6.chunk`: the tcgen05 tile kernel on every SM, tensor-bound).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config 2|3|4|5|6|7] [--compute auto|simt|mma] [--kv fp16|fp8]
@@ -68,8 +69,11 @@ FALLBACK_HBM_GBS = 6800.0
 HEADLINE_TIMED_S = 1.0
 EXTRA_TIMED_S = 0.3
 MAX_PASSES = 4000
-EXTRAS_DEFAULT = "3,4,5,2.fp8,3.fp8,6,7"
+EXTRAS_DEFAULT = "3,4,5,2.fp8,3.fp8,6,6.chunk,7"
 
+CHUNK_ONLY_NAME = ("chunked-prefill chunk alone: the 952-token chunk of config 6 (positions "
+                   "2048..2999 of a 3000-token prompt) without the decodes, bs=16, H=32, Hk=8, "
+                   "D=128, new rows written first")
 WORKLOAD_NAMES = {
     2: "llama3-8b decode layer: S=64, L~U[256,4096], bs=16, H=32, Hk=8, D=128, "
        "fp16 cache [16384,16,8,128], 1 new token/seq written",
@@ -118,7 +122,7 @@ def parse(argv=None):
                     help="repeat the K-step timed pass until this much timed device work")
     ap.add_argument("--extras", default=EXTRAS_DEFAULT,
                     help="comma list of other workloads timed into `configs` with the default "
-                         "workload (3, 4, 5, 2.fp8, 3.fp8, 6, 7), or 'none'")
+                         "workload (3, 4, 5, 2.fp8, 3.fp8, 6, 6.chunk, 7), or 'none'")
     return ap.parse_args(argv)
 
 
@@ -735,8 +739,11 @@ def chunk_entry(key, wl, m, peak, peak_kind):
     roof, attn_ms = chunk_roofline(wl, m, peak, peak_kind)
     st, ak = spread(m["step_passes"]), spread(m["attn_ms"])
     Tq = wl.q.shape[0]
+    if key.endswith(".chunk"):
+        roof["kernel"] = ("attention call = chunk_plan_kernel (one CTA) + chunk_attention_kernel "
+                          "(tcgen05) on every SM")
     return {
-        "workload": WORKLOAD_NAMES[int(key)],
+        "workload": CHUNK_ONLY_NAME if key.endswith(".chunk") else WORKLOAD_NAMES[int(key)],
         "value": round(wl.kv_bytes() / (st["median"] * 1e-3) / 1e9, 2), "unit": UNIT,
         "ms_per_step": round(st["median"], 5),
         "ms_per_step_p10_p90": [round(st["p10"], 5), round(st["p90"], 5)],
@@ -811,7 +818,9 @@ def run_extras(args, keys, local, flush, stream, peak, peak_kind):
     for key in keys:
         cfg = int(key.split(".")[0])
         kv = "fp8" if key.endswith(".fp8") else "fp16"
-        wl = W.config(cfg)
+        # "6.chunk": the chunk of config 6 without its decodes
+        wl = (W.config6_chunked_prefill(num_decodes=0) if key.endswith(".chunk")
+              else W.config(cfg))
         if cfg == 5:
             dev, entry = measure_write(wl, args, local, flush, stream, EXTRA_TIMED_S, peak,
                                        peak_kind)

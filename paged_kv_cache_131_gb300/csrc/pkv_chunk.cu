@@ -77,6 +77,7 @@ constexpr int kStepKeys = kStepBlocks * kBS;   // 128 keys: the score MMA's N
 constexpr int kKStages = 3;                    // key ring depth (steps)
 constexpr int kVStages = 2;                    // value ring depth (steps)
 constexpr int kPartTokens = 4096;              // KV partition
+constexpr int kClaimLead = 1;                  // steps staged after the next item is claimed
 constexpr int kPartBlocks = kPartTokens / kBS;
 // softmax: eight warps; warp 3 + 4 wh + q takes the rows (tensor-memory
 // lanes) 32 q + 16 wh .. + 15, two threads per row: lanes 16 h + i take keys
@@ -98,7 +99,7 @@ constexpr float kRescaleLog2 = 8.f;            // move the reference past 2^8
 // (single precision: this GPU's double-precision rate is low)
 constexpr float kHbmBytesPerUs = 6.0e6f;        // decode stream, whole GPU
 constexpr float kSmBytesPerUs = 58.0e3f;        // decode stream per SM
-constexpr float kTileStepUs = 1.7f;             // one 128-key step of a tile
+constexpr float kTileStepUs = 1.4f;             // one 128-key step of a tile
 
 struct ChunkParams {
     CUtensorMap tm_k;  // keys: one 128-byte chunk of 16 rows per copy
@@ -364,8 +365,8 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
     // min(HBM rate, SMs x per-SM rate); tile: its steps at a per-step cost
     // over the remaining SMs, plus half an average item for the last wave.
     // Rates measured on this GPU (chunked prefill beside decodes: the decode
-    // kernel streams ~58 GB/s per SM when it shares the GPU, a tile step
-    // costs ~1.7 us beside it).  Thread i tries 2 + 2i SMs; the smallest
+    // kernel streams ~58 GB/s per SM when it shares the GPU; a tile step
+    // costs 1.1-1.6 us beside it, 1.4 gave the shortest calls).  Thread i tries 2 + 2i SMs; the smallest
     // estimate wins (ties: fewer SMs).
     __shared__ unsigned long long best_w[32];
     unsigned long long key = ~0ull;
@@ -435,12 +436,15 @@ __device__ __forceinline__ int id_of(const int (&ids)[kPartBlocks / 32], int b) 
 }
 
 // The (partition, kv head, tile) of item `local` of a sequence: partition-
-// major, then kv head, then tile (consecutive items share their keys).
+// major, then tile (the last first), then kv head.
 __device__ __forceinline__ int3 decode_item(const SeqGeo &sg, int local, int G, int Hk) {
     for (int pt = 0; pt < sg.parts; ++pt) {
         const int t0 = first_tile(sg, pt, G);
         const int nt = sg.tiles - t0;
-        if (local < nt * Hk) return make_int3(pt, local / nt, t0 + local % nt);
+        // a partition's tiles longest first (a later tile sees more keys),
+        // every KV head of a tile together, so the CTAs that finish first
+        // take the short ones at the end
+        if (local < nt * Hk) return make_int3(pt, local % Hk, sg.tiles - 1 - local / Hk);
         local -= nt * Hk;
     }
     return make_int3(-1, -1, -1);
@@ -593,11 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < CH)
                 tensor_g2s_3d(sb + lane * (kRows * 128), &p.tm_q, 128 * lane, cur.kvh * G,
                               cur.q0 + cur.tile * (kRows >> logG), br.qs_full());
-            // the next item is taken once this one's first steps are staged
-            // (its lookups then overlap this item's work)
+            // the next item is taken when this one's last steps are staged,
+            // a ring's depth before its softmax ends: the CTAs that finish
+            // first take the next items (its lookups overlap those steps)
             Fetched nxt;
             nxt.done = 1;
-            const int fetch_at = min(cur.nsteps, kKStages) - 1;
+            const int fetch_at = max(cur.nsteps - kClaimLead, 0);
             for (int n = 0; n < cur.nsteps; ++n, ++gs) {
                 const int ks = gs % kKStages;
                 if (gs >= kKStages && !wait_all(br.k_empty(ks), ((gs / kKStages) - 1) & 1)) {

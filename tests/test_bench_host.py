@@ -71,7 +71,7 @@ def test_default_run_is_short_and_times_every_workload():
     args = bench.parse([])
     assert (args.gpus, args.steps, args.warmup, args.config) == (1, 20, 5, 2)
     keys = args.extras.split(",")
-    assert {"3", "4", "5", "2.fp8", "3.fp8", "6", "7"} == set(keys)
+    assert {"3", "4", "5", "2.fp8", "3.fp8", "6", "6.chunk", "7"} == set(keys)
 
 
 def test_config5_write_bytes_count_the_slot_mapping_once():
