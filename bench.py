@@ -116,6 +116,8 @@ def parse(argv=None):
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--kv-heads", type=int, default=8,
                     help="config 2 only: KV heads of the layer (query heads = 4x), same lengths")
+    ap.add_argument("--chunk-only", action="store_true",
+                    help="config 6 only: the chunk without the decodes (the tile kernel alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--timed-s", type=float, default=HEADLINE_TIMED_S,
@@ -479,7 +481,8 @@ def reference_line(args, gbs, t, n, sample):
         "ms_per_step": round(t / max(n, 1) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64" if args.config != 5 else "u8",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES[args.config], "sample": sample},
+        "config": {"workload": CHUNK_ONLY_NAME if args.chunk_only else WORKLOAD_NAMES[args.config],
+                   "sample": sample},
         "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample, **host_cpu_info()},
         "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -913,7 +916,8 @@ def main_chunk(args, wl, rank, world, local):
         "vs_baseline": None,
         "dtype": "f16xf16->f32",
         "data": "synthetic (seeded N(0,1) fp16, shuffled physical blocks)",
-        "config": {"workload": WORKLOAD_NAMES[args.config], "global_batch": wl.num_seqs * world,
+        "config": {"workload": CHUNK_ONLY_NAME if args.chunk_only else WORKLOAD_NAMES[args.config],
+                   "global_batch": wl.num_seqs * world,
                    "query_tokens": Tq, "seq_len": int(wl.max_seq_len),
                    "parallelism": f"replicas x{world}", "l2": L2_NOTE,
                    "kv_cache": "resident in HBM (state), not copied per step"},
@@ -1020,8 +1024,14 @@ def main():
     rank, world, local = dist_env()
     from paged_kv_cache_131_gb300 import workloads as W
 
-    wl = (W.config2_llama8b(num_kv_heads=args.kv_heads) if args.config == 2 and
-          args.kv_heads != 8 else W.config(args.config))
+    if args.chunk_only and args.config != 6:
+        raise SystemExit("--chunk-only goes with --config 6")
+    if args.chunk_only:
+        wl = W.config6_chunked_prefill(num_decodes=0)
+    elif args.config == 2 and args.kv_heads != 8:
+        wl = W.config2_llama8b(num_kv_heads=args.kv_heads)
+    else:
+        wl = W.config(args.config)
     if args.impl == "reference":
         run_reference(args, wl, rank)
         return
