@@ -675,8 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 2) {
         // ============================ score MMAs ============================
-        // (one issuing thread; an MMA that depends on the previous one holds
-        // its issuer back, so the scores and the P V products have one
+        // (one issuing thread; inside this kernel each MMA held its issuer
+        // back ~110-140 cycles, so the scores and the P V products have one
         // issuing warp each and their chains overlap in the tensor pipe)
         int gs = 0;
         bool ok = true;
@@ -714,9 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    // one MMA per k step over the step's keys (each MMA
-                    // instruction costs the issuing thread about the same
-                    // whatever its N, so fewer and wider ones are faster)
+                    // one MMA per k step over the step's keys (an MMA of
+                    // N 64 or less costs the issuing thread about as much as
+                    // one of N 128, so fewer and wider ones are faster)
                     const int nb = min(kStepBlocks, nblk - n * kStepBlocks);
                     const uint32_t idesc = tc::idesc_f16_f32(kRows, nb * kBS, false, false);
                     const uint32_t k_s = sb + Gm::kOffK + ks * Gm::kK;
