@@ -257,6 +257,21 @@ __device__ __forceinline__ void balanced_body(const BalancedParams &p, uint8_t *
     // tables and queries are read before grid_dependency_wait(); the caches
     // and the outputs are touched only after it.
 
+    // While the lengths below make their round trip: the copies' tensor maps,
+    // and this CTA's share of the block table into L2 (a small table only),
+    // so the block-table window it reads next is an L2 hit.
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&p.tm_k);
+        prefetch_tensormap(&p.tm_v);
+    }
+    if (static_cast<int64_t>(S) * p.max_blocks_per_seq <= (int64_t(4) << 20)) {  // <= 16 MB
+        const int lines = (S * p.max_blocks_per_seq * 4 + 127) >> 7;
+        const int per = (lines + grid - 1) / grid, end = min(lines, (blockIdx.x + 1) * per);
+        const char *tb = reinterpret_cast<const char *>(p.block_tables);
+        for (int i = blockIdx.x * per + threadIdx.x; i < end; i += nthreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + static_cast<size_t>(i) * 128));
+    }
+
     // ---- lengths (clamped to the block table) and their block-count prefix sum
     const int cap = p.max_blocks_per_seq * kBS;
     const int chunk = (S + nthreads - 1) / nthreads;

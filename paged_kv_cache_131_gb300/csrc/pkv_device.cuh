@@ -110,6 +110,11 @@ __device__ __forceinline__ void tensor_g2s_3d(uint32_t dst, const void *tmap, in
         : "memory");
 }
 
+// Fetch a tensor map (a kernel parameter) ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 // Same with an L2 cache-policy hint (createpolicy).
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes,
                                               uint32_t bar, uint64_t policy) {
