@@ -143,6 +143,26 @@ def test_fp8_full_size_all_elements(pkv, cfg):
     _close(out, ref)
 
 
+@pytest.mark.parametrize("S,H,Hk", [(800, 32, 8), (400, 64, 16)])
+def test_fp8_many_short_sequences_every_element(pkv, S, H, Hk):
+    """Many short sequences, several whole ones in every CTA range and cut
+    ones at both ends, so each consumer warp finishes, writes and merges
+    many times per launch; Hk 16 adds a second head group.  Every element
+    against the oracle, two calls in a row."""
+    from paged_kv_cache_131_gb300.harness import DeviceDecodeFp8
+    lens = [17 + (53 * i) % 250 for i in range(S)]
+    wl = W.small_decode(509 + Hk, lens, H=H, Hk=Hk, D=128)
+    dev = DeviceDecodeFp8(wl)
+    dev.write()
+    k8, v8, ks, vs = _oracle_fp8_state(wl, workers=oracle.default_workers())
+    ref = oracle.decode_attention_fp8(wl.q, k8, v8, ks, vs, wl.block_tables, wl.seq_lens,
+                                      wl.scale, workers=oracle.default_workers())
+    for _ in range(2):
+        dev.out.fill_(float("nan"))
+        _close(dev.decode().cpu().numpy(), ref)
+    assert pkv.pkv_get_device_error() == (0, -1)
+
+
 def test_fp8_repeated_calls_every_element(pkv):
     """FP8 decode, calls in a row on one workspace: every call within
     tolerance of the oracle (outputs poisoned before each call)."""
