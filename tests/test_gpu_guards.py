@@ -1,9 +1,10 @@
-"""Writes stay inside their buffers: the attention outputs and the caller's
-workspace are placed inside larger device buffers filled with a sentinel,
-and after two calls every sentinel byte before and after them is unchanged
-(fp16 decode on both schedules, FP8 decode, the multi-token call).  Each
-case splits sequences across CTAs, so partial states, tickets and merges
-all run; the outputs are also checked against the oracle."""
+"""Writes stay inside their buffers: the attention outputs, the caller's
+workspace and a cache being written are placed inside larger device buffers
+filled with a sentinel, and afterwards every sentinel byte before and after
+them is unchanged (fp16 decode on both schedules, FP8 decode, the
+multi-token call, the cache write at every vector width).  The attention
+cases split sequences across CTAs, so partial states, tickets and merges all
+run; every result is also checked against the oracle."""
 
 import numpy as np
 import pytest
@@ -118,3 +119,36 @@ def test_chunk_writes_stay_in_bounds(pkv):
                                  wl.scale, workers=oracle.default_workers())
     _close(dev.out, ref)
     assert pkv.pkv_get_device_error() == (0, -1)
+
+
+@pytest.mark.parametrize("row_width,vec_align", [(2048, 16), (656, 16), (132, 4), (37, 1)])
+def test_cache_write_stays_in_the_cache(pkv, row_width, vec_align):
+    """The cache sits inside a sentinel-filled buffer; slots include the
+    cache's first and last, plus a padding slot and one out of range (both
+    skipped).  Every byte outside the cache keeps its sentinel, and the cache
+    equals the oracle's write."""
+    nb, bs = 8, 16
+    rng = np.random.default_rng(row_width)
+    cache_bytes = nb * bs * row_width
+    buf = torch.full((WS_PAD + cache_bytes + WS_PAD,), WS_SENTINEL, dtype=torch.uint8,
+                     device="cuda")
+    init = rng.integers(0, 256, size=cache_bytes, dtype=np.uint8)
+    cache = buf[WS_PAD:WS_PAD + cache_bytes]
+    cache.copy_(torch.from_numpy(init))
+    slots = np.array([0, nb * bs - 1, -1, 5, nb * bs, 77], dtype=np.int64)
+    rows = rng.integers(0, 256, size=(slots.size, row_width), dtype=np.uint8)
+    view = pkv.pkv_view(0, 0, bs * row_width, row_width, 0)
+    st = pkv.pkv_cache_write(torch.from_numpy(rows).cuda(), None, torch.from_numpy(slots).cuda(),
+                             cache, None, view, bs, nb, check=False)
+    assert st == 0
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert (b[:WS_PAD] == WS_SENTINEL).all() and (b[WS_PAD + cache_bytes:] == WS_SENTINEL).all()
+    ref = init.copy()
+    ok = (slots >= 0) & (slots < nb * bs)
+    oracle.cache_write(ref, rows[ok], slots[ok], offset=0, layer=0, layer_stride=0,
+                       block_stride=bs * row_width, row_width=row_width, block_size=bs,
+                       num_blocks=nb)
+    assert np.array_equal(b[WS_PAD:WS_PAD + cache_bytes], ref)
+    # the out-of-range slot (token 4) was recorded as a slot error, and skipped
+    assert pkv.pkv_get_device_error() == (1, 4)
