@@ -22,8 +22,9 @@
 // first that-many, so the two run side by side on disjoint SMs.
 //
 // Per CTA, warp-specialised, all hand-offs through mbarriers:
-//  * warp 0 takes the items (the next one while the current one is staged),
-//    stages the tile's query rows into shared memory and the partition's
+//  * warp 0 takes the items (the next one when the current one's last step
+//    is staged; the longest items are handed out first), stages the tile's
+//    query rows into shared memory and the partition's
 //    keys, 8 blocks (128 keys) per step, one tensor copy per block and
 //    64-dimension chunk, into a 3-step ring laid out [chunk][key][128 B] so
 //    the 128 keys form one MMA operand;
