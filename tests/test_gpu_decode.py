@@ -267,6 +267,47 @@ def test_non_default_stream(pkv):
     assert_close(out.cpu().numpy(), ref)
 
 
+def test_concurrent_streams_own_workspaces(pkv):
+    """Calls in flight together on four streams, each with its own workspace
+    (fp16 on both schedules and FP8): each result matches the oracle, so no
+    state is shared between calls beyond the device error record."""
+    from paged_kv_cache_131_gb300.harness import DeviceDecode, DeviceDecodeFp8
+    cases = [(221, [3000 + 53 * i for i in range(8)], BALANCED),
+             (222, [2500 + 71 * i for i in range(12)], BALANCED),
+             (223, [1800 + 37 * i for i in range(10)], GRID)]
+    devs = []
+    for index, lens, schedule in cases:
+        wl = W.small_decode(index, lens, H=32, Hk=8, D=128)
+        dev = DeviceDecode(wl, schedule=schedule)
+        dev.write()
+        devs.append((wl, dev))
+    wl8 = W.small_decode(224, [2200 + 89 * i for i in range(9)], H=32, Hk=8, D=128)
+    dev8 = DeviceDecodeFp8(wl8)
+    dev8.write()
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    for _ in range(3):
+        for (wl, dev), s in zip(devs, streams):
+            with torch.cuda.stream(s):
+                dev.out.fill_(float("nan"))
+                dev.decode(stream=s)
+        with torch.cuda.stream(streams[3]):
+            dev8.out.fill_(float("nan"))
+            dev8.decode(stream=streams[3])
+    torch.cuda.synchronize()
+    for wl, dev in devs:
+        k, v = oracle_after_write(wl)
+        ref = oracle.decode_attention(wl.q, k, v, wl.block_tables, wl.seq_lens, wl.scale,
+                                      workers=oracle.default_workers())
+        assert_close(dev.out.cpu().numpy(), ref)
+    from test_gpu_fp8 import _oracle_fp8_state
+    k8, v8, ks, vs = _oracle_fp8_state(wl8, workers=oracle.default_workers())
+    ref8 = oracle.decode_attention_fp8(wl8.q, k8, v8, ks, vs, wl8.block_tables, wl8.seq_lens,
+                                       wl8.scale, workers=oracle.default_workers())
+    assert_close(dev8.out.cpu().numpy(), ref8)
+    assert pkv.pkv_get_device_error() == (0, -1)
+
+
 # ------------------------------------------------------------- bad data
 
 
