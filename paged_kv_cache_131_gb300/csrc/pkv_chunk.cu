@@ -212,6 +212,40 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Packed fp32 pairs (the f32x2 forms of sm_100 and later: one instruction for
+// two lanes' worth of fma or add) and the three-input maximum.
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f32x2_split(uint64_t r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+
+// a * b + c per lane, round to nearest
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Geometry of sequence s for this kernel; false if the sequence is not
 // ours (too few rows) or invalid (recorded when `report`).
 struct SeqGeo {
@@ -864,7 +898,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 8; ++i) mr[i] = kNegInf;
                 if (fast) {
 #pragma unroll
-                    for (int e = 0; e < kGroupKeys; ++e) mr[e & 7] = fmaxf(mr[e & 7], __uint_as_float(sx[e]));
+                    for (int e = 0; e < kGroupKeys / 2; ++e)
+                        mr[e & 7] = fmax3(mr[e & 7], __uint_as_float(sx[2 * e]),
+                                          __uint_as_float(sx[2 * e + 1]));
                 } else {
 #pragma unroll
                     for (int e = 0; e < kGroupKeys; ++e) {
@@ -874,8 +910,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mr[e & 7] = fmaxf(mr[e & 7], t);
                     }
                 }
-                float mx = fmaxf(fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])),
-                                 fmaxf(fmaxf(mr[4], mr[5]), fmaxf(mr[6], mr[7])));
+                float mx = fmax3(fmax3(mr[0], mr[1], mr[2]), fmax3(mr[3], mr[4], mr[5]),
+                                 fmaxf(mr[6], mr[7]));
                 if (fast) mx *= sl2;
                 // the row's other half: the thread 16 lanes away
                 const float mo = __shfl_xor_sync(0xffffffffu, mx, 16);
@@ -920,17 +956,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::fence_after_sync();
                 }
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                // key pairs in packed fp32 lanes: one fma and one add per pair
+                const uint64_t a2 = f32x2(a, a), nms2 = f32x2(-ms, -ms);
+                uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};
                 uint32_t x[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sx[2 * e]), a, -ms));
-                    const float p1 = ex2(fmaf(__uint_as_float(sx[2 * e + 1]), a, -ms));
-                    l4[e & 3] += p0 + p1;
+                    const float2 t = f32x2_split(fma_f32x2(
+                        f32x2(__uint_as_float(sx[2 * e]), __uint_as_float(sx[2 * e + 1])), a2, nms2));
+                    const float p0 = ex2(t.x), p1 = ex2(t.y);
+                    l2[e & 3] = add_f32x2(l2[e & 3], f32x2(p0, p1));
                     x[e] = pack_half2(p0, p1);
                 }
                 tc::st32_halves<32>(tl + kTmemP + 64 * pb, x);
-                l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                const float2 la = f32x2_split(add_f32x2(add_f32x2(l2[0], l2[1]), add_f32x2(l2[2], l2[3])));
+                l += la.x + la.y;
                 tc::wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
