@@ -26,7 +26,7 @@
 //    is staged; the longest items are handed out first), stages the tile's
 //    query rows into shared memory and the partition's
 //    keys, 8 blocks (128 keys) per step, one tensor copy per block and
-//    64-dimension chunk, into a 3-step ring laid out [chunk][key][128 B] so
+//    64-dimension chunk, into a 4-step ring laid out [chunk][key][128 B] so
 //    the 128 keys form one MMA operand;
 //  * warp 1 stages the values, one tensor copy per block, into a 2-step ring;
 //  * warp 2 (one thread) copies the query tile into tensor memory (two
@@ -75,7 +75,7 @@ using dec::kNegInf;
 constexpr int kRows = 128;                     // query rows per tile: the MMA's M
 constexpr int kStepBlocks = 8;                 // blocks per step
 constexpr int kStepKeys = kStepBlocks * kBS;   // 128 keys: the score MMA's N
-constexpr int kKStages = 3;                    // key ring depth (steps)
+constexpr int kKStages = 4;                    // key ring depth (steps)
 constexpr int kVStages = 2;                    // value ring depth (steps)
 constexpr int kPartTokens = 4096;              // KV partition
 constexpr int kClaimLead = 1;                  // steps staged after the next item is claimed
@@ -855,6 +855,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t valid[kPartBlocks / 32];
 #pragma unroll
             for (int w = 0; w < kPartBlocks / 32; ++w) valid[w] = in.valid[w];
+            // every block of the item in range (the usual case): the steps
+            // need no look-up in the array above
+            bool all_valid = true;
+#pragma unroll
+            for (int w = 0; w < kPartBlocks / 32; ++w) {
+                const int nbw = min(max(nblk - 32 * w, 0), 32);
+                const uint32_t need = nbw == 32 ? 0xffffffffu : ((1u << nbw) - 1u);
+                all_valid = all_valid && (valid[w] & need) == need;
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(br.q_empty(slot));
             if (done) break;
@@ -886,22 +895,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nbg = min(max(nb - 4 * h, 0), 4);  // this thread's blocks
                 const int kbase = part * kPartTokens + n * kStepKeys + kGroupKeys * h;
                 const int b0 = n * kStepBlocks + 4 * h;
-                const uint32_t vmask = (valid[b0 >> 5] >> (b0 & 31)) & 0xFu;
-                // every key of the warp visible (and a non-negative scale):
-                // the maximum of the raw scores, scaled once; else scale and
-                // mask each score
+                uint32_t vmask = 0xFu;
+                if (!all_valid) vmask = (valid[b0 >> 5] >> (b0 & 31)) & 0xFu;
+                // the maximum of the raw scores first (independent of the
+                // masks, so the two overlap); it stands, scaled once, when
+                // every key of the warp is visible and the scale is not
+                // negative, else the scores are scaled and masked and their
+                // maximum taken again
                 const bool fast = __all_sync(0xffffffffu, nbg == 4 && vmask == 0xFu &&
                                                               kbase + kGroupKeys - 1 <= lim &&
                                                               sl2 >= 0.f);
                 float mr[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mr[i] = kNegInf;
-                if (fast) {
 #pragma unroll
-                    for (int e = 0; e < kGroupKeys / 2; ++e)
-                        mr[e & 7] = fmax3(mr[e & 7], __uint_as_float(sx[2 * e]),
-                                          __uint_as_float(sx[2 * e + 1]));
-                } else {
+                for (int e = 0; e < kGroupKeys / 2; ++e)
+                    mr[e & 7] = fmax3(mr[e & 7], __uint_as_float(sx[2 * e]),
+                                      __uint_as_float(sx[2 * e + 1]));
+                float mx = fmax3(fmax3(mr[0], mr[1], mr[2]), fmax3(mr[3], mr[4], mr[5]),
+                                 fmaxf(mr[6], mr[7]));
+                if (!fast) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mr[i] = kNegInf;
 #pragma unroll
                     for (int e = 0; e < kGroupKeys; ++e) {
                         const bool vis = e < nbg * kBS && ((vmask >> (e >> 4)) & 1u) && kbase + e <= lim;
@@ -909,10 +924,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sx[e] = __float_as_uint(t);
                         mr[e & 7] = fmaxf(mr[e & 7], t);
                     }
+                    mx = fmax3(fmax3(mr[0], mr[1], mr[2]), fmax3(mr[3], mr[4], mr[5]),
+                               fmaxf(mr[6], mr[7]));
+                } else {
+                    mx *= sl2;
                 }
-                float mx = fmax3(fmax3(mr[0], mr[1], mr[2]), fmax3(mr[3], mr[4], mr[5]),
-                                 fmaxf(mr[6], mr[7]));
-                if (fast) mx *= sl2;
                 // the row's other half: the thread 16 lanes away
                 const float mo = __shfl_xor_sync(0xffffffffu, mx, 16);
                 const float m_new = fmaxf(m_used, fmaxf(mx, mo));
