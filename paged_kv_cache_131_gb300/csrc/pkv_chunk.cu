@@ -100,7 +100,7 @@ constexpr float kRescaleLog2 = 8.f;            // move the reference past 2^8
 // (single precision: this GPU's double-precision rate is low)
 constexpr float kHbmBytesPerUs = 6.0e6f;        // decode stream, whole GPU
 constexpr float kSmBytesPerUs = 58.0e3f;        // decode stream per SM
-constexpr float kTileStepUs = 1.4f;             // one 128-key step of a tile
+constexpr float kTileStepUs = 1.3f;             // one 128-key step of a tile
 
 struct ChunkParams {
     CUtensorMap tm_k;  // keys: one 128-byte chunk of 16 rows per copy
@@ -401,8 +401,9 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const __grid_constant_
     // over the remaining SMs, plus half an average item for the last wave.
     // Rates measured on this GPU (chunked prefill beside decodes: the decode
     // kernel streams ~58 GB/s per SM when it shares the GPU; a tile step
-    // costs 1.1-1.6 us beside it, 1.4 gave the shortest calls).  Thread i tries 2 + 2i SMs; the smallest
-    // estimate wins (ties: fewer SMs).
+    // costs ~1-1.5 us beside it, 1.2-1.3 gave the shortest calls, 1.1 far
+    // longer ones).  Thread i tries 2 + 2i SMs; the smallest estimate wins
+    // (ties: fewer SMs).
     __shared__ unsigned long long best_w[32];
     unsigned long long key = ~0ull;
     if (dec_blocks > 0) {
