@@ -98,8 +98,12 @@ DECODE_SOURCES = [os.path.join(CSRC, f)
                   for f in ("pkv_decode_balanced.cu", "pkv_decode_common.cuh", "pkv_device.cuh",
                             "pkv_tensor_map.cu")]
 WRITE_SOURCES = [os.path.join(CSRC, "pkv_write.cu")]
+CHUNK_SOURCES = [os.path.join(CSRC, f)
+                 for f in ("pkv_chunk.cu", "pkv_tcgen05.cuh", "pkv_device.cuh",
+                           "pkv_decode_common.cuh", "pkv_decode_host.h", "pkv_tensor_map.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_dram_traffic.txt")
 WRITE_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cache_write_kernel_dram_traffic.txt")
+CHUNK_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chunk_attention_kernel_dram_traffic.txt")
 
 
 def parse(argv=None):
@@ -181,6 +185,10 @@ def write_source_hash() -> str:
     return source_hash(WRITE_SOURCES)
 
 
+def chunk_source_hash() -> str:
+    return source_hash(CHUNK_SOURCES)
+
+
 def _read_record(path: str, current_hash: str) -> dict:
     """key = value lines of a committed ncu summary, or {} when the file is
     missing or was taken on other kernel sources than the current ones."""
@@ -206,6 +214,14 @@ def recorded_traffic(workload_key: str):
 def recorded_decode_value(key: str):
     """Another figure of the decode ncu record (e.g. an L2 hit rate), same gate."""
     v = _read_record(TRAFFIC_FILE, decode_source_hash()).get(key)
+    return float(v) if v else None
+
+
+def recorded_chunk_traffic(workload_key: str):
+    """DRAM bytes per tile-kernel launch from its committed ncu summary, if it
+    was taken on the current tile kernel source (else None)."""
+    v = _read_record(CHUNK_TRAFFIC_FILE, chunk_source_hash()).get(
+        f"traffic_bytes_per_launch.{workload_key}")
     return float(v) if v else None
 
 
@@ -745,6 +761,8 @@ def chunk_entry(key, wl, m, peak, peak_kind):
     if key.endswith(".chunk"):
         roof["kernel"] = ("attention call = chunk_plan_kernel (one CTA) + chunk_attention_kernel "
                           "(tcgen05) on every SM")
+        # DRAM bytes of the dominant kernel, the tile kernel (ncu record)
+        roof["traffic"] = recorded_chunk_traffic("config6.chunk")
     return {
         "workload": CHUNK_ONLY_NAME if key.endswith(".chunk") else WORKLOAD_NAMES[int(key)],
         "value": round(wl.kv_bytes() / (st["median"] * 1e-3) / 1e9, 2), "unit": UNIT,
@@ -889,6 +907,8 @@ def main_chunk(args, wl, rank, world, local):
         return
     peak_hbm, peak_kind = measured_peaks()
     roof, attn_ms = chunk_roofline(wl, m, peak_hbm, peak_kind)
+    if args.chunk_only:
+        roof["traffic"] = recorded_chunk_traffic("config6.chunk")
     kv_bytes = wl.kv_bytes()
     Tq = wl.q.shape[0]
     cpu = None

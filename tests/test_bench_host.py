@@ -95,3 +95,20 @@ def test_unique_kv_bytes_of_the_shared_prefix_workload():
     # in the third block of each sequence, the last of which holds the new token)
     rows = 32 + (40 - 32) + (50 - 32 - 16) + 16 + (35 - 32)
     assert bench.unique_kv_bytes(wl) == rows * 2 * 64 * 4
+
+
+def test_chunk_traffic_record_gated_by_chunk_source(monkeypatch):
+    monkeypatch.setattr(bench, "chunk_source_hash", lambda: "0" * 16)
+    assert bench.recorded_chunk_traffic("config6.chunk") is None
+
+
+def test_chunk_traffic_record_reads_the_inputs_once():
+    got = bench.recorded_chunk_traffic("config6.chunk")
+    if got is None:
+        pytest.skip("traffic record taken on other tile-kernel sources (re-capture with ncu)")
+    # the 3000-token prompt's keys and values (bs 16, Hk 8, D 128, fp16) and
+    # the 952 chunk tokens' query rows (H 32): each read once from DRAM; the
+    # output may stay in L2
+    kv = 2 * 3000 * 8 * 128 * 2
+    q = 952 * 32 * 128 * 2
+    assert kv + q <= got <= 1.1 * (kv + q)
