@@ -763,6 +763,9 @@ def chunk_entry(key, wl, m, peak, peak_kind):
                           "(tcgen05) on every SM")
         # DRAM bytes of the dominant kernel, the tile kernel (ncu record)
         roof["traffic"] = recorded_chunk_traffic("config6.chunk")
+    elif key == "7":
+        # the call is the balanced schedule alone (query-column mode)
+        roof["traffic"] = recorded_traffic("config7.fp16")
     return {
         "workload": CHUNK_ONLY_NAME if key.endswith(".chunk") else WORKLOAD_NAMES[int(key)],
         "value": round(wl.kv_bytes() / (st["median"] * 1e-3) / 1e9, 2), "unit": UNIT,
@@ -909,6 +912,8 @@ def main_chunk(args, wl, rank, world, local):
     roof, attn_ms = chunk_roofline(wl, m, peak_hbm, peak_kind)
     if args.chunk_only:
         roof["traffic"] = recorded_chunk_traffic("config6.chunk")
+    elif args.config == 7:
+        roof["traffic"] = recorded_traffic("config7.fp16")
     kv_bytes = wl.kv_bytes()
     Tq = wl.q.shape[0]
     cpu = None

@@ -14,7 +14,9 @@ import bench  # noqa: E402
 
 # algorithmic bytes per decode launch of the Llama-8B decode layer (S=64,
 # L~U[256,4096], Hk 8, D 128): K+V rows, q, out, block tables, lengths
-ALGORITHMIC = {"config2.fp16": 545_891_164, "config2.fp8": 281_999_324}
+ALGORITHMIC = {"config2.fp16": 545_891_164, "config2.fp8": 281_999_324,
+               # draft verification (64 x 4 new tokens, query-column mode)
+               "config7.fp16": 614_122_464}
 
 
 @pytest.mark.parametrize("key", sorted(ALGORITHMIC))
